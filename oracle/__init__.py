@@ -1,0 +1,1 @@
+"""The fp64 CPU oracle: test infrastructure only (never imported by the product path)."""
