@@ -1,0 +1,389 @@
+"""Benchmark of the verifier step on GB300.
+
+One step = one pass of the whole hot path at the M=5 verifier shapes:
+  (1) the Q2B32 verifier linear K=N=4096 at M=5 (q2_tiny_gemm),
+  (2) the routed MoE FFN, 64 experts, H=4096, F=2048, top-6 over the same 5 rows
+      (q2_moe_grouped),
+  (3) the p/q verify of 3 sessions x 4 drafts over V=129280 (pq_verify).
+Inputs are seeded synthetic tensors (see speculative_decode_verifier_gb300.synth); weights
+are random, not trained.  Device timing replays one CUDA graph per input set, rotating over
+4 sets, so every step touches > 250 MB (more than the 126 MB L2).
+
+Prints one JSON line.  `value` is the device-timed step time in microseconds (inputs resident
+in HBM); `e2e` is the same step through the Python binding with pinned host buffers copied
+in and results copied out inside the timed region.  `--impl reference` times the fp64 CPU
+oracle on the host cores instead (the only place this file runs the oracle besides the
+cpu_baseline leg).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from speculative_decode_verifier_gb300 import synth  # noqa: E402
+
+METRIC = "verifier step µs & Q2B32 GEMM HBM GB/s (% peak) at M=5; pq_verify rows/s"
+WORKLOAD = ("verifier step at M=5: Q2B32 linear K=N=4096 M=5 + routed MoE FFN 64 experts "
+            "H=4096 F=2048 top-6 M=5 + pq_verify S=3 k=4 V=129280 T=1")
+N_SETS = 4
+LAUNCHES_PER_STEP = 2 + 6 + 2   # prep+gemm; route, prep X, gate/up, prep h, down, combine; stats+verify
+EXPERT_BYTES = 3 * 2048 * (4096 // 32) * 12   # gate + up + down of one expert
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+# ----------------------------------------------------------------------------- inputs
+
+def make_inputs(set_id: int):
+    g = synth.config_gemm(1, salt=set_id)
+    m = synth.config_moe(2, salt=set_id)
+    v = synth.config_verify(3, salt=set_id)
+    return g, m, v
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={gpu_index}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], None, set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx = float(parts[2])
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ----------------------------------------------------------------------------- device arm
+
+def run_device(args, rank: int, world: int):
+    import torch
+    from speculative_decode_verifier_gb300 import build, q2v
+    build.build()
+    q2v.load()
+    dev = torch.device("cuda", int(os.environ.get("LOCAL_RANK", 0)))
+    torch.cuda.set_device(dev)
+
+    def D(a):
+        a = np.ascontiguousarray(a)
+        if a.dtype == np.uint16:
+            a = a.view(np.int16)
+        return torch.from_numpy(a).to(dev)
+
+    # resident inputs, N_SETS rotating sets
+    sets = []
+    for i in range(N_SETS):
+        g, m, v = make_inputs(i)
+        sets.append(dict(
+            W=D(g["W"].reshape(-1)), A=D(g["A"]), X=D(m["X"]), R=D(m["router"]),
+            T=D(v["target"]), Dl=D(v["draft"]), x=D(v["drafts"]), ua=D(v["u_acc"]), uf=D(v["u_fin"]),
+            host=dict(A=g["A"], X=m["X"], R=m["router"], T=v["target"], Dl=v["draft"], x=v["drafts"],
+                      ua=v["u_acc"], uf=v["u_fin"])))
+        if i == 0:
+            moe_w = {k: D(m[k].reshape(-1)) for k in ("Wg", "Wu", "Wd")}
+            shapes = dict(N=g["N"], K=g["K"], M=g["M"], E=m["E"], H=m["H"], F=m["F"], topk=m["topk"],
+                          S=v["target"].shape[0], k=v["target"].shape[1] - 1, V=v["target"].shape[2])
+    sh = shapes
+    Y1 = torch.empty((sh["M"], sh["N"]), dtype=torch.float32, device=dev)
+    Y2 = torch.empty((sh["M"], sh["H"]), dtype=torch.float32, device=dev)
+    ids = torch.empty((sh["M"], sh["topk"]), dtype=torch.int32, device=dev)
+    gw = torch.empty((sh["M"], sh["topk"]), dtype=torch.float32, device=dev)
+    n_acc = torch.empty(sh["S"], dtype=torch.int32, device=dev)
+    toks = torch.empty((sh["S"], sh["k"] + 1), dtype=torch.int32, device=dev)
+    ws1 = q2v.workspace(q2v.q2_tiny_gemm_workspace(sh["M"], sh["N"], sh["K"]), dev)
+    ws2 = q2v.workspace(q2v.q2_moe_grouped_workspace(sh["M"], sh["E"], sh["topk"], sh["H"], sh["F"]), dev)
+    ws3 = q2v.workspace(q2v.pq_verify_workspace(sh["S"], sh["k"], sh["V"]), dev)
+
+    def part_gemm(s):
+        q2v.q2_tiny_gemm(s["W"], sh["N"], sh["K"], s["A"], Y=Y1, ws=ws1)
+
+    def part_moe(s):
+        q2v.q2_moe_grouped(moe_w["Wg"], moe_w["Wu"], moe_w["Wd"], sh["E"], sh["H"], sh["F"], sh["topk"], s["X"],
+                           s["R"], Y=Y2, ids_out=ids, w_out=gw, ws=ws2)
+
+    def part_pq(s):
+        q2v.pq_verify(s["T"], s["Dl"], s["x"], s["ua"], s["uf"], 1.0, n_acc=n_acc, tokens=toks, ws=ws3)
+
+    def step(s):
+        part_gemm(s)
+        part_moe(s)
+        part_pq(s)
+
+    # eager warm-up (also caches device attributes before any capture) and routing facts
+    active = []
+    for s in sets:
+        step(s)
+        torch.cuda.synchronize()
+        active.append(int(torch.unique(ids).numel()))
+    for w in (ws1, ws2, ws3):
+        st = q2v.q2_get_device_status(w)
+        assert st == 0, f"device status {st} after warm-up"
+
+    def capture(fn):
+        graphs = []
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            for s in sets:
+                fn(s)
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        for s in sets:
+            gr = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(gr):
+                fn(s)
+            graphs.append(gr)
+        torch.cuda.synchronize()
+        return graphs
+
+    def timed(graphs, steps, warmup, clocks=False):
+        for i in range(warmup):
+            graphs[i % N_SETS].replay()
+        torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        sampler = ClockSampler(dev.index) if clocks else None
+        if clocks:
+            time.sleep(0.25)
+        torch.cuda.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record()
+        reps = steps
+        for i in range(reps):
+            graphs[i % N_SETS].replay()
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        # keep the clock sampler running over a few more replays so it sees load
+        if clocks:
+            t_end = time.time() + 0.6
+            while time.time() < t_end:
+                for i in range(N_SETS):
+                    graphs[i].replay()
+                torch.cuda.synchronize()
+        if world > 1:
+            torch.distributed.barrier()
+        ck = sampler.stop() if sampler else None
+        return ms / reps * 1000.0, ck
+
+    g_step = capture(step)
+    step_us, clocks = timed(g_step, args.steps, args.warmup, clocks=True)
+    if world > 1:
+        t = torch.tensor([step_us], device=dev)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        step_us = float(t.item())
+    gemm_us, _ = timed(capture(part_gemm), args.steps, args.warmup)
+    moe_us, _ = timed(capture(part_moe), args.steps, args.warmup)
+    pq_us, _ = timed(capture(part_pq), args.steps, args.warmup)
+
+    # e2e: through the binding, pinned host inputs in, results out, every step
+    pin = []
+    for s in sets:
+        h = {k: torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).pin_memory()
+             for k, a in s["host"].items()}
+        pin.append(h)
+    out_host = dict(Y1=torch.empty_like(Y1, device="cpu").pin_memory(), Y2=torch.empty_like(Y2, device="cpu").pin_memory(),
+                    n=torch.empty_like(n_acc, device="cpu").pin_memory(),
+                    t=torch.empty_like(toks, device="cpu").pin_memory())
+    h2d = sum(t.numel() * t.element_size() for t in pin[0].values())
+    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
+    dev_in = [dict(A=torch.empty_like(s["A"]), X=torch.empty_like(s["X"]), R=torch.empty_like(s["R"]),
+                   T=torch.empty_like(s["T"]), Dl=torch.empty_like(s["Dl"]), x=torch.empty_like(s["x"]),
+                   ua=torch.empty_like(s["ua"]), uf=torch.empty_like(s["uf"]), W=s["W"]) for s in sets]
+
+    def e2e_step(i):
+        s = dev_in[i % N_SETS]
+        h = pin[i % N_SETS]
+        for key in ("A", "X", "R", "T", "Dl", "x", "ua", "uf"):
+            s[key].copy_(h[key], non_blocking=True)
+        step(s)
+        out_host["Y1"].copy_(Y1, non_blocking=True)
+        out_host["Y2"].copy_(Y2, non_blocking=True)
+        out_host["n"].copy_(n_acc, non_blocking=True)
+        out_host["t"].copy_(toks, non_blocking=True)
+
+    for i in range(args.warmup):
+        e2e_step(i)
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for i in range(args.steps):
+        e2e_step(i)
+    e1.record()
+    torch.cuda.synchronize()
+    e2e_us = e0.elapsed_time(e1) / args.steps * 1000.0
+
+    peak, peak_kind = _peaks()
+    gemm_bytes = sh["N"] * (sh["K"] // 32) * 12 + sh["M"] * sh["K"] * 2 + sh["M"] * sh["N"] * 4
+    pq_bytes = (sh["S"] * (2 * sh["k"] + 1) * sh["V"] * 4 + sh["S"] * sh["k"] * 8 + sh["S"] * 4
+                + sh["S"] * (sh["k"] + 2) * 4)
+    moe_bytes = statistics.mean(active) * EXPERT_BYTES + sh["M"] * sh["H"] * (2 + 4) + sh["M"] * sh["E"] * 4
+    gemm_gbs = gemm_bytes / (gemm_us * 1e-6) / 1e9
+    moe_gbs = moe_bytes / (moe_us * 1e-6) / 1e9
+    pq_gbs = pq_bytes / (pq_us * 1e-6) / 1e9
+    parts = {
+        "q2_tiny_gemm": {"us": gemm_us, "bytes": gemm_bytes, "GB/s": gemm_gbs, "frac": gemm_gbs / peak},
+        "q2_moe_grouped": {"us": moe_us, "bytes": moe_bytes, "active_experts": statistics.mean(active),
+                           "GB/s": moe_gbs, "frac": moe_gbs / peak},
+        "pq_verify": {"us": pq_us, "bytes": pq_bytes, "GB/s": pq_gbs, "frac": pq_gbs / peak,
+                      "rows_per_s": sh["S"] * (sh["k"] + 1) / (pq_us * 1e-6),
+                      "draft_rows_per_s": sh["S"] * sh["k"] / (pq_us * 1e-6)},
+    }
+    traffic = None
+    tfile = os.path.join(ROOT, "profiles", "traffic.json")
+    if os.path.exists(tfile):
+        try:
+            traffic = json.load(open(tfile)).get("q2_moe_grouped")
+        except Exception:
+            traffic = None
+    line = {
+        "metric": METRIC, "value": step_us, "unit": "µs", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": step_us / 1000.0, "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "q2b32 weights, bf16->f16 operands, fp32 accumulate/logits",
+        "data": "synthetic (seeded; random weights)",
+        "config": {"workload": WORKLOAD, "sets": N_SETS,
+                   "l2": "inputs larger than L2: 4 rotating input sets, > 250 MB touched per step",
+                   "parallelism": "replicas" if world > 1 else "single GPU", "graph": "one CUDA graph per step"},
+        "q2_gemm_m5_GB/s": gemm_gbs, "q2_gemm_m5_frac_of_measured_peak": gemm_gbs / peak,
+        "q2_gemm_m5_frac_of_8TBs": gemm_gbs / 8000.0,
+        "pq_verify_rows_per_s": parts["pq_verify"]["rows_per_s"],
+        "parts": parts,
+        "roofline": {"bound": "hbm", "kernel": "q2_moe_grouped (the MoE FFN call; grouped dequant GEMMs dominate)",
+                     "achieved": moe_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": moe_gbs / peak, "traffic": traffic},
+        "e2e": {"value": e2e_us, "unit": "µs", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "clocks": clocks,
+    }
+    return line
+
+
+# ----------------------------------------------------------------------------- oracle arm
+
+def _oracle_step(g, m, v, frac: float, threads: int):
+    """One oracle pass over a `frac` sample of the step (leading output rows of the linear and
+    of each expert projection are not separable in the oracle, so the sample is: the linear on
+    frac*N rows, the MoE on ceil(frac*M) rows, pq_verify on all sessions)."""
+    from oracle import oracle
+    n = max(16, int(g["N"] * frac))
+    rows = g["W"][:n]
+    t0 = time.perf_counter()
+    oracle.gemm(rows, n, g["K"], g["A"], threads=threads)
+    t1 = time.perf_counter()
+    mrows = 1
+    oracle.moe(m["Wg"], m["Wu"], m["Wd"], m["E"], m["H"], m["F"], m["topk"], m["X"][:mrows], m["router"][:mrows],
+               threads=threads)
+    t2 = time.perf_counter()
+    oracle.pq_verify(v["target"], v["draft"], v["drafts"], v["u_acc"], v["u_fin"], v["T"], threads=threads)
+    t3 = time.perf_counter()
+    # scale each part to the full workload
+    return (t1 - t0) * g["N"] / n + (t2 - t1) * m["M"] / mrows + (t3 - t2)
+
+
+def run_oracle(steps: int, warmup: int):
+    from oracle import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    g, m, v = make_inputs(0)
+    frac = 0.25
+    for _ in range(max(0, min(warmup, 1))):
+        _oracle_step(g, m, v, frac, threads)
+    times = [_oracle_step(g, m, v, frac, threads) for _ in range(steps)]
+    us = statistics.mean(times) * 1e6
+    return us, threads, (f"per step: the linear on 25% of its 4096 output rows, the MoE FFN on 1 of 5 rows "
+                         f"(all 6 experts of that row), pq_verify on all 3 sessions; times scaled to the "
+                         f"full step; fp64; {threads} OpenMP threads")
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(args.warmup, 3)
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+
+    if args.impl == "reference":
+        if rank != 0:
+            return
+        us, cores, sample = run_oracle(max(1, min(args.steps, 5)), 1)
+        print(json.dumps({
+            "impl": "reference", "metric": METRIC, "value": us, "unit": "µs", "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1000.0, "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; random weights)",
+            "config": {"workload": WORKLOAD},
+            "cpu_baseline": {"value": us, "unit": "µs", "cores": cores, "kind": "oracle", "sample": sample},
+            "e2e": {"value": us, "unit": "µs", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }))
+        return
+
+    if world > 1:
+        import torch
+        torch.distributed.init_process_group("nccl")
+    line = run_device(args, rank, world)
+    if rank == 0:
+        if not args.no_cpu_baseline and world == 1:
+            us, cores, sample = run_oracle(1, 0)
+            line["cpu_baseline"] = {"value": us, "unit": "µs", "cores": cores, "kind": "oracle", "sample": sample}
+        print(json.dumps(line))
+    if world > 1:
+        import torch
+        torch.distributed.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,185 @@
+/*
+ * q2v.h -- C ABI of libq2v, the GB300 (sm_103a) target-verifier step of lossless p/q
+ * speculative decoding.
+ *
+ * The verifier of a speculative-decoding cycle runs the target model over K+1 rows
+ * (one committed row and K draft rows) and then accepts or replaces the drafts
+ * ("Optimizing DeepSeek-V4-Flash on a single NVIDIA GB10/GX10 with DSpark speculative
+ * decoding", page 1, opening post, "Current results": the verifier takes about 148 ms
+ * of a 169 ms cycle at about 5 target rows; page 2, the verifier-bottleneck reply: the
+ * verify executes attention, routed MoE, projections and the vocabulary head over the
+ * K+1 rows).  This library provides the two hot parts of that step:
+ *
+ *   q2_tiny_gemm     Y = A W^T for 1..64 activation rows against Q2B32 weights
+ *                    (dense projections and the vocabulary head);
+ *   q2_moe_grouped   the routed-expert FFN over the same rows (device routing,
+ *                    fused gate+up+SiLU, down projection, weighted combine);
+ *   pq_verify        the exact p/q rejection-sampling verify over target and draft
+ *                    logits.
+ *
+ * Q2B32 weight format (a stand-in for the 2-bit GGUF formats that the pages name but
+ * do not define): blocks of 32 consecutive weights of one row along K, 12 bytes each:
+ * bytes 0..7 hold the 32 two-bit unsigned codes q, four per byte, low bits first
+ * (code j in byte j/4, bits 2(j%4)..2(j%4)+1); bytes 8..9 an fp16 scale d; bytes
+ * 10..11 an fp16 offset m (little-endian).  w = d*q + m.  A matrix with N rows and K
+ * columns is N*(K/32) blocks, row-major over N, the K/32 blocks of a row contiguous.
+ *
+ * Conventions for every entry point:
+ *  - All tensor pointers are DEVICE pointers owned by the caller.  The library never
+ *    allocates, frees or synchronises on the enqueue path; every call only enqueues
+ *    kernels on `stream` and returns.
+ *  - Workspace: each call takes a caller-owned device workspace of at least the size
+ *    its *_workspace() query returns (16-byte aligned).  The first 256 bytes hold a
+ *    device status word shared by all calls on that workspace; each call initialises
+ *    the rest of the scratch it uses.  Calls that share a workspace must be ordered
+ *    on one stream.
+ *  - Errors found on the host (bad sizes, NULL or misaligned pointers, too small a
+ *    workspace) are returned before anything is enqueued.  Errors found on the device
+ *    (a draft token out of range, a weight scale outside the exact range) are recorded
+ *    in the workspace's status word; the affected outputs are then unspecified.  Read
+ *    and clear the word with q2_get_device_status().  No kernel traps, asserts or
+ *    waits without a bound.
+ */
+#ifndef Q2V_H
+#define Q2V_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream (cudaStream_t); 0 is the legacy default stream. */
+typedef struct CUstream_st *q2_stream_t;
+
+typedef enum {
+    Q2_OK = 0,
+    Q2_ERR_INVALID_ARG = 1, /* a size, count, pointer or temperature is invalid           */
+    Q2_ERR_ALIGNMENT = 2,   /* a pointer or leading dimension breaks the alignment rules   */
+    Q2_ERR_UNSUPPORTED = 3, /* valid, but outside the sizes this build implements          */
+    Q2_ERR_WORKSPACE = 4,   /* workspace NULL, misaligned or smaller than the query        */
+    Q2_ERR_CUDA = 5,        /* a CUDA runtime call (launch, attribute, copy) failed        */
+    Q2_ERR_TIMEOUT = 6,     /* a bounded device-side wait gave up                          */
+    Q2_ERR_BAD_TOKEN = 7,   /* device: a draft token is outside [0, V)                     */
+    Q2_ERR_RANGE = 8        /* device: a Q2B32 scale |d| > 16376 (outside the exact path)  */
+} q2_status;
+
+#define Q2_WORKSPACE_HEADER_BYTES 256
+
+/* ------------------------------------------------------------------ tiny GEMM */
+
+/* Workspace bytes for q2_tiny_gemm with these sizes (>= Q2_WORKSPACE_HEADER_BYTES). */
+size_t q2_tiny_gemm_workspace(int M, int N, int K);
+
+/*
+ * Y[m][n] = sum_k A[m][k] * w[n][k]  for m < M, n < N   (Y = A W^T, fp32 out).
+ *
+ * The "projections and the vocabulary head" of the K+1-row verify (page 2 of the
+ * thread above, verifier-bottleneck reply) with the tiny-batch matmul shapes of
+ * post #1 (K+1 = 1..5 rows per session; up to 12 sessions batched in the cohort
+ * post #20 describes).
+ *
+ *   W    Q2B32 weights of an [N,K] matrix: N*(K/32)*12 bytes, 16-byte aligned.
+ *   N    output features, 1 <= N.          K   reduction length, K % 32 == 0, 32 <= K <= 8192.
+ *   A    bf16 activations [M][lda] (row-major), 16-byte aligned, lda >= K, lda % 8 == 0.
+ *   M    activation rows, 1 <= M <= 64.
+ *   Y    fp32 output [M][ldy], ldy >= N, 4-byte aligned.  Fully overwritten for n < N.
+ *   ws   workspace of q2_tiny_gemm_workspace(M,N,K) bytes.
+ * Accumulation is fp32; each product uses the weight rounded to fp16 once (q*d) and the
+ * offset m exactly, and activations converted to fp16 under an exact per-row power-of-two
+ * scale, so |Y - exact| stays far below 2e-3 * sum_k |a_k w_k|.
+ * Device errors: Q2_ERR_RANGE if a block has |d| > 16376.
+ */
+q2_status q2_tiny_gemm(const void *W, int N, int K, const uint16_t *A, int M, int lda,
+                       float *Y, int ldy, void *ws, size_t ws_bytes, q2_stream_t stream);
+
+/* ------------------------------------------------------------------ routed MoE */
+
+/* Workspace bytes for q2_moe_grouped with these sizes. */
+size_t q2_moe_grouped_workspace(int M, int E, int topk, int H, int F);
+
+#define Q2_MOE_RENORMALIZE 1u /* divide the selected gate probabilities by their sum */
+
+/*
+ * Routed-expert FFN over M rows (the "routed MoE" of the K+1-row verify; the fused
+ * router, fused gate+up+SwiGLU decode and expert dedup named in "1x Spark tuned
+ * DSpark for DeepSeek-V4-Flash ...", reply on the decode arc, and "ds4-on-spark",
+ * section "What the fork adds": "MoE gate_up expert dedup"):
+ *
+ *   prob[r] = softmax(router_logits[r][0..E));  top-`topk` experts by probability,
+ *   ties to the lower expert index;  g = the selected probabilities (renormalised to
+ *   sum 1 only when flags has Q2_MOE_RENORMALIZE);
+ *   h = silu(x Wg_e^T) * (x Wu_e^T)  (silu(z) = z / (1 + e^-z)),   out = h Wd_e^T;
+ *   Y[r] = sum over the selected slots, in descending-probability order, of g * out.
+ *
+ * Each active expert's weights are read once for all rows routed to it.
+ *   Wg, Wu  Q2B32 [E][F rows][H/32 blocks];  Wd  Q2B32 [E][H rows][F/32 blocks]; 16-B aligned.
+ *   E <= 256 experts, 1 <= topk <= min(E, 16), H and F multiples of 32, 32 <= H, F <= 8192.
+ *   X       bf16 [M][H], 16-byte aligned, 1 <= M <= 64.
+ *   router_logits fp32 [M][E].
+ *   Y       fp32 [M][H] (overwritten).
+ *   topk_ids_out int32 [M][topk], topk_w_out fp32 [M][topk]: optional (NULL to skip).
+ *   flags   0 or Q2_MOE_RENORMALIZE.
+ * Device errors: Q2_ERR_RANGE as for q2_tiny_gemm.
+ */
+q2_status q2_moe_grouped(const void *Wg, const void *Wu, const void *Wd, int E, int H, int F,
+                         int topk, unsigned flags, const uint16_t *X, int M,
+                         const float *router_logits, float *Y, int32_t *topk_ids_out,
+                         float *topk_w_out, void *ws, size_t ws_bytes, q2_stream_t stream);
+
+/* ------------------------------------------------------------------ p/q verify */
+
+/* Workspace bytes for pq_verify with these sizes. */
+size_t pq_verify_workspace(int S, int k, int V);
+
+/*
+ * Exact p/q rejection-sampling verify for S independent sessions of k drafts each
+ * ("Optimizing DeepSeek-V4-Flash ...", page 1, opening post: drafts are sampled from
+ * q, the target defines p, accepted tokens follow min(1, p(x)/q(x)), rejected drafts
+ * are replaced from the positive residual distribution; posts #12 and #20: "exact
+ * residual correction"; "1x Spark tuned DSpark ...", deep-dive, "On losslessness":
+ * the verify rows are the only token source, drawn with the request's own sampler).
+ *
+ * For session s:  p_i = softmax(target[s][i] / T) (i = 0..k),  q_i = softmax(draft[s][i] / T)
+ * (i < k).  For i = 0..k-1 with x_i = draft_tokens[s][i]: accept iff q_i(x_i) == 0 or
+ * u_acc[s][i] < p_i(x_i) / q_i(x_i); stop at the first rejection j.  If j < k, draw y
+ * from max(0, p_j - q_j) normalised (from p_j if that mass is zero); if all k are
+ * accepted, draw the extra token y from p_k.  A draw takes the smallest token y (in
+ * ascending index) whose cumulative mass exceeds u_fin[s] times the total.
+ *
+ *   target_logits fp32 [S][k+1][V];  draft_logits fp32 [S][k][V] (NULL allowed when k == 0);
+ *                 both 16-byte aligned.
+ *   draft_tokens  int32 [S][k], each must lie in [0, V) (else device Q2_ERR_BAD_TOKEN).
+ *   u_acc fp32 [S][k], u_fin fp32 [S]: uniforms in [0, 1), supplied by the caller's
+ *                 per-session RNG.
+ *   S >= 1, 0 <= k <= 16, 1 <= V <= 2^28, temperature > 0 and finite.
+ *   n_accepted    int32 [S]: j, in [0, k].
+ *   out_tokens    int32 [S][k+1]: x_0..x_{j-1}, y, then -1.
+ *   probs_out     optional fp32 [S][2k+1][V]: rows p_0..p_k then q_0..q_{k-1} (for tests).
+ * Arithmetic is fp32 with fp64 cross-chunk sums; tokens equal the exact (fp64) result
+ * except when a uniform lies within about 1e-6 of a decision boundary.
+ */
+q2_status pq_verify(const float *target_logits, const float *draft_logits,
+                    const int32_t *draft_tokens, const float *u_acc, const float *u_fin,
+                    int S, int k, int V, float temperature, int32_t *n_accepted,
+                    int32_t *out_tokens, float *probs_out, void *ws, size_t ws_bytes,
+                    q2_stream_t stream);
+
+/* ------------------------------------------------------------------ status */
+
+/* Synchronise `stream`, read the device status word of workspace `ws`, clear it, and
+ * return it (Q2_OK if no device error was recorded since the last read). */
+q2_status q2_get_device_status(const void *ws, q2_stream_t stream);
+
+/* Static description of a status code. */
+const char *q2_status_string(q2_status status);
+
+/* Library version: major*10000 + minor*100 + patch. */
+int q2_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* Q2V_H */

@@ -1,0 +1,265 @@
+// q2v_api.cu -- the extern "C" boundary of libq2v: argument checks, workspace carving
+// and kernel dispatch.  Nothing here allocates, frees or synchronises except
+// q2_get_device_status, whose job is to read the device status word.
+#include <math.h>
+#include <stdio.h>
+
+#include "q2v_kernels.cuh"
+
+using namespace q2v;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+int g_sms[kMaxDevices];  // cached SM count per device (0 = unknown)
+
+int device_sms() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    if (g_sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) n = 148;
+        g_sms[dev] = n;
+    }
+    return g_sms[dev];
+}
+
+bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+unsigned int *status_word(void *ws) { return &static_cast<WsHeader *>(ws)->status; }
+
+// Sequential carve of 256-byte-aligned regions after the header.
+struct Carver {
+    char *base;
+    size_t off;
+    explicit Carver(void *ws) : base(static_cast<char *>(ws)), off(Q2_WORKSPACE_HEADER_BYTES) {}
+    void *take(size_t bytes) {
+        void *p = base ? base + off : nullptr;
+        off += align_up(bytes, 256);
+        return p;
+    }
+};
+
+q2_status check_ws(void *ws, size_t ws_bytes, size_t need) {
+    if (!ws || !aligned(ws, 16) || ws_bytes < need) return Q2_ERR_WORKSPACE;
+    return Q2_OK;
+}
+
+q2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? Q2_OK : Q2_ERR_CUDA; }
+
+// ---------------------------------------------------------------- tiny GEMM sizes
+
+bool gemm_k_ok(int K) { return K >= kBlockK && K % kBlockK == 0 && K <= kMaxTileWarps * kTileBlocks * kBlockK; }
+
+size_t gemm_ws_bytes(int M, int K) {
+    Carver c(nullptr);
+    c.take(PrepLayout(K).bytes(M));
+    return c.off;
+}
+
+// ---------------------------------------------------------------- pq_verify sizes
+
+int pq_cmax(int V) { return std::min(cdiv(V, kChunkAlign), kMaxChunks); }
+
+struct PqCarve {
+    float *stats;
+    double *mass, *pmass;
+    unsigned int *tickets;
+    size_t bytes;
+};
+
+PqCarve pq_carve(void *ws, int S, int k, int V) {
+    Carver c(ws);
+    PqCarve r{};
+    const size_t R = 2 * (size_t)k + 1, C = pq_cmax(V);
+    r.stats = static_cast<float *>(c.take((size_t)S * R * C * 2 * sizeof(float)));
+    r.mass = static_cast<double *>(c.take((size_t)S * C * sizeof(double)));
+    r.pmass = static_cast<double *>(c.take((size_t)S * C * sizeof(double)));
+    r.tickets = static_cast<unsigned int *>(c.take((size_t)S * sizeof(unsigned int)));
+    r.bytes = c.off;
+    return r;
+}
+
+// ---------------------------------------------------------------- MoE sizes
+
+struct MoeCarve {
+    MoeWs w;
+    size_t bytes;
+};
+
+MoeCarve moe_carve(void *ws, int M, int E, int topk, int H, int F) {
+    Carver c(ws);
+    MoeCarve r{};
+    const size_t P = (size_t)M * topk;
+    r.w.counts = static_cast<int *>(c.take((size_t)E * sizeof(int)));
+    r.w.offsets = static_cast<int *>(c.take((size_t)(E + 1) * sizeof(int)));
+    r.w.active = static_cast<int *>(c.take((size_t)(E + 1) * sizeof(int)));
+    r.w.pair_row = static_cast<int *>(c.take(P * sizeof(int)));
+    r.w.pair_of = static_cast<int *>(c.take(P * sizeof(int)));
+    r.w.gate_w = static_cast<float *>(c.take(P * sizeof(float)));
+    r.w.h = static_cast<float *>(c.take(2 * P * (size_t)F * sizeof(float)));
+    r.w.out = static_cast<float *>(c.take(P * (size_t)H * sizeof(float)));
+    const PrepLayout LX(H), LH(F);
+    void *px = c.take(LX.bytes(M));
+    void *ph = c.take(LH.bytes((int)P));
+    if (ws) {
+        r.w.prepX = PrepPtrs::carve(px, LX, M);
+        r.w.prepH = PrepPtrs::carve(ph, LH, (int)P);
+    }
+    r.bytes = c.off;
+    return r;
+}
+
+}  // namespace
+
+extern "C" {
+
+int q2_version(void) { return Q2V_VERSION; }
+
+const char *q2_status_string(q2_status s) {
+    switch (s) {
+        case Q2_OK: return "ok";
+        case Q2_ERR_INVALID_ARG: return "invalid argument";
+        case Q2_ERR_ALIGNMENT: return "misaligned pointer or leading dimension";
+        case Q2_ERR_UNSUPPORTED: return "unsupported size";
+        case Q2_ERR_WORKSPACE: return "workspace missing, misaligned or too small";
+        case Q2_ERR_CUDA: return "CUDA runtime error";
+        case Q2_ERR_TIMEOUT: return "device wait timed out";
+        case Q2_ERR_BAD_TOKEN: return "draft token out of range";
+        case Q2_ERR_RANGE: return "Q2B32 scale outside the exact range";
+    }
+    return "unknown status";
+}
+
+q2_status q2_get_device_status(const void *ws, q2_stream_t stream) {
+    if (!ws || !aligned(ws, 16)) return Q2_ERR_WORKSPACE;
+    unsigned int st = 0;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemcpyAsync(&st, ws, sizeof(st), cudaMemcpyDeviceToHost, s) != cudaSuccess) return Q2_ERR_CUDA;
+    if (cudaStreamSynchronize(s) != cudaSuccess) return Q2_ERR_CUDA;
+    if (st != 0) {
+        if (cudaMemsetAsync(const_cast<void *>(ws), 0, sizeof(st), s) != cudaSuccess) return Q2_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return Q2_ERR_CUDA;
+    }
+    return static_cast<q2_status>(st);
+}
+
+// ---------------------------------------------------------------- tiny GEMM
+
+size_t q2_tiny_gemm_workspace(int M, int N, int K) {
+    (void)N;
+    if (M < 1 || M > 64 || !gemm_k_ok(K)) return Q2_WORKSPACE_HEADER_BYTES;
+    return gemm_ws_bytes(M, K);
+}
+
+q2_status q2_tiny_gemm(const void *W, int N, int K, const uint16_t *A, int M, int lda, float *Y, int ldy,
+                       void *ws, size_t ws_bytes, q2_stream_t stream) {
+    if (!W || !A || !Y || N < 1 || M < 1 || K < kBlockK || K % kBlockK != 0 || lda < K || ldy < N)
+        return Q2_ERR_INVALID_ARG;
+    if (M > 64 || !gemm_k_ok(K)) return Q2_ERR_UNSUPPORTED;
+    if (!aligned(W, 16) || !aligned(A, 16) || lda % 8 != 0 || !aligned(Y, 4)) return Q2_ERR_ALIGNMENT;
+    const q2_status wst = check_ws(ws, ws_bytes, gemm_ws_bytes(M, K));
+    if (wst != Q2_OK) return wst;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    Carver c(ws);
+    const PrepLayout L(K);
+    const PrepPtrs P = PrepPtrs::carve(c.take(L.bytes(M)), L, M);
+    launch_prep(A, false, lda, nullptr, M, K, P, L, s);
+    return cuda_status(launch_gemm_small(W, N, K, P, L, M, Y, ldy, status_word(ws), s));
+}
+
+// ---------------------------------------------------------------- routed MoE
+
+size_t q2_moe_grouped_workspace(int M, int E, int topk, int H, int F) {
+    if (M < 1 || M > 64 || E < 1 || E > 256 || topk < 1 || topk > 16 || topk > E || !gemm_k_ok(H) ||
+        !gemm_k_ok(F))
+        return Q2_WORKSPACE_HEADER_BYTES;
+    return moe_carve(nullptr, M, E, topk, H, F).bytes;
+}
+
+q2_status q2_moe_grouped(const void *Wg, const void *Wu, const void *Wd, int E, int H, int F, int topk,
+                         unsigned flags, const uint16_t *X, int M, const float *router_logits, float *Y,
+                         int32_t *topk_ids_out, float *topk_w_out, void *ws, size_t ws_bytes,
+                         q2_stream_t stream) {
+    if (!Wg || !Wu || !Wd || !X || !router_logits || !Y || E < 1 || topk < 1 || topk > E || M < 1 || H < kBlockK ||
+        F < kBlockK || H % kBlockK != 0 || F % kBlockK != 0 || (flags & ~Q2_MOE_RENORMALIZE) != 0)
+        return Q2_ERR_INVALID_ARG;
+    if (M > 64 || E > 256 || topk > 16 || !gemm_k_ok(H) || !gemm_k_ok(F)) return Q2_ERR_UNSUPPORTED;
+    if (!aligned(Wg, 16) || !aligned(Wu, 16) || !aligned(Wd, 16) || !aligned(X, 16) || !aligned(router_logits, 4) ||
+        !aligned(Y, 4) || !aligned(topk_ids_out, 4) || !aligned(topk_w_out, 4))
+        return Q2_ERR_ALIGNMENT;
+    const MoeCarve need = moe_carve(nullptr, M, E, topk, H, F);
+    const q2_status wst = check_ws(ws, ws_bytes, need.bytes);
+    if (wst != Q2_OK) return wst;
+    MoeArgs a;
+    a.Wg = static_cast<const uint8_t *>(Wg);
+    a.Wu = static_cast<const uint8_t *>(Wu);
+    a.Wd = static_cast<const uint8_t *>(Wd);
+    a.E = E; a.H = H; a.F = F; a.topk = topk; a.M = M; a.flags = flags;
+    a.X = X;
+    a.router = router_logits;
+    a.Y = Y;
+    a.ids_out = topk_ids_out;
+    a.w_out = topk_w_out;
+    a.status = status_word(ws);
+    const MoeCarve mc = moe_carve(ws, M, E, topk, H, F);
+    return cuda_status(launch_moe(a, mc.w, device_sms(), reinterpret_cast<cudaStream_t>(stream)));
+}
+
+// ---------------------------------------------------------------- p/q verify
+
+size_t pq_verify_workspace(int S, int k, int V) {
+    if (S < 1 || k < 0 || k > kMaxDrafts || V < 1 || V > (1 << 28)) return Q2_WORKSPACE_HEADER_BYTES;
+    if (V <= kWarpTierMaxV) return Q2_WORKSPACE_HEADER_BYTES;
+    return pq_carve(nullptr, S, k, V).bytes;
+}
+
+q2_status pq_verify(const float *target_logits, const float *draft_logits, const int32_t *draft_tokens,
+                    const float *u_acc, const float *u_fin, int S, int k, int V, float temperature,
+                    int32_t *n_accepted, int32_t *out_tokens, float *probs_out, void *ws, size_t ws_bytes,
+                    q2_stream_t stream) {
+    if (S < 1 || k < 0 || V < 1 || !target_logits || !u_fin || !n_accepted || !out_tokens ||
+        !(temperature > 0.0f) || !isfinite(temperature))
+        return Q2_ERR_INVALID_ARG;
+    if (k > 0 && (!draft_logits || !draft_tokens || !u_acc)) return Q2_ERR_INVALID_ARG;
+    if (k > kMaxDrafts || V > (1 << 28)) return Q2_ERR_UNSUPPORTED;
+    if (!aligned(target_logits, 16) || (k > 0 && !aligned(draft_logits, 16)) || !aligned(draft_tokens, 4) ||
+        !aligned(u_acc, 4) || !aligned(u_fin, 4) || !aligned(n_accepted, 4) || !aligned(out_tokens, 4) ||
+        !aligned(probs_out, 4))
+        return Q2_ERR_ALIGNMENT;
+    const bool warp_tier = V <= kWarpTierMaxV;
+    if (!warp_tier && S > 65535) return Q2_ERR_UNSUPPORTED;  // sessions map to grid.y
+    const size_t need = warp_tier ? (size_t)Q2_WORKSPACE_HEADER_BYTES : pq_carve(nullptr, S, k, V).bytes;
+    const q2_status wst = check_ws(ws, ws_bytes, need);
+    if (wst != Q2_OK) return wst;
+    PqArgs a;
+    a.target = target_logits;
+    a.draft = draft_logits;
+    a.drafts = draft_tokens;
+    a.u_acc = u_acc;
+    a.u_fin = u_fin;
+    a.S = S; a.k = k; a.V = V;
+    a.beta64 = 1.4426950408889634 / (double)temperature;
+    a.beta = (float)a.beta64;
+    a.n_acc = n_accepted;
+    a.tokens = out_tokens;
+    a.probs = probs_out;
+    a.status = status_word(ws);
+    PqSplit sp{};
+    const int sms = device_sms();
+    if (!warp_tier) {
+        const PqCarve pc = pq_carve(ws, S, k, V);
+        int C = std::max(1, std::min(cdiv(2 * sms, S), pq_cmax(V)));
+        const int L = (int)align_up((size_t)cdiv(V, C), kChunkAlign);
+        C = cdiv(V, L);
+        sp.C = C;
+        sp.L = L;
+        sp.stats = pc.stats;
+        sp.mass = pc.mass;
+        sp.pmass = pc.pmass;
+        sp.tickets = pc.tickets;
+    }
+    return cuda_status(launch_pq_verify(a, sp, warp_tier, sms, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// q2v_kernels.cuh -- launch interfaces between the C ABI (q2v_api.cu) and the kernels.
+#pragma once
+
+#include "q2v_common.cuh"
+#include "q2v_mma_core.cuh"
+
+namespace q2v {
+
+// ------------------------------------------------------------------ GEMM
+
+void launch_prep(const void *src, bool src_f32, int ld, const int *rows, int R, int K, const PrepPtrs &P,
+                 const PrepLayout &L, cudaStream_t s);
+cudaError_t launch_gemm_small(const void *W, int N, int K, const PrepPtrs &P, const PrepLayout &L, int M,
+                              float *Y, int ldy, unsigned int *status, cudaStream_t s);
+
+// ------------------------------------------------------------------ p/q verify
+
+constexpr int kMaxDrafts = 16;
+constexpr int kMaxRows = 2 * kMaxDrafts + 1;
+constexpr int kWarpTierMaxV = 4096;   // sessions with V at most this use one warp each
+constexpr int kChunkAlign = 128;      // chunk lengths are multiples of this (float4 x 32 lanes)
+constexpr int kMaxChunks = 1024;      // chunks per session (workspace sizing bound)
+
+struct PqArgs {
+    const float *target;
+    const float *draft;
+    const int32_t *drafts;
+    const float *u_acc;
+    const float *u_fin;
+    int S, k, V;
+    float beta;     // log2(e) / T
+    double beta64;  // log2(e) / T in fp64
+    int32_t *n_acc;
+    int32_t *tokens;
+    float *probs;
+    unsigned int *status;
+};
+
+struct PqSplit {
+    int C;               // chunks per session
+    int L;               // chunk length (multiple of kChunkAlign)
+    float *stats;        // [S][2k+1][C] float2 (max, sum)
+    double *mass;        // [S][C]
+    double *pmass;       // [S][C]
+    unsigned int *tickets;  // [S]
+};
+
+cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier, int num_sms, cudaStream_t st);
+
+// ------------------------------------------------------------------ routed MoE
+
+struct MoeArgs {
+    const uint8_t *Wg, *Wu, *Wd;
+    int E, H, F, topk, M;
+    unsigned flags;
+    const uint16_t *X;
+    const float *router;
+    float *Y;
+    int32_t *ids_out;
+    float *w_out;
+    unsigned int *status;
+};
+
+struct MoeWs {
+    int *counts;      // [E]
+    int *offsets;     // [E+1]
+    int *active;      // [E] expert ids with count > 0, ascending; active_n at active[E]
+    int *pair_row;    // [M*topk] activation row of each expert-grouped pair
+    int *pair_of;     // [M*topk] grouped position of (row, slot)
+    float *gate_w;    // [M*topk] gate weight of (row, slot)
+    float *h;         // [M*topk][F] fp32 silu(gate) * up per grouped pair
+    float *out;       // [M*topk][H] fp32 down projection per grouped pair
+    PrepPtrs prepX;   // prepared X rows (K = H)
+    PrepPtrs prepH;   // prepared h rows (K = F)
+};
+
+cudaError_t launch_moe(const MoeArgs &a, const MoeWs &w, int num_sms, cudaStream_t s);
+
+}  // namespace q2v

@@ -120,10 +120,14 @@ def q2b32_weights(st: Streams, N: int, K: int, d_lo=0.01, d_hi=0.05, m_std=0.02,
     [batch*N, K/32, 12] (expert e's matrix is rows e*N..e*N+N-1)."""
     rows = batch * N
     nb = K // Q2B32_BLOCK_K
-    codes = st["codes"].integers(0, 4, size=(rows, K), dtype=np.uint8)
+    out = np.empty((rows, nb, Q2B32_BLOCK_BYTES), np.uint8)
+    # a uniform byte is four independent uniform 2-bit codes
+    out[..., :8] = st["codes"].integers(0, 256, size=(rows, nb, 8), dtype=np.uint8)
     d = fp16_bits(st["d"].uniform(d_lo, d_hi, size=(rows, nb)))
     m = fp16_bits(st["m"].normal(0.0, m_std, size=(rows, nb)))
-    return pack_q2b32(codes, d, m)
+    out[..., 8:10] = d.view(np.uint8).reshape(rows, nb, 2)
+    out[..., 10:12] = m.view(np.uint8).reshape(rows, nb, 2)
+    return out
 
 
 def activations_bf16(st: Streams, M: int, K: int, std: float = 1.0) -> np.ndarray:

@@ -1,0 +1,128 @@
+"""q2_tiny_gemm on the GPU against the fp64 oracle, element by element:
+|gpu - oracle| <= 2e-3 * sum_k |a_k w_k|."""
+import numpy as np
+import pytest
+
+from _util import check_gemm, to_dev
+from speculative_decode_verifier_gb300 import synth
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def env(orc):
+    import torch
+
+    from speculative_decode_verifier_gb300 import build, q2v
+    build.build()
+    q2v.load()
+    return torch.device("cuda:0"), q2v, orc
+
+
+def _run(env, W, N, K, A, ws=None):
+    dev, q2v, _ = env
+    Y = q2v.q2_tiny_gemm(to_dev(W.reshape(-1), dev), N, K, to_dev(A, dev), ws=ws)
+    return Y.cpu().numpy()
+
+
+@pytest.mark.parametrize("M", [1, 2, 3, 4])
+def test_tiny_smoke_config(env, M):
+    g = synth.config_gemm(0, M=M)
+    Y = _run(env, g["W"], g["N"], g["K"], g["A"])
+    Yo, absY = env[2].gemm(g["W"], g["N"], g["K"], g["A"])
+    check_gemm(Y, Yo, absY, f"cfg0 M={M}")
+
+
+def test_verifier_linear_config(env):
+    g = synth.config_gemm(1)
+    Y = _run(env, g["W"], g["N"], g["K"], g["A"])
+    Yo, absY = env[2].gemm(g["W"], g["N"], g["K"], g["A"])
+    worst = check_gemm(Y, Yo, absY, "cfg1")
+    assert worst < 1e-4  # far inside the bound
+
+
+@pytest.mark.parametrize("M,N,K", [
+    (5, 517, 96),      # ragged N (not a multiple of 16), odd block count (3 blocks)
+    (3, 33, 160),      # 5 blocks: a partial tile, 4-byte-aligned rows
+    (7, 48, 288),      # 9 blocks: two tiles, the second nearly empty
+    (8, 64, 4096),
+    (9, 64, 1024),     # two activation slices
+    (16, 40, 2048),
+    (33, 50, 512),
+    (64, 32, 4096),    # the largest M
+    (5, 64, 8192),     # the largest K (32 warp tiles)
+    (1, 1, 32),        # the smallest problem
+])
+def test_shapes(env, M, N, K):
+    st = synth.Streams(1000 + M * 7 + N + K)
+    W = synth.q2b32_weights(st, N, K)
+    A = synth.activations_bf16(st, M, K)
+    Y = _run(env, W, N, K, A)
+    Yo, absY = env[2].gemm(W, N, K, A)
+    check_gemm(Y, Yo, absY, f"M={M} N={N} K={K}")
+
+
+def test_activation_range_extremes(env):
+    """Rows far outside the f16 range, tiny rows and an all-zero row: the per-row power-of-two
+    scale keeps them exact."""
+    st = synth.Streams(77)
+    M, N, K = 5, 32, 512
+    W = synth.q2b32_weights(st, N, K)
+    a = st["A"].normal(0, 1, size=(M, K))
+    a[0] *= 1e30
+    a[1] *= 1e-30
+    a[2] = 0.0
+    a[3] *= 7e4
+    A = synth.bf16_bits(a)
+    Y = _run(env, W, N, K, A)
+    Yo, absY = env[2].gemm(W, N, K, A)
+    assert np.all(Y[2] == 0.0)
+    check_gemm(Y[[0, 1, 3, 4]], Yo[[0, 1, 3, 4]], absY[[0, 1, 3, 4]], "extremes")
+
+
+def test_scale_extremes_within_range(env):
+    """d = 0 (offset only), subnormal-small and large in-range scales."""
+    st = synth.Streams(78)
+    M, N, K = 4, 48, 256
+    codes = st["codes"].integers(0, 4, size=(N, K), dtype=np.uint8)
+    d = st["d"].uniform(0.01, 0.05, size=(N, K // 32))
+    d[0:16] = 0.0
+    d[16:32] = 1e-6
+    d[32:48] = 12000.0
+    m = st["m"].normal(0, 0.02, size=(N, K // 32))
+    W = synth.pack_q2b32(codes, synth.fp16_bits(d), synth.fp16_bits(m))
+    A = synth.activations_bf16(st, M, K)
+    Y = _run(env, W, N, K, A)
+    Yo, absY = env[2].gemm(W, N, K, A)
+    check_gemm(Y, Yo, absY, "scales")
+
+
+def test_scale_out_of_range_sets_status(env):
+    dev, q2v, _ = env
+    st = synth.Streams(79)
+    N, K, M = 16, 64, 2
+    codes = st["codes"].integers(0, 4, size=(N, K), dtype=np.uint8)
+    d = np.full((N, K // 32), 0.02)
+    d[3, 1] = 30000.0
+    W = synth.pack_q2b32(codes, synth.fp16_bits(d), synth.fp16_bits(np.zeros((N, K // 32))))
+    A = synth.activations_bf16(st, M, K)
+    ws = q2v.workspace(q2v.q2_tiny_gemm_workspace(M, N, K), dev)
+    _run(env, W, N, K, A, ws=ws)
+    assert q2v.q2_get_device_status(ws) == 8  # Q2_ERR_RANGE
+    assert q2v.q2_get_device_status(ws) == 0  # read clears it
+
+
+def test_deterministic_and_ldy(env):
+    import torch
+    dev, q2v, orc = env
+    g = synth.config_gemm(1, M=5)
+    Wd = to_dev(g["W"].reshape(-1), dev)
+    Ad = to_dev(g["A"], dev)
+    Y1 = q2v.q2_tiny_gemm(Wd, g["N"], g["K"], Ad).cpu()
+    Y2 = q2v.q2_tiny_gemm(Wd, g["N"], g["K"], Ad).cpu()
+    assert torch.equal(Y1, Y2)
+    # a padded output (ldy > N) leaves the padding untouched
+    Yp = torch.full((5, g["N"] + 8), 7.0, device=dev)
+    q2v.q2_tiny_gemm(Wd, g["N"], g["K"], Ad, Y=Yp)
+    assert torch.equal(Yp[:, :g["N"]].cpu(), Y1)
+    assert torch.all(Yp[:, g["N"]:] == 7.0)
