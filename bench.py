@@ -159,6 +159,13 @@ def run_device(args, rank: int, world: int):
         part_moe(s)
         part_pq(s)
 
+    if args.profile:
+        # eager steps on one input set, for an ncu launch list (no graphs, no e2e, no oracle)
+        for i in range(args.warmup + args.steps):
+            step(sets[i % N_SETS])
+        torch.cuda.synchronize()
+        return None
+
     # eager warm-up (also caches device attributes before any capture) and routing facts
     active = []
     for s in sets:
@@ -352,6 +359,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile", action="store_true",
+                    help="run warmup+steps eager steps only (for an ncu launch list); prints nothing")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -375,6 +384,8 @@ def main():
         import torch
         torch.distributed.init_process_group("nccl")
     line = run_device(args, rank, world)
+    if line is None:
+        return
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
             us, cores, sample = run_oracle(1, 0)

@@ -62,7 +62,7 @@ typedef enum {
     Q2_ERR_CUDA = 5,        /* a CUDA runtime call (launch, attribute, copy) failed        */
     Q2_ERR_TIMEOUT = 6,     /* a bounded device-side wait gave up                          */
     Q2_ERR_BAD_TOKEN = 7,   /* device: a draft token is outside [0, V)                     */
-    Q2_ERR_RANGE = 8        /* device: a Q2B32 scale |d| > 16376 (outside the exact path)  */
+    Q2_ERR_RANGE = 8        /* device: a Q2B32 scale |d| >= 64 (outside the exact path)    */
 } q2_status;
 
 #define Q2_WORKSPACE_HEADER_BYTES 256
@@ -86,10 +86,11 @@ size_t q2_tiny_gemm_workspace(int M, int N, int K);
  *   M    activation rows, 1 <= M <= 64.
  *   Y    fp32 output [M][ldy], ldy >= N, 4-byte aligned.  Fully overwritten for n < N.
  *   ws   workspace of q2_tiny_gemm_workspace(M,N,K) bytes.
- * Accumulation is fp32; each product uses the weight rounded to fp16 once (q*d) and the
- * offset m exactly, and activations converted to fp16 under an exact per-row power-of-two
- * scale, so |Y - exact| stays far below 2e-3 * sum_k |a_k w_k|.
- * Device errors: Q2_ERR_RANGE if a block has |d| > 16376.
+ * Accumulation is fp32; each product uses q*d rounded once to fp16 and the offset m
+ * exactly, and activations converted to fp16 under an exact per-row power-of-two scale, so
+ * |Y - exact| stays far below 2e-3 * sum_k |a_k w_k|.  Scales must satisfy |d| < 64 (real
+ * 2-bit block scales are orders of magnitude smaller).
+ * Device errors: Q2_ERR_RANGE if a block has a finite |d| >= 64.
  */
 q2_status q2_tiny_gemm(const void *W, int N, int K, const uint16_t *A, int M, int lda,
                        float *Y, int ldy, void *ws, size_t ws_bytes, q2_stream_t stream);

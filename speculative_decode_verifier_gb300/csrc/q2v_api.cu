@@ -63,7 +63,7 @@ int pq_cmax(int V) { return std::min(cdiv(V, kChunkAlign), kMaxChunks); }
 
 struct PqCarve {
     float *stats;
-    double *mass, *pmass;
+    float *mass, *pmass;
     unsigned int *tickets;
     size_t bytes;
 };
@@ -73,8 +73,8 @@ PqCarve pq_carve(void *ws, int S, int k, int V) {
     PqCarve r{};
     const size_t R = 2 * (size_t)k + 1, C = pq_cmax(V);
     r.stats = static_cast<float *>(c.take((size_t)S * R * C * 2 * sizeof(float)));
-    r.mass = static_cast<double *>(c.take((size_t)S * C * sizeof(double)));
-    r.pmass = static_cast<double *>(c.take((size_t)S * C * sizeof(double)));
+    r.mass = static_cast<float *>(c.take((size_t)S * C * sizeof(float)));
+    r.pmass = static_cast<float *>(c.take((size_t)S * C * sizeof(float)));
     r.tickets = static_cast<unsigned int *>(c.take((size_t)S * sizeof(unsigned int)));
     r.bytes = c.off;
     return r;
@@ -97,8 +97,8 @@ MoeCarve moe_carve(void *ws, int M, int E, int topk, int H, int F) {
     r.w.pair_row = static_cast<int *>(c.take(P * sizeof(int)));
     r.w.pair_of = static_cast<int *>(c.take(P * sizeof(int)));
     r.w.gate_w = static_cast<float *>(c.take(P * sizeof(float)));
-    r.w.h = static_cast<float *>(c.take(2 * P * (size_t)F * sizeof(float)));
-    r.w.out = static_cast<float *>(c.take(P * (size_t)H * sizeof(float)));
+    r.w.h = static_cast<float *>(c.take((size_t)kMaxKSplits * 2 * P * (size_t)F * sizeof(float)));
+    r.w.out = static_cast<float *>(c.take((size_t)kMaxKSplits * P * (size_t)H * sizeof(float)));
     const PrepLayout LX(H), LH(F);
     void *px = c.take(LX.bytes(M));
     void *ph = c.take(LH.bytes((int)P));
@@ -164,7 +164,8 @@ q2_status q2_tiny_gemm(const void *W, int N, int K, const uint16_t *A, int M, in
     Carver c(ws);
     const PrepLayout L(K);
     const PrepPtrs P = PrepPtrs::carve(c.take(L.bytes(M)), L, M);
-    launch_prep(A, false, lda, nullptr, M, K, P, L, s);
+    const cudaError_t e = launch_prep_bf16(A, lda, nullptr, M, K, P, L, s);
+    if (e != cudaSuccess) return Q2_ERR_CUDA;
     return cuda_status(launch_gemm_small(W, N, K, P, L, M, Y, ldy, status_word(ws), s));
 }
 
@@ -239,8 +240,7 @@ q2_status pq_verify(const float *target_logits, const float *draft_logits, const
     a.u_acc = u_acc;
     a.u_fin = u_fin;
     a.S = S; a.k = k; a.V = V;
-    a.beta64 = 1.4426950408889634 / (double)temperature;
-    a.beta = (float)a.beta64;
+    a.beta = (float)(1.4426950408889634 / (double)temperature);
     a.n_acc = n_accepted;
     a.tokens = out_tokens;
     a.probs = probs_out;

@@ -27,6 +27,34 @@ __device__ __forceinline__ void set_status(unsigned int *status, unsigned int co
 }
 
 __host__ __device__ __forceinline__ int cdiv(int a, int b) { return (a + b - 1) / b; }
+
+// ---------------------------------------------------------------- programmatic dependent launch
+//
+// Every kernel of the library is launched with programmatic stream serialization, so it
+// may start while the previous kernel in the stream is still running.  Each kernel calls
+// pdl_wait() before touching anything a predecessor may write (it returns once every
+// prerequisite grid has completed and its memory is visible) and then pdl_trigger() so its
+// own successor can be scheduled early.  The only reads issued before pdl_wait() are of
+// Q2B32 weights in GEMM kernels whose programmatic predecessor is the library's own prep
+// kernel, which itself has already waited for everything before it.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;\n" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, cudaStream_t stream,
+                              Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 __host__ __device__ __forceinline__ size_t align_up(size_t a, size_t b) { return (a + b - 1) / b * b; }
 
 // ---------------------------------------------------------------- tensor-core MMA (legacy path)
@@ -72,34 +100,53 @@ __device__ __forceinline__ uint32_t pack_half2(__half lo, __half hi) {
     return (uint32_t)__half_as_ushort(lo) | ((uint32_t)__half_as_ushort(hi) << 16);
 }
 
-// Two Q2B32 codes -> their dequantised product q*d as an f16x2, exactly rounded once.
+// Two Q2B32 codes -> their products with the block scale, as an f16x2, each exactly
+// rounded once.
 //
-// Codes c_i (bits 2i..2i+1) and c_{i+8} (bits 2i+16..2i+17) of a 32-bit code word are
-// moved to bits 8..9 of each 16-bit half and or-ed into the f16 constant 4.0 (0x4400):
-// in [4, 8) the f16 spacing is 2^-8, so the halves read 4 + c exactly.  Then
-// fma(4 + c, d, -4d) = c*d computed exactly and rounded once to f16 (-4d is exact for
-// any |d| <= 16376).  The offset m is applied separately in fp32.
-template <int I>
-__device__ __forceinline__ uint32_t dequant_pair(uint32_t word, uint32_t d2, uint32_t nd4) {
-    constexpr int sh = 8 - 2 * I;
-    uint32_t v = sh >= 0 ? (word << (sh >= 0 ? sh : 0)) : (word >> (sh < 0 ? -sh : 0));
-    uint32_t x = lop3_and_or(v, 0x03000300u, 0x44004400u);
-    return hfma2_u32(x, d2, nd4);
+// A 32-bit code word holds 16 codes, code c at bits 2c.  Codes i and i+8 (i = 0..3) sit at
+// the same bit offset 2i inside the low and the high 16-bit half; for i = 4..7 they do
+// after one shift of the word by 8.  Or-ed into the f16 constant 1024 (0x6400), whose
+// mantissa step is 1, the masked halves read exactly 1024 + q * 4^p with p = i mod 4.  Then
+// fma(1024 + q*4^p, d, -1024 d) = q * 4^p * d, computed exactly and rounded once to f16
+// (-1024 d is exact for |d| < 64, and 192 |d| stays below the f16 maximum).  The activation
+// that meets this product in the MMA carries the matching factor 4^-p (applied, exactly, when
+// the activations are prepared), so each product is q * d * a.  The offset m is applied
+// separately, exactly.  Per two weights: one lop3 and one fma (plus one shift per 8 pairs).
+template <int POS>
+__device__ __forceinline__ uint32_t dequant_pos(uint32_t v, uint32_t d2, uint32_t nd1024) {
+    uint32_t x, r;
+    // (v & mask) | 1024.0h2 in one lop3 (mask as an immediate), then one f16x2 fma
+    asm("lop3.b32 %0, %1, %2, %3, 0xEA;\n" : "=r"(x) : "r"(v), "n"(0x00030003u << POS), "r"(0x64006400u));
+    asm("fma.rn.f16x2 %0, %1, %2, %3;\n" : "=r"(r) : "r"(x), "r"(d2), "r"(nd1024));
+    return r;
 }
 
-// f16x2 {d, d} and {-4d, -4d} from a block's packed (d | m << 16) word.
-__device__ __forceinline__ void scale_pair(uint32_t dm, uint32_t &d2, uint32_t &nd4) {
-    uint32_t d = dm & 0xFFFFu;
+// f16x2 {d, d} and {-1024 d, -1024 d} from a block's packed (d | m << 16) word.
+__device__ __forceinline__ void scale_pair(uint32_t dm, uint32_t &d2, uint32_t &nd1024) {
+    const uint32_t d = dm & 0xFFFFu;
     d2 = d | (d << 16);
-    __half nd = __hmul(__ushort_as_half((unsigned short)d), __float2half_rn(-4.0f));
-    uint32_t n = __half_as_ushort(nd);
-    nd4 = n | (n << 16);
+    const __half nd = __hmul(__ushort_as_half((unsigned short)d), __ushort_as_half((unsigned short)0xE400u));  // * -1024
+    const uint32_t n = __half_as_ushort(nd);
+    nd1024 = n | (n << 16);
 }
 
-// |d| > 16376 makes -4d overflow: flag it.
+// Division by a run-time constant d >= 1 for 0 <= u < 2^31 (round-up multiply-shift:
+// s = ceil(log2 d), m = floor(2^32 (2^s - d) / d) + 1, u / d = (umulhi(u, m) + u) >> s).
+struct FastDiv {
+    uint32_t d, m, s;
+    FastDiv() = default;
+    __host__ __device__ explicit FastDiv(uint32_t d_) : d(d_) {
+        s = 0;
+        while ((1u << s) < d) ++s;
+        m = (uint32_t)((((uint64_t)1 << 32) * (((uint64_t)1 << s) - d)) / d + 1);
+    }
+    __device__ __forceinline__ uint32_t div(uint32_t u) const { return (__umulhi(u, m) + u) >> s; }
+};
+
+// |d| >= 64 (finite) is outside the exact range of dequant_pos: flag it.
 __device__ __forceinline__ bool scale_out_of_range(uint32_t dm) {
-    uint32_t mag = dm & 0x7FFFu;
-    return mag > 0x73FFu && mag < 0x7C00u;  // 0x73FF = 16376; >= 0x7C00 is inf/nan (propagates)
+    const uint32_t mag = dm & 0x7FFFu;
+    return mag >= 0x5400u && mag < 0x7C00u;  // 0x5400 = 64.0; >= 0x7C00 is inf/nan (propagates)
 }
 
 }  // namespace q2v

@@ -10,93 +10,102 @@
 
 namespace q2v {
 
-// One CTA per activation row: per-row exponent, permuted f16x2 pair slots, hi/lo block
-// sums.  src rows: bf16 bits or fp32, row r of the prep is source row rows[r] (or r).
-template <bool F32>
-__global__ void __launch_bounds__(256) prep_act_kernel(const void *__restrict__ src, int ld,
-                                                       const int *__restrict__ rows, int R, int K,
-                                                       PrepPtrs P, PrepLayout L) {
+// One CTA per activation row, one thread per Q2B32 block of 32 activations (K <= 8192,
+// so at most 256 blocks): per-row exponent, permuted f16x2 pair slots, hi/lo block sums.
+// Row r of the prep is source row rows[r] (or r when rows is NULL); rows[r] < 0 gives a
+// zero row.  Source rows are bf16 with leading dimension ld (ld % 8 == 0, 16-byte base).
+__global__ void __launch_bounds__(256) prep_bf16_kernel(const uint16_t *__restrict__ src, int ld,
+                                                        const int *__restrict__ rows, int R, int K,
+                                                        PrepPtrs P, PrepLayout L) {
+    __shared__ float scratch[32];
+    pdl_wait();
+    pdl_trigger();
     const int r = blockIdx.x;
-    if (r >= R) return;
+    const int b = threadIdx.x;
     const int srow = rows ? rows[r] : r;
-    const int tid = threadIdx.x;
-    __shared__ float red[8];
-    __shared__ int sexp;
-    auto at = [&](int k) -> float {
-        if (F32) return reinterpret_cast<const float *>(src)[(size_t)srow * ld + k];
-        const uint16_t b = reinterpret_cast<const uint16_t *>(src)[(size_t)srow * ld + k];
-        return __uint_as_float((uint32_t)b << 16);
-    };
+    float v[32];
     float mx = 0.0f;
-    if (srow >= 0)
-        for (int k = tid; k < K; k += blockDim.x) mx = fmaxf(mx, fabsf(at(k)));
+    if (b < L.nb && srow >= 0) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(src + (size_t)srow * ld + (size_t)b * kBlockK);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if ((tid & 31) == 0) red[tid >> 5] = mx;
-    __syncthreads();
-    if (tid == 0) {
-        float m = 0.0f;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
-        sexp = act_exponent(m);
-        P.exps[r] = sexp;
-    }
-    __syncthreads();
-    const int e = sexp;
-    uint32_t *act = P.act + (size_t)r * L.act_words_per_row();
-    for (int j = tid; j < L.nbp * 16; j += blockDim.x) {
-        const int b = j >> 4, p = j & 15;
-        uint32_t v = 0;
-        if (srow >= 0 && b < L.nb) {
-            const int k0 = b * kBlockK + 16 * (p >> 3) + (p & 7);
-            v = pack_half2(__float2half_rn(ldexpf(at(k0), -e)), __float2half_rn(ldexpf(at(k0 + 8), -e)));
+        for (int j = 0; j < 4; ++j) {
+            const uint4 q = __ldg(p + j);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[8 * j + 2 * i] = __uint_as_float(w[i] << 16);
+                v[8 * j + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
         }
-        act[j] = v;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fabsf(v[j]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
     }
-    __half *sh = reinterpret_cast<__half *>(P.shi + (size_t)r * L.sum_words_per_row());
-    __half *sl = reinterpret_cast<__half *>(P.slo + (size_t)r * L.sum_words_per_row());
-    for (int b = tid; b < L.nbp; b += blockDim.x) {
-        float s = 0.0f;
-        if (srow >= 0 && b < L.nb)
-            for (int kk = 0; kk < kBlockK; ++kk)
-                s += __half2float(__float2half_rn(ldexpf(at(b * kBlockK + kk), -e)));
-        const __half hi = __float2half_rn(s);
-        sh[b] = hi;
-        sl[b] = __float2half_rn(s - __half2float(hi));
-    }
+    const int e = act_exponent(block_max_nonneg(mx, scratch));
+    if (b == 0) P.exps[r] = e;
+    if (b < L.nbp)
+        prep_store_block(v, e, P.act + (size_t)r * L.act_words_per_row(),
+                         reinterpret_cast<__half *>(P.shi + (size_t)r * L.sum_words_per_row()),
+                         reinterpret_cast<__half *>(P.slo + (size_t)r * L.sum_words_per_row()), b);
 }
 
-void launch_prep(const void *src, bool src_f32, int ld, const int *rows, int R, int K, const PrepPtrs &P,
-                 const PrepLayout &L, cudaStream_t s) {
-    if (R <= 0) return;
-    if (src_f32)
-        prep_act_kernel<true><<<R, 256, 0, s>>>(src, ld, rows, R, K, P, L);
-    else
-        prep_act_kernel<false><<<R, 256, 0, s>>>(src, ld, rows, R, K, P, L);
+cudaError_t launch_prep_bf16(const uint16_t *src, int ld, const int *rows, int R, int K, const PrepPtrs &P,
+                             const PrepLayout &L, cudaStream_t s) {
+    return launch_pdl(prep_bf16_kernel, dim3(R), dim3(256), s, src, ld, rows, R, K, P, L);
 }
 
-// Dense small-M GEMM: CTA = 16 weight rows, one warp per K tile; the activation rows are
-// processed in slices of 8 with the weight tile kept in registers across slices.
+// Dense small-M GEMM: CTA = 16 weight rows and ceil(tiles/2) warps (<= 16); warp w owns K
+// tiles w and w + nwarps, both requested before the programmatic wait (they do not depend
+// on the prep kernel), so the weight stream overlaps the prep and the launch.  The prepared
+// activation rows are then staged in shared memory, 8 at a time, with the weight tiles
+// kept in registers across slices.  Partial sums of the K split are reduced across warps
+// in warp order.
+constexpr int kGemmWarps = 16;
+constexpr int kMaxTilesPerWarp = kMaxTileWarps / kGemmWarps;
+
 template <bool ALIGN8>
-__global__ void __launch_bounds__(1024) q2_gemm_mma_kernel(const uint8_t *__restrict__ W, int N, int K,
-                                                           PrepPtrs P, PrepLayout L, int M,
-                                                           float *__restrict__ Y, int ldy,
-                                                           unsigned int *status) {
-    __shared__ float red[kMaxTileWarps * kRowsPerCta * 8];
+__global__ void __launch_bounds__(kGemmWarps * 32) q2_gemm_mma_kernel(const uint8_t *__restrict__ W, int N, int K,
+                                                                         PrepPtrs P, PrepLayout L, int M, int ncols,
+                                                                         float *__restrict__ Y, int ldy,
+                                                                         unsigned int *status) {
+    extern __shared__ __align__(16) uint32_t sm_act[];
+    __shared__ float red[kGemmWarps * kRowsPerCta * 8];
+    __shared__ int s_rows[8];
     const int n0 = blockIdx.x * kRowsPerCta;
     const int rows_valid = min(kRowsPerCta, N - n0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int nwarps = blockDim.x >> 5;
     const size_t row_bytes = (size_t)L.nb * kBlockBytes;
-    TileRegs wr;
-    load_tile<ALIGN8>(wr, W + (size_t)n0 * row_bytes, row_bytes, rows_valid, L.nb, warp, lane);
+    static_assert(kMaxTilesPerWarp == 2, "two weight tiles per warp");
+    TileRegs wr0, wr1;
+    load_tile<ALIGN8>(wr0, W + (size_t)n0 * row_bytes, row_bytes, rows_valid, L.nb, warp, lane);
+    if (warp + nwarps < L.ntk)
+        load_tile<ALIGN8>(wr1, W + (size_t)n0 * row_bytes, row_bytes, rows_valid, L.nb, warp + nwarps, lane);
+    pdl_wait();
+    pdl_trigger();
+    const SmemAct SA(L, ncols);
+    zero_column(sm_act, SA);
     bool range_bad = false;
     for (int m0 = 0; m0 < M; m0 += 8) {
         const int mc = min(8, M - m0);
-        ActRegs ar;
-        const int col = lane >> 2;
-        load_act(ar, P, L, col < mc ? m0 + col : -1, warp, lane);
-        float acc[4] = {0.f, 0.f, 0.f, 0.f};
-        compute_tile(wr, ar, acc, range_bad);
+        if (threadIdx.x < 8) s_rows[threadIdx.x] = m0 + threadIdx.x;
+        __syncthreads();
+        stage_act(sm_act, SA, P, L, s_rows, mc);
+        float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+        // one tile at a time (not unrolled), so the two tiles' register lifetimes stay apart
+#pragma unroll 1
+        for (int i = 0; i < kMaxTilesPerWarp; ++i) {
+            const int tile = warp + i * nwarps;
+            if (tile < L.ntk) {
+                TileRegs cur;
+#pragma unroll
+                for (int q = 0; q < 12; ++q)
+                    (&cur.w[0][0][0])[q] = i ? (&wr1.w[0][0][0])[q] : (&wr0.w[0][0][0])[q];
+                compute_tile_smem(cur, sm_act, SA, mc, tile, lane, acc, range_bad);
+            }
+        }
         store_fragments(red + warp * kRowsPerCta * 8, acc, lane);
         __syncthreads();
         for (int j = threadIdx.x; j < kRowsPerCta * mc; j += blockDim.x) {
@@ -110,17 +119,39 @@ __global__ void __launch_bounds__(1024) q2_gemm_mma_kernel(const uint8_t *__rest
     if (range_bad) set_status(status, Q2_ERR_RANGE);
 }
 
+namespace {
+size_t g_gemm_smem[2];  // dynamic shared memory each variant was configured for
+
+template <bool A8>
+cudaError_t launch_gemm_variant(const uint8_t *w, int N, int K, const PrepPtrs &P, const PrepLayout &L, int M,
+                                float *Y, int ldy, unsigned int *status, cudaStream_t s) {
+    auto kern = q2_gemm_mma_kernel<A8>;
+    const int ncols = min(8, M);
+    const size_t smem = SmemAct(L, ncols).bytes();
+    if (g_gemm_smem[A8] < smem) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        g_gemm_smem[A8] = smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(cdiv(N, kRowsPerCta));
+    cfg.blockDim = dim3(32 * cdiv(L.ntk, kMaxTilesPerWarp));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, w, N, K, P, L, M, ncols, Y, ldy, status);
+}
+}  // namespace
+
 cudaError_t launch_gemm_small(const void *W, int N, int K, const PrepPtrs &P, const PrepLayout &L, int M,
                               float *Y, int ldy, unsigned int *status, cudaStream_t s) {
-    const int grid = cdiv(N, kRowsPerCta);
-    const int block = 32 * L.ntk;
-    if ((L.nb % 2) == 0)
-        q2_gemm_mma_kernel<true><<<grid, block, 0, s>>>(static_cast<const uint8_t *>(W), N, K, P, L, M, Y, ldy,
-                                                        status);
-    else
-        q2_gemm_mma_kernel<false><<<grid, block, 0, s>>>(static_cast<const uint8_t *>(W), N, K, P, L, M, Y, ldy,
-                                                         status);
-    return cudaGetLastError();
+    const uint8_t *w = static_cast<const uint8_t *>(W);
+    if ((L.nb % 2) == 0) return launch_gemm_variant<true>(w, N, K, P, L, M, Y, ldy, status, s);
+    return launch_gemm_variant<false>(w, N, K, P, L, M, Y, ldy, status, s);
 }
 
 }  // namespace q2v

@@ -8,8 +8,8 @@ namespace q2v {
 
 // ------------------------------------------------------------------ GEMM
 
-void launch_prep(const void *src, bool src_f32, int ld, const int *rows, int R, int K, const PrepPtrs &P,
-                 const PrepLayout &L, cudaStream_t s);
+cudaError_t launch_prep_bf16(const uint16_t *src, int ld, const int *rows, int R, int K, const PrepPtrs &P,
+                             const PrepLayout &L, cudaStream_t s);
 cudaError_t launch_gemm_small(const void *W, int N, int K, const PrepPtrs &P, const PrepLayout &L, int M,
                               float *Y, int ldy, unsigned int *status, cudaStream_t s);
 
@@ -29,7 +29,6 @@ struct PqArgs {
     const float *u_fin;
     int S, k, V;
     float beta;     // log2(e) / T
-    double beta64;  // log2(e) / T in fp64
     int32_t *n_acc;
     int32_t *tokens;
     float *probs;
@@ -40,14 +39,16 @@ struct PqSplit {
     int C;               // chunks per session
     int L;               // chunk length (multiple of kChunkAlign)
     float *stats;        // [S][2k+1][C] float2 (max, sum)
-    double *mass;        // [S][C]
-    double *pmass;       // [S][C]
+    float *mass;         // [S][C] draw mass of each chunk
+    float *pmass;        // [S][C] p_j mass of each chunk (zero-residual fallback)
     unsigned int *tickets;  // [S]
 };
 
 cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier, int num_sms, cudaStream_t st);
 
 // ------------------------------------------------------------------ routed MoE
+
+constexpr int kMaxKSplits = 8;  // K splits of the grouped GEMM units (workspace sizing bound)
 
 struct MoeArgs {
     const uint8_t *Wg, *Wu, *Wd;
@@ -68,8 +69,8 @@ struct MoeWs {
     int *pair_row;    // [M*topk] activation row of each expert-grouped pair
     int *pair_of;     // [M*topk] grouped position of (row, slot)
     float *gate_w;    // [M*topk] gate weight of (row, slot)
-    float *h;         // [M*topk][F] fp32 silu(gate) * up per grouped pair
-    float *out;       // [M*topk][H] fp32 down projection per grouped pair
+    float *h;         // [KS][2][M*topk][F] fp32 gate and up partial sums per K split
+    float *out;       // [KS][M*topk][H] fp32 down projection partial sums per K split
     PrepPtrs prepX;   // prepared X rows (K = H)
     PrepPtrs prepH;   // prepared h rows (K = F)
 };

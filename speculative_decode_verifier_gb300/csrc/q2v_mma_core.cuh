@@ -7,7 +7,8 @@
 // warp streams 16 rows x 96 contiguous bytes.  Operand mapping: a k16 MMA step takes, for
 // thread t's logical columns (2t, 2t+1) and (2t+8, 2t+9), the code pairs (c_i, c_{i+8})
 // and (c_{i+1}, c_{i+9}) of one 16-code word of thread t's own block, so the A fragments
-// are decoded from the thread's own registers with no exchange.  The activation rows are
+// are decoded from the thread's own registers with no exchange (see dequant_pos: one lop3
+// and one fma per two weights).  The activation rows are
 // the 8-wide B operand; a separate prep kernel writes them once per call, as f16 under an
 // exact per-row power-of-two scale, in exactly this permuted order, so a thread's B
 // fragments for a whole tile are 128 contiguous bytes.  The Q2B32 offset m enters as its
@@ -104,74 +105,119 @@ __device__ __forceinline__ void load_tile(TileRegs &r, const uint8_t *__restrict
     }
 }
 
-// B-operand registers of one tile for one thread: column g's 16 pair slots of blocks
-// 2t and 2t+1 (32 words) and the hi/lo block-sum words of that block pair.
-struct ActRegs {
-    uint32_t a[32];
-    uint32_t shi, slo;
+// ---------------------------------------------------------------- shared-memory B operand
+//
+// Staged activations for up to `ncols` columns plus one all-zero column (index ncols),
+// which every MMA column without a row reads.  Column c holds its blocks in pairs: block
+// pair j = b/2 starts at word 34*j (32 words of data and 2 of skew), block b at
+// 34*(b/2) + 16*(b%2), pair slot p at + p.  A k16 step's 8-byte fragment load has threads
+// g = 0..7 on columns CS*g apart (CS == 8 mod 32) and t = 0..3 on block pairs 34 words
+// (2 banks) apart, so the warp's 64 words cover all 32 banks twice: two wavefronts, the
+// minimum for 256 bytes.  Each thread's base address is fixed for a tile; every step's
+// offset is a compile-time constant.  Block sums follow: shi/slo[c][SWW] words,
+// SWW == 4 (mod 32), word j = f16x2 (S[2j], S[2j+1]).
+constexpr int kPairWords = 34;
+
+struct SmemAct {
+    int CS, SWW, ncols;
+    __host__ __device__ SmemAct(const PrepLayout &L, int ncols_)
+        : CS((int)align_up((size_t)L.nbp / 2 * kPairWords, 32) + 8),
+          SWW((int)align_up((size_t)L.nbp / 2, 32) + 4),
+          ncols(ncols_) {}
+    __host__ __device__ size_t words() const { return (size_t)(ncols + 1) * (CS + 2 * SWW); }
+    __host__ __device__ size_t bytes() const { return words() * 4; }
+    __device__ uint32_t *act(uint32_t *sm, int c) const { return sm + (size_t)c * CS; }
+    __device__ uint32_t *shi(uint32_t *sm, int c) const { return sm + (size_t)(ncols + 1) * CS + (size_t)c * SWW; }
+    __device__ uint32_t *slo(uint32_t *sm, int c) const {
+        return sm + (size_t)(ncols + 1) * (CS + SWW) + (size_t)c * SWW;
+    }
 };
 
-// row < 0: a zero column (past the last activation row).
-__device__ __forceinline__ void load_act(ActRegs &r, const PrepPtrs &P, const PrepLayout &L, int row,
-                                         int tile, int lane) {
-    const int t = lane & 3;
-    if (row < 0) {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) r.a[j] = 0u;
-        r.shi = r.slo = 0u;
-        return;
+// Zero the all-zero column (once per CTA).  Block-wide; ends synchronised.
+__device__ __forceinline__ void zero_column(uint32_t *sm, const SmemAct &SA) {
+    for (int j = threadIdx.x; j < SA.CS; j += blockDim.x) SA.act(sm, SA.ncols)[j] = 0u;
+    for (int j = threadIdx.x; j < SA.SWW; j += blockDim.x) {
+        SA.shi(sm, SA.ncols)[j] = 0u;
+        SA.slo(sm, SA.ncols)[j] = 0u;
     }
-    const uint4 *src = reinterpret_cast<const uint4 *>(
-        P.act + (size_t)row * L.act_words_per_row() + (size_t)(tile * kTileBlocks + 2 * t) * 16);
-#pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint4 v = __ldg(src + j);
-        r.a[4 * j] = v.x; r.a[4 * j + 1] = v.y; r.a[4 * j + 2] = v.z; r.a[4 * j + 3] = v.w;
-    }
-    const size_t si = (size_t)row * L.sum_words_per_row() + (size_t)tile * 4 + t;
-    r.shi = __ldg(P.shi + si);
-    r.slo = __ldg(P.slo + si);
+    __syncthreads();
 }
 
-// acc (fragment rows g, g+8; columns 2t, 2t+1 of the n8 tile) += this tile's products.
-__device__ __forceinline__ void compute_tile(const TileRegs &r, const ActRegs &b, float (&acc)[4],
-                                             bool &range_bad) {
+// Copy the prepared rows rows[0..n) (n <= ncols) into shared memory.  Block-wide; ends
+// synchronised.
+__device__ __forceinline__ void stage_act(uint32_t *sm, const SmemAct &SA, const PrepPtrs &P, const PrepLayout &L,
+                                          const int *rows, int n) {
+    const int n16 = L.nbp * 4;  // 16-byte groups per row
+    for (int j = threadIdx.x; j < n * n16; j += blockDim.x) {
+        const int c = j / n16, q = j - c * n16;
+        const int b = q >> 2, grp = q & 3;
+        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(P.act + (size_t)rows[c] * L.act_words_per_row()) + q);
+        uint2 *dst = reinterpret_cast<uint2 *>(SA.act(sm, c) + (b >> 1) * kPairWords + (b & 1) * 16 + 4 * grp);
+        dst[0] = make_uint2(v.x, v.y);
+        dst[1] = make_uint2(v.z, v.w);
+    }
+    const int nw = L.nbp / 2;
+    for (int j = threadIdx.x; j < n * nw; j += blockDim.x) {
+        const int c = j / nw, i = j - c * nw;
+        SA.shi(sm, c)[i] = __ldg(P.shi + (size_t)rows[c] * L.sum_words_per_row() + i);
+        SA.slo(sm, c)[i] = __ldg(P.slo + (size_t)rows[c] * L.sum_words_per_row() + i);
+    }
+    __syncthreads();
+}
+
+// acc[0] += block 2t and the offsets' hi part, acc[1] += block 2t+1 and the lo part: two
+// independent MMA chains, issued alternately.  B fragments come from the staged operand,
+// column g (or the zero column when g has no row in the current slice of n columns).
+__device__ __forceinline__ void compute_tile_smem(const TileRegs &r, uint32_t *sm, const SmemAct &SA, int n,
+                                                  int tile, int lane, float (&acc)[2][4], bool &range_bad) {
+    const int g = lane >> 2, t = lane & 3;
+    const int cg = g < n ? g : SA.ncols;
+    const uint32_t *base = SA.act(sm, cg) + (tile * 4 + t) * kPairWords;  // block pair (2t, 2t+1)
+    uint32_t d2[2][2], nd[2][2];  // [block 2t | 2t+1][row g | g+8]
 #pragma unroll
     for (int bi = 0; bi < 2; ++bi) {
-        uint32_t d2a, nda, d2b, ndb;
-        scale_pair(r.w[0][bi][2], d2a, nda);
-        scale_pair(r.w[1][bi][2], d2b, ndb);
+        scale_pair(r.w[0][bi][2], d2[bi][0], nd[bi][0]);
+        scale_pair(r.w[1][bi][2], d2[bi][1], nd[bi][1]);
         range_bad |= scale_out_of_range(r.w[0][bi][2]) | scale_out_of_range(r.w[1][bi][2]);
-#pragma unroll
-        for (int w = 0; w < 2; ++w) {
-            const uint32_t c0 = r.w[0][bi][w], c1 = r.w[1][bi][w];
-#define Q2V_STEP(PP)                                                                          \
-    {                                                                                         \
-        const uint32_t a0 = dequant_pair<2 * (PP)>(c0, d2a, nda);                             \
-        const uint32_t a2 = dequant_pair<2 * (PP) + 1>(c0, d2a, nda);                         \
-        const uint32_t a1 = dequant_pair<2 * (PP)>(c1, d2b, ndb);                             \
-        const uint32_t a3 = dequant_pair<2 * (PP) + 1>(c1, d2b, ndb);                         \
-        mma_16816(acc, a0, a1, a2, a3, b.a[bi * 16 + 8 * w + 2 * (PP)],                      \
-                  b.a[bi * 16 + 8 * w + 2 * (PP) + 1]);                                       \
     }
-            Q2V_STEP(0) Q2V_STEP(1) Q2V_STEP(2) Q2V_STEP(3)
-#undef Q2V_STEP
+#pragma unroll
+    for (int w = 0; w < 2; ++w) {
+#pragma unroll
+        for (int pp = 0; pp < 4; ++pp) {
+#pragma unroll
+            for (int bi = 0; bi < 2; ++bi) {
+                const uint2 bb = *reinterpret_cast<const uint2 *>(base + bi * 16 + 8 * w + 2 * pp);
+                const uint32_t c0 = r.w[0][bi][w], c1 = r.w[1][bi][w];
+                const uint32_t va = pp < 2 ? c0 : (c0 >> 8), vb = pp < 2 ? c1 : (c1 >> 8);
+                uint32_t a0, a1, a2, a3;
+                if (pp & 1) {
+                    a0 = dequant_pos<4>(va, d2[bi][0], nd[bi][0]);
+                    a2 = dequant_pos<6>(va, d2[bi][0], nd[bi][0]);
+                    a1 = dequant_pos<4>(vb, d2[bi][1], nd[bi][1]);
+                    a3 = dequant_pos<6>(vb, d2[bi][1], nd[bi][1]);
+                } else {
+                    a0 = dequant_pos<0>(va, d2[bi][0], nd[bi][0]);
+                    a2 = dequant_pos<2>(va, d2[bi][0], nd[bi][0]);
+                    a1 = dequant_pos<0>(vb, d2[bi][1], nd[bi][1]);
+                    a3 = dequant_pos<2>(vb, d2[bi][1], nd[bi][1]);
+                }
+                mma_16816(acc[bi], a0, a1, a2, a3, bb.x, bb.y);
+            }
         }
     }
-    // offsets: sum over the tile's blocks of m[row][b] * S[b][col], with S = hi + lo
     const uint32_t am0 = prmt(r.w[0][0][2], r.w[0][1][2], 0x7632u);
     const uint32_t am1 = prmt(r.w[1][0][2], r.w[1][1][2], 0x7632u);
-    mma_1688(acc, am0, am1, b.shi);
-    mma_1688(acc, am0, am1, b.slo);
+    mma_1688(acc[0], am0, am1, SA.shi(sm, cg)[tile * 4 + t]);
+    mma_1688(acc[1], am0, am1, SA.slo(sm, cg)[tile * 4 + t]);
 }
 
-// red[16][8] (this warp's slice) <- the fragment accumulators.
-__device__ __forceinline__ void store_fragments(float *red, const float (&acc)[4], int lane) {
+// red[16][8] (this warp's slice) <- the sum of the two fragment accumulator chains.
+__device__ __forceinline__ void store_fragments(float *red, const float (&acc)[2][4], int lane) {
     const int g = lane >> 2, t = lane & 3;
-    red[g * 8 + 2 * t] = acc[0];
-    red[g * 8 + 2 * t + 1] = acc[1];
-    red[(g + 8) * 8 + 2 * t] = acc[2];
-    red[(g + 8) * 8 + 2 * t + 1] = acc[3];
+    red[g * 8 + 2 * t] = acc[0][0] + acc[1][0];
+    red[g * 8 + 2 * t + 1] = acc[0][1] + acc[1][1];
+    red[(g + 8) * 8 + 2 * t] = acc[0][2] + acc[1][2];
+    red[(g + 8) * 8 + 2 * t + 1] = acc[0][3] + acc[1][3];
 }
 
 // Per-row power-of-two exponent e so that max|a| * 2^-e lies in [2^9, 2^10): the scaled
@@ -179,6 +225,46 @@ __device__ __forceinline__ void store_fragments(float *red, const float (&acc)[4
 __device__ __forceinline__ int act_exponent(float maxabs) {
     if (!(maxabs > 0.0f) || !isfinite(maxabs)) return 0;
     return ilogbf(maxabs) - 9;
+}
+
+// Write prepared block b of one row from its 32 activations: 16 f16x2 pair slots (slot p
+// holds elements k0 and k0+8, k0 = 16*(p/8) + p%8), element j scaled by 2^-e * 4^-(j%4)
+// (the row scale and the code-position factor of dequant_pos, both exact), and the sum of
+// the block's f16 activations under the row scale alone, split into hi + lo f16.  The
+// padding blocks (v all zero) store zeros.
+__device__ __forceinline__ void prep_store_block(const float (&v)[32], int e, uint32_t *act_row, __half *sh,
+                                                 __half *sl, int b) {
+    __half h[32];
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        h[j] = __float2half_rn(ldexpf(v[j], -e - 2 * (j & 3)));
+        s += __half2float(__float2half_rn(ldexpf(v[j], -e)));
+    }
+    uint32_t w[16];
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+        const int k0 = 16 * (p >> 3) + (p & 7);
+        w[p] = pack_half2(h[k0], h[k0 + 8]);
+    }
+    uint4 *dst = reinterpret_cast<uint4 *>(act_row + (size_t)b * 16);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    const __half hi = __float2half_rn(s);
+    sh[b] = hi;
+    sl[b] = __float2half_rn(s - __half2float(hi));
+}
+
+// Block-wide max of non-negative values (blockDim.x <= 1024); every thread gets the result.
+__device__ __forceinline__ float block_max_nonneg(float v, float *scratch32) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) scratch32[warp] = v;
+    __syncthreads();
+    float m = 0.0f;
+    for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, scratch32[w]);
+    return m;
 }
 
 }  // namespace q2v

@@ -12,11 +12,15 @@
 //                weights, a deterministic counting sort of the (row, slot) pairs by expert
 //                (pairs of one expert ordered by row), the list of active experts;
 //   2. prep X:   the activation rows in the small-M GEMM's B-operand layout;
-//   3. gate/up:  one grouped GEMM over (active expert, gate|up, 16-row tile) items; every
-//                expert's weights are read once for all rows routed to it;
-//   4. prep h:   h = silu(gate) * up, fused into the B-operand prep of the down GEMM;
-//   5. down:     grouped GEMM over (active expert, 16-row tile) items;
-//   6. combine:  Y[r] = sum over slots, in slot order, of g * out (deterministic).
+//   3. gate/up:  one grouped GEMM over units (active expert, gate|up, 16-row group, K split);
+//                each warp streams whole units with a one-tile register lookahead, with no
+//                shared memory and no barriers; every active expert's weights are read
+//                once for all rows routed to it;
+//   4. prep h:   h = silu(sum of gate splits) * (sum of up splits), fused into the B-operand
+//                prep of the down GEMM;
+//   5. down:     the same grouped GEMM over (active expert, 16-row group, K split) units;
+//   6. combine:  Y[r] = sum over slots, in slot order, of g * (sum of the down splits).
+// Every sum runs in a fixed order, so the result is deterministic.
 #include <math.h>
 
 #include "q2v_kernels.cuh"
@@ -29,6 +33,8 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(MoeArgs a, Moe
     __shared__ int s_ids[64 * 16];
     __shared__ float s_g[64 * 16];
     __shared__ int s_cnt[257];
+    pdl_wait();
+    pdl_trigger();
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
     const int E = a.E, K = a.topk, M = a.M;
     for (int e = tid; e <= E; e += blockDim.x) s_cnt[e] = 0;
@@ -104,152 +110,310 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(MoeArgs a, Moe
     }
 }
 
-// h = silu(gate) * up for the grouped pairs, written straight into the down GEMM's
-// B-operand layout (one CTA per pair; same scaling rules as prep_act_kernel).
-__global__ void __launch_bounds__(256) moe_prep_h_kernel(const float *__restrict__ gu, int P, int F,
+
+// h for grouped pair r: silu(sum_ks G[ks][r]) * sum_ks U[ks][r] (fixed order), prepared as
+// the down GEMM's B operand.  One CTA per pair, one thread per 32-element block of F.
+__global__ void __launch_bounds__(256) moe_prep_h_kernel(const float *__restrict__ gu, int P, int F, int KS,
                                                          PrepPtrs Pp, PrepLayout L) {
-    const int r = blockIdx.x;
-    if (r >= P) return;
-    const int tid = threadIdx.x;
-    __shared__ float red[8];
-    __shared__ int sexp;
-    const float *G = gu + (size_t)r * F;
-    const float *U = gu + (size_t)P * F + (size_t)r * F;
-    auto h = [&](int k) -> float {
-        const float z = G[k];
-        return z / (1.0f + expf(-z)) * U[k];
-    };
+    __shared__ float scratch[32];
+    pdl_wait();
+    pdl_trigger();
+    const int r = blockIdx.x, b = threadIdx.x;
+    float v[32];
     float mx = 0.0f;
-    for (int k = tid; k < F; k += blockDim.x) mx = fmaxf(mx, fabsf(h(k)));
+    if (b < L.nb) {
+        float g[32], u[32];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    if ((tid & 31) == 0) red[tid >> 5] = mx;
-    __syncthreads();
-    if (tid == 0) {
-        float m = 0.0f;
-        for (int w = 0; w < (int)(blockDim.x >> 5); ++w) m = fmaxf(m, red[w]);
-        sexp = act_exponent(m);
-        Pp.exps[r] = sexp;
-    }
-    __syncthreads();
-    const int e = sexp;
-    uint32_t *act = Pp.act + (size_t)r * L.act_words_per_row();
-    for (int j = tid; j < L.nbp * 16; j += blockDim.x) {
-        const int b = j >> 4, p = j & 15;
-        uint32_t v = 0;
-        if (b < L.nb) {
-            const int k0 = b * kBlockK + 16 * (p >> 3) + (p & 7);
-            v = pack_half2(__float2half_rn(ldexpf(h(k0), -e)), __float2half_rn(ldexpf(h(k0 + 8), -e)));
+        for (int j = 0; j < 32; ++j) g[j] = u[j] = 0.0f;
+        for (int ks = 0; ks < KS; ++ks) {
+            const float4 *G = reinterpret_cast<const float4 *>(gu + ((size_t)(ks * 2 + 0) * P + r) * F + (size_t)b * 32);
+            const float4 *U = reinterpret_cast<const float4 *>(gu + ((size_t)(ks * 2 + 1) * P + r) * F + (size_t)b * 32);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const float4 x = G[j], y = U[j];
+                g[4 * j] += x.x; g[4 * j + 1] += x.y; g[4 * j + 2] += x.z; g[4 * j + 3] += x.w;
+                u[4 * j] += y.x; u[4 * j + 1] += y.y; u[4 * j + 2] += y.z; u[4 * j + 3] += y.w;
+            }
         }
-        act[j] = v;
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            v[j] = g[j] / (1.0f + expf(-g[j])) * u[j];
+            mx = fmaxf(mx, fabsf(v[j]));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
     }
-    __half *sh = reinterpret_cast<__half *>(Pp.shi + (size_t)r * L.sum_words_per_row());
-    __half *sl = reinterpret_cast<__half *>(Pp.slo + (size_t)r * L.sum_words_per_row());
-    for (int b = tid; b < L.nbp; b += blockDim.x) {
-        float s = 0.0f;
-        if (b < L.nb)
-            for (int kk = 0; kk < kBlockK; ++kk) s += __half2float(__float2half_rn(ldexpf(h(b * kBlockK + kk), -e)));
-        const __half hi = __float2half_rn(s);
-        sh[b] = hi;
-        sl[b] = __float2half_rn(s - __half2float(hi));
-    }
+    const int e = act_exponent(block_max_nonneg(mx, scratch));
+    if (b == 0) Pp.exps[r] = e;
+    if (b < L.nbp)
+        prep_store_block(v, e, Pp.act + (size_t)r * L.act_words_per_row(),
+                         reinterpret_cast<__half *>(Pp.shi + (size_t)r * L.sum_words_per_row()),
+                         reinterpret_cast<__half *>(Pp.slo + (size_t)r * L.sum_words_per_row()), b);
 }
 
-// Grouped small-M GEMM over work items (active expert, matrix, 16-row tile).
-//   GATEUP: matrices {Wg, Wu} [E][F][H/32], K = H, activation col c of expert e is the
-//           prepared X row pair_row[offsets[e] + c]; output gu[matrix][pos][F].
-//   DOWN:   matrix Wd [E][H][F/32], K = F, activation col c is prepared h row
-//           offsets[e] + c; output out[pos][H].
-// Each CTA takes a contiguous range of items (so consecutive items share an expert).
+// Grouped small-M GEMM over units u = (active expert, matrix, 16-row group, K split),
+// enumerated expert-major.
+//   GATEUP: matrices {Wg, Wu} [E][F][H/32], K = H; activation column c of expert e is the
+//           prepared X row pair_row[offsets[e] + c]; output gu[ks][matrix][pos][F].
+//   DOWN:   matrix Wd [E][H][F/32], K = F; activation column c is prepared h row
+//           offsets[e] + c; output out[ks][pos][H].
+// Each CTA takes a contiguous range of units.  Within it, for each run of units of one
+// expert (and each slice of 8 of its rows), the CTA stages those rows' prepared
+// activations in shared memory once; its warps then take the run's units round-robin and
+// stream their weight tiles with two tiles in flight ahead of the one being computed.
+// Accumulators never leave the warp: each unit's 16 x 8 partial result is written straight
+// to its K-split slot, so there are no cross-warp reductions.
+struct UnitInfo {
+    const uint8_t *W0;
+    int rows_valid, n0, t0, t1, mat, ks, ai;
+};
+
+template <bool GATEUP>
+struct UnitMap {
+    FastDiv per_expert, groups, KS;
+    int tps, ntk, Nrows;
+    size_t row_bytes, mat_bytes;
+    const uint8_t *Wg, *Wu, *Wd;
+    const int *active;
+    __device__ UnitInfo operator()(int u) const {
+        UnitInfo ui;
+        ui.ai = (int)per_expert.div((uint32_t)u);
+        const uint32_t rem = (uint32_t)u - (uint32_t)ui.ai * per_expert.d;
+        const uint32_t r1 = KS.div(rem);
+        ui.ks = (int)(rem - r1 * KS.d);
+        ui.mat = (int)groups.div(r1);
+        const int grp = (int)(r1 - (uint32_t)ui.mat * groups.d);
+        const int e = active[ui.ai];
+        ui.n0 = grp * kRowsPerCta;
+        ui.rows_valid = min(kRowsPerCta, Nrows - ui.n0);
+        ui.t0 = ui.ks * tps;
+        ui.t1 = min(ntk, ui.t0 + tps);
+        const uint8_t *Wm = GATEUP ? (ui.mat ? Wu : Wg) : Wd;
+        ui.W0 = Wm + (size_t)e * mat_bytes + (size_t)ui.n0 * row_bytes;
+        return ui;
+    }
+};
+
 template <bool GATEUP, bool ALIGN8>
-__global__ void __launch_bounds__(1024) moe_grouped_kernel(MoeArgs a, MoeWs w, float *__restrict__ outp) {
-    __shared__ float red[kMaxTileWarps * kRowsPerCta * 8];
+__global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, int KS, int ncols,
+                                                            float *__restrict__ outp) {
+    extern __shared__ __align__(16) uint32_t sm_act[];
+    __shared__ int s_active[257];
+    __shared__ int s_off[256];
+    __shared__ int s_cnt[256];
+    __shared__ int s_prow[64 * 16];
+    __shared__ int s_rows[8], s_exps[8];
+    pdl_wait();
+    pdl_trigger();
+    const int P = a.M * a.topk;
+    for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_active[i] = w.active[i];
+    for (int i = threadIdx.x; i < a.E; i += blockDim.x) {
+        s_off[i] = w.offsets[i];
+        s_cnt[i] = w.counts[i];
+    }
+    if (GATEUP)
+        for (int i = threadIdx.x; i < P; i += blockDim.x) s_prow[i] = w.pair_row[i];
+    __syncthreads();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
     const int K = GATEUP ? a.H : a.F;
-    const int Nrows = GATEUP ? a.F : a.H;
     const PrepLayout L(K);
-    const PrepPtrs &Pp = GATEUP ? w.prepX : w.prepH;
-    const int tiles = cdiv(Nrows, kRowsPerCta);
-    const int per_expert = (GATEUP ? 2 : 1) * tiles;
-    const int n_active = w.active[a.E];
-    const int total = n_active * per_expert;
+    const SmemAct SA(L, ncols);
+    const PrepPtrs &Pp0 = GATEUP ? w.prepX : w.prepH;
+    zero_column(sm_act, SA);
+    UnitMap<GATEUP> um;
+    um.Nrows = GATEUP ? a.F : a.H;
+    const int groups = cdiv(um.Nrows, kRowsPerCta);
+    const int per_expert = (GATEUP ? 2 : 1) * groups * KS;
+    um.groups = FastDiv((uint32_t)groups);
+    um.KS = FastDiv((uint32_t)KS);
+    um.per_expert = FastDiv((uint32_t)per_expert);
+    um.ntk = L.ntk;
+    um.tps = cdiv(L.ntk, KS);
+    um.row_bytes = (size_t)L.nb * kBlockBytes;
+    um.mat_bytes = (size_t)um.Nrows * um.row_bytes;
+    um.Wg = a.Wg;
+    um.Wu = a.Wu;
+    um.Wd = a.Wd;
+    um.active = s_active;
+    const int total = s_active[a.E] * per_expert;
     const int q = cdiv(total, gridDim.x);
     const int i0 = blockIdx.x * q, i1 = min(total, i0 + q);
-    const size_t row_bytes = (size_t)L.nb * kBlockBytes;
-    const size_t mat_bytes = (size_t)Nrows * row_bytes;
-    const int P = a.M * a.topk;
+    const int g = lane >> 2, t = lane & 3;
+    const int mats = GATEUP ? 2 : 1;
     bool range_bad = false;
-    for (int item = i0; item < i1; ++item) {
-        const int ai = item / per_expert, rem = item - ai * per_expert;
-        const int mat = GATEUP ? rem / tiles : 0;
-        const int tile = GATEUP ? rem - mat * tiles : rem;
-        const int e = w.active[ai];
-        const int off = w.offsets[e], cnt = w.counts[e];
-        const uint8_t *Wm = GATEUP ? (mat ? a.Wu : a.Wg) : a.Wd;
-        const int n0 = tile * kRowsPerCta;
-        const int rows_valid = min(kRowsPerCta, Nrows - n0);
-        const uint8_t *W0 = Wm + (size_t)e * mat_bytes + (size_t)n0 * row_bytes;
-        TileRegs wr;
-        if (warp < L.ntk) load_tile<ALIGN8>(wr, W0, row_bytes, rows_valid, L.nb, warp, lane);
-        float *dst = outp + (GATEUP ? (size_t)mat * P * Nrows : 0);
+
+    for (int seg0 = i0; seg0 < i1;) {
+        // the run of units of one expert
+        const int ai = seg0 / per_expert;
+        const int seg1 = min(i1, (ai + 1) * per_expert);
+        const int e = s_active[ai];
+        const int off = s_off[e], cnt = s_cnt[e];
         for (int m0 = 0; m0 < cnt; m0 += 8) {
             const int mc = min(8, cnt - m0);
-            float acc[4] = {0.f, 0.f, 0.f, 0.f};
-            if (warp < L.ntk) {
-                const int col = lane >> 2;
-                int prow = -1;
-                if (col < mc) prow = GATEUP ? w.pair_row[off + m0 + col] : off + m0 + col;
-                ActRegs ar;
-                load_act(ar, Pp, L, prow, warp, lane);
-                compute_tile(wr, ar, acc, range_bad);
-            }
-            store_fragments(red + warp * kRowsPerCta * 8, acc, lane);
-            __syncthreads();
-            for (int j = threadIdx.x; j < kRowsPerCta * mc; j += blockDim.x) {
-                const int r = j % kRowsPerCta, m = j / kRowsPerCta;
-                float s = 0.0f;
-                for (int ww = 0; ww < nwarps; ++ww) s += red[ww * kRowsPerCta * 8 + r * 8 + m];
-                const int pos = off + m0 + m;
-                const int ex = GATEUP ? Pp.exps[w.pair_row[pos]] : Pp.exps[pos];
-                if (r < rows_valid) dst[(size_t)pos * Nrows + n0 + r] = ldexpf(s, ex);
+            __syncthreads();  // the previous run's warps are done with the staged operand
+            if (threadIdx.x < 8) {
+                const int c = threadIdx.x;
+                const int r = c < mc ? (GATEUP ? s_prow[off + m0 + c] : off + m0 + c) : -1;
+                s_rows[c] = r;
+                s_exps[c] = r >= 0 ? Pp0.exps[r] : 0;
             }
             __syncthreads();
+            stage_act(sm_act, SA, Pp0, L, s_rows, mc);
+
+            // this warp's stream: units seg0 + warp, + nwarps, ...; each unit's tiles t0..t1-1.
+            // Two tile buffers with fixed names: while one is consumed the next is in flight.  A position carries what its load and its unit's epilogue need.
+            struct Pos {
+                int u, tile, t1, rv, n0, slot;  // slot = ks * mats + mat
+                const uint8_t *W0;
+            };
+            auto at_unit = [&](int uu) {
+                Pos p;
+                p.u = uu;
+                if (uu < seg1) {
+                    const UnitInfo ui = um(uu);
+                    p.tile = ui.t0;
+                    p.t1 = ui.t1;
+                    p.rv = ui.rows_valid;
+                    p.n0 = ui.n0;
+                    p.slot = ui.ks * mats + ui.mat;
+                    p.W0 = ui.W0;
+                }
+                return p;
+            };
+            auto next_pos = [&](Pos p) {
+                if (p.u >= seg1) return p;
+                if (++p.tile >= p.t1) return at_unit(p.u + nwarps);
+                return p;
+            };
+            auto issue = [&](TileRegs &buf, const Pos &p) {
+                if (p.u < seg1) load_tile<ALIGN8>(buf, p.W0, um.row_bytes, p.rv, L.nb, p.tile, lane);
+            };
+            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            auto finish_unit = [&](const Pos &p) {
+                float *dst = outp + (size_t)p.slot * P * um.Nrows;
+#pragma unroll
+                for (int qq = 0; qq < 4; ++qq) {
+                    const int c = 2 * t + (qq & 1), rr = g + 8 * (qq >> 1);
+                    if (c < mc && rr < p.rv) {
+                        const int pos = off + m0 + c;
+                        dst[(size_t)pos * um.Nrows + p.n0 + rr] = ldexpf(acc[0][qq] + acc[1][qq], s_exps[c]);
+                    }
+                    acc[0][qq] = 0.0f;
+                    acc[1][qq] = 0.0f;
+                }
+            };
+            Pos p0 = at_unit(seg0 + warp);
+            Pos p1 = next_pos(p0);
+            Pos last = p1;
+            TileRegs b0, b1;
+            issue(b0, p0);
+            issue(b1, p1);
+#define Q2V_CONSUME(BUF, POS)                                                      \
+    if (POS.u >= seg1) break;                                                      \
+    compute_tile_smem(BUF, sm_act, SA, mc, POS.tile, lane, acc, range_bad);        \
+    if (POS.tile + 1 >= POS.t1) finish_unit(POS);                                  \
+    POS = next_pos(last);                                                          \
+    last = POS;                                                                    \
+    issue(BUF, POS);
+            while (true) {
+                Q2V_CONSUME(b0, p0)
+                Q2V_CONSUME(b1, p1)
+            }
+#undef Q2V_CONSUME
         }
+        seg0 = seg1;
     }
     if (range_bad) set_status(a.status, Q2_ERR_RANGE);
 }
 
-__global__ void moe_combine_kernel(MoeArgs a, MoeWs w) {
-    const int H = a.H, K = a.topk;
+__global__ void __launch_bounds__(256) moe_combine_kernel(MoeArgs a, MoeWs w, int KS) {
+    pdl_wait();
+    pdl_trigger();
+    const int H = a.H, K = a.topk, P = a.M * a.topk;
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)a.M * H;
          i += (size_t)gridDim.x * blockDim.x) {
         const int r = (int)(i / H), n = (int)(i - (size_t)r * H);
+        int pos[16];
+        float gw[16];
+        for (int t = 0; t < K; ++t) {  // all indices first: one dependent round trip, not K
+            pos[t] = w.pair_of[r * K + t];
+            gw[t] = w.gate_w[r * K + t];
+        }
         float y = 0.0f;
         for (int t = 0; t < K; ++t) {
-            const int p = r * K + t;
-            y = fmaf(w.gate_w[p], w.out[(size_t)w.pair_of[p] * H + n], y);
+            float o = 0.0f;
+            for (int ks = 0; ks < KS; ++ks) o += w.out[((size_t)ks * P + pos[t]) * H + n];
+            y = fmaf(gw[t], o, y);
         }
         a.Y[i] = y;
     }
 }
 
+namespace {
+int g_stream_blocks[4];  // resident CTAs per SM of the four stream-kernel variants (0 = unknown)
+size_t g_stream_smem[4];  // dynamic shared memory each variant was configured for
+
+template <bool GU, bool A8>
+cudaError_t launch_stream_variant(int idx, const MoeArgs &a, const MoeWs &w, int KS, float *out, int num_sms,
+                                  size_t smem, cudaStream_t s) {
+    auto kern = moe_stream_kernel<GU, A8>;
+    if (g_stream_smem[idx] < smem) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 256, smem) != cudaSuccess || n <= 0) n = 1;
+        g_stream_blocks[idx] = n;
+        g_stream_smem[idx] = smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms * g_stream_blocks[idx]);
+    cfg.blockDim = dim3(256);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, a, w, KS, min(8, a.M), out);
+}
+
+template <bool GU>
+cudaError_t launch_stream(const MoeArgs &a, const MoeWs &w, int KS, float *out, int num_sms, const PrepLayout &L,
+                          cudaStream_t s) {
+    const size_t smem = SmemAct(L, min(8, a.M)).bytes();
+    if (L.nb % 2 == 0) return launch_stream_variant<GU, true>(GU ? 0 : 2, a, w, KS, out, num_sms, smem, s);
+    return launch_stream_variant<GU, false>(GU ? 1 : 3, a, w, KS, out, num_sms, smem, s);
+}
+
+// K splits so that the expected number of units is a few per resident warp.
+int choose_ks(int units_without_split, int ntk, int resident_warps) {
+    int ks = 1;
+    while (ks < kMaxKSplits && ks < ntk && (long long)units_without_split * ks < 4LL * resident_warps) ks *= 2;
+    return ks;
+}
+}  // namespace
+
 cudaError_t launch_moe(const MoeArgs &a, const MoeWs &w, int num_sms, cudaStream_t s) {
-    moe_route_kernel<<<1, kRouteThreads, 0, s>>>(a, w);
+    cudaError_t err = launch_pdl(moe_route_kernel, dim3(1), dim3(kRouteThreads), s, a, w);
+    if (err != cudaSuccess) return err;
     const PrepLayout LX(a.H), LH(a.F);
-    launch_prep(a.X, false, a.H, nullptr, a.M, a.H, w.prepX, LX, s);
-    const int grid = 2 * num_sms;
+    err = launch_prep_bf16(a.X, a.H, nullptr, a.M, a.H, w.prepX, LX, s);
+    if (err != cudaSuccess) return err;
     const int P = a.M * a.topk;
-    if (LX.nb % 2 == 0)
-        moe_grouped_kernel<true, true><<<grid, 32 * LX.ntk, 0, s>>>(a, w, w.h);
-    else
-        moe_grouped_kernel<true, false><<<grid, 32 * LX.ntk, 0, s>>>(a, w, w.h);
-    moe_prep_h_kernel<<<P, 256, 0, s>>>(w.h, P, a.F, w.prepH, LH);
-    if (LH.nb % 2 == 0)
-        moe_grouped_kernel<false, true><<<grid, 32 * LH.ntk, 0, s>>>(a, w, w.out);
-    else
-        moe_grouped_kernel<false, false><<<grid, 32 * LH.ntk, 0, s>>>(a, w, w.out);
-    moe_combine_kernel<<<min(cdiv(a.M * a.H, 256), 4 * num_sms), 256, 0, s>>>(a, w);
-    return cudaGetLastError();
+    const int expect_active = min(a.E, P);
+    const int resident_warps = num_sms * 24;
+    const int ks_gu = choose_ks(expect_active * 2 * cdiv(a.F, kRowsPerCta), LX.ntk, resident_warps);
+    const int ks_d = choose_ks(expect_active * cdiv(a.H, kRowsPerCta), LH.ntk, resident_warps);
+    err = launch_stream<true>(a, w, ks_gu, w.h, num_sms, LX, s);
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(moe_prep_h_kernel, dim3(P), dim3(256), s, (const float *)w.h, P, a.F, ks_gu, w.prepH, LH);
+    if (err != cudaSuccess) return err;
+    err = launch_stream<false>(a, w, ks_d, w.out, num_sms, LH, s);
+    if (err != cudaSuccess) return err;
+    return launch_pdl(moe_combine_kernel, dim3(max(1, min(cdiv(a.M * a.H, 256), 4 * num_sms))), dim3(256), s, a,
+                      w, ks_d);
 }
 
 }  // namespace q2v

@@ -18,8 +18,11 @@
 //     partials, runs the accept scan, computes its chunk's residual (or bonus) mass from
 //     one or two rows, and the last CTA of the session to finish (an atomic ticket; no
 //     CTA ever waits on another) runs the inverse-CDF search inside the selected chunk.
-// Row statistics and masses are combined across chunks in fp64; the accept ratio is
-// evaluated in fp64.
+//
+// Arithmetic is fp32 throughout (exponentials on the SFU via ex2.approx): reductions are
+// trees, and the running cumulative sums of the draws are compensated (a hi + lo pair
+// updated with an exact two-sum), so the CDF carries the accuracy of a much wider type
+// at fp32 speed.  The accept ratio is formed in the log2 domain.
 #include <math.h>
 
 #include "q2v_kernels.cuh"
@@ -32,17 +35,43 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-__device__ __forceinline__ double warp_sum_d(double v) {
+__device__ __forceinline__ float warp_sum(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
 
-__device__ __forceinline__ float warp_max_f(float v) {
+__device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
     return v;
 }
+
+// Inclusive warp scan (lane order), fp32.
+__device__ __forceinline__ float warp_incl_scan(float v, int lane) {
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const float n = __shfl_up_sync(0xffffffffu, v, o);
+        if (lane >= o) v += n;
+    }
+    return v;
+}
+
+// A compensated running sum: hi + lo, each addition exact up to the final rounding of lo
+// (Knuth's two-sum of hi and the addend).
+struct CSum {
+    float hi = 0.0f, lo = 0.0f;
+    __device__ __forceinline__ void add(float b) {
+        const float s = hi + b;
+        const float bb = s - hi;
+        const float err = (hi - (s - bb)) + (b - bb);
+        hi = s;
+        lo += err;
+    }
+    // carry + x compared with the target, without losing the low part
+    __device__ __forceinline__ bool exceeds(float x, float target) const { return hi + (lo + x) > target; }
+    __device__ __forceinline__ float value() const { return hi + lo; }
+};
 
 __device__ __forceinline__ const float *row_ptr(const PqArgs &a, int s, int r) {
     // rows 0..k: target rows; rows k+1..2k: draft rows 0..k-1
@@ -51,26 +80,28 @@ __device__ __forceinline__ const float *row_ptr(const PqArgs &a, int s, int r) {
 }
 
 // Accept scan for session s, given row maxima and log2 of row sums (rows as above).
-// Returns j in [0, k], or -1 if a draft token is out of range.
-__device__ int accept_scan(const PqArgs &a, int s, const float *rowM, const double *rowL2Z) {
+// The ratio p/q is formed in the log2 domain: ratio = 2^(lp - lq) with
+// lp = (t(x) - max_t) * beta - log2 Z_t (likewise lq), so neither probability underflows on
+// its own; q(x) == 0 exactly (a -inf draft logit) accepts.  Returns j in [0, k], or -1 if
+// a draft token is out of range.
+__device__ int accept_scan(const PqArgs &a, int s, const float *rowM, const float *rowL2Z) {
     for (int i = 0; i < a.k; ++i) {
         const int x = a.drafts[(size_t)s * a.k + i];
         if (x < 0 || x >= a.V) return -1;
     }
     for (int i = 0; i < a.k; ++i) {
         const int x = a.drafts[(size_t)s * a.k + i];
-        const double tx = (double)row_ptr(a, s, i)[x], dx = (double)row_ptr(a, s, a.k + 1 + i)[x];
-        const double lp = (tx - (double)rowM[i]) * a.beta64 - rowL2Z[i];
-        const double lq = (dx - (double)rowM[a.k + 1 + i]) * a.beta64 - rowL2Z[a.k + 1 + i];
-        const double q = exp2(lq);
-        if (q == 0.0) continue;  // q(x) == 0 accepts
-        const double ratio = exp2(lp) / q;
-        if (!((double)a.u_acc[(size_t)s * a.k + i] < ratio)) return i;
+        const float tx = row_ptr(a, s, i)[x], dx = row_ptr(a, s, a.k + 1 + i)[x];
+        if (dx == -INFINITY) continue;  // q(x) == 0 accepts
+        const float lp = (tx - rowM[i]) * a.beta - rowL2Z[i];
+        const float lq = (dx - rowM[a.k + 1 + i]) * a.beta - rowL2Z[a.k + 1 + i];
+        const float ratio = ex2(lp - lq);
+        if (!(a.u_acc[(size_t)s * a.k + i] < ratio)) return i;
     }
     return a.k;
 }
 
-// Weight of token y in the final draw.  mode 0: residual of row j; 1: p of row `rp`.
+// Weight of token y in the final draw.  mode 0: residual max(0, p_j - q_j); 1: p of row t.
 struct DrawRows {
     const float *t, *d;  // target row, draft row (d unused in mode 1)
     float mt, md;        // row maxima
@@ -97,13 +128,35 @@ __device__ __forceinline__ void write_tokens(const PqArgs &a, int s, int j, int 
     a.n_acc[s] = j;
 }
 
+__device__ __forceinline__ DrawRows draw_rows(const PqArgs &a, int s, int j, const float *rowM,
+                                              const float *rowL2Z) {
+    DrawRows D;
+    D.t = row_ptr(a, s, j);
+    D.mt = rowM[j];
+    D.lt = rowL2Z[j];
+    if (j < a.k) {
+        D.d = row_ptr(a, s, a.k + 1 + j);
+        D.md = rowM[a.k + 1 + j];
+        D.ld = rowL2Z[a.k + 1 + j];
+        D.mode = 0;
+    } else {
+        D.d = D.t;
+        D.md = D.mt;
+        D.ld = D.lt;
+        D.mode = 1;
+    }
+    return D;
+}
+
 // ===================================================================== small-V tier
 
 constexpr int kWarpTierWarps = 8;
 
 __global__ void __launch_bounds__(kWarpTierWarps * 32) pqv_warp_kernel(PqArgs a) {
     __shared__ float sM[kWarpTierWarps][kMaxRows];
-    __shared__ double sL2Z[kWarpTierWarps][kMaxRows];
+    __shared__ float sL2Z[kWarpTierWarps][kMaxRows];
+    pdl_wait();
+    pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int R = 2 * a.k + 1;
     const float beta = a.beta;
@@ -120,12 +173,11 @@ __global__ void __launch_bounds__(kWarpTierWarps * 32) pqv_warp_kernel(PqArgs a)
                     z += ex2((v - m) * beta);
                 }
             }
-            const float M = warp_max_f(m);
-            double zz = (m > -INFINITY) ? (double)z * (double)ex2((m - M) * beta) : 0.0;
-            zz = warp_sum_d(zz);
+            const float M = warp_max(m);
+            const float zz = warp_sum((m > -INFINITY) ? z * ex2((m - M) * beta) : 0.0f);
             if (lane == 0) {
                 sM[warp][r] = M;
-                sL2Z[warp][r] = log2(zz);
+                sL2Z[warp][r] = log2f(zz);
             }
         }
         __syncwarp();
@@ -136,7 +188,7 @@ __global__ void __launch_bounds__(kWarpTierWarps * 32) pqv_warp_kernel(PqArgs a)
             for (int r = 0; r < R; ++r) {
                 const float *x = row_ptr(a, s, r);
                 float *o = a.probs + ((size_t)s * R + r) * a.V;
-                const float M = sM[warp][r], L2 = (float)sL2Z[warp][r];
+                const float M = sM[warp][r], L2 = sL2Z[warp][r];
                 for (int y = lane; y < a.V; y += 32) o[y] = ex2((x[y] - M) * beta - L2);
             }
         }
@@ -148,59 +200,31 @@ __global__ void __launch_bounds__(kWarpTierWarps * 32) pqv_warp_kernel(PqArgs a)
             __syncwarp();
             continue;
         }
-        DrawRows D;
-        const int jr = j;  // target row of the draw
-        D.t = row_ptr(a, s, jr);
-        D.mt = sM[warp][jr];
-        D.lt = (float)sL2Z[warp][jr];
-        if (j < a.k) {
-            D.d = row_ptr(a, s, a.k + 1 + j);
-            D.md = sM[warp][a.k + 1 + j];
-            D.ld = (float)sL2Z[warp][a.k + 1 + j];
-            D.mode = 0;
-        } else {
-            D.d = D.t;
-            D.md = D.mt;
-            D.ld = D.lt;
-            D.mode = 1;
-        }
-        // pass 1: total mass (chunks of 32 scanned exactly as in pass 2)
-        double total = 0.0;
+        DrawRows D = draw_rows(a, s, j, sM[warp], sL2Z[warp]);
+        // pass 1: the total mass, scanned in chunks of 32 exactly as pass 2 scans
+        CSum total;
         for (int pass = 0; pass < 2; ++pass) {
-            total = 0.0;
+            total = CSum();
             for (int base = 0; base < a.V; base += 32) {
                 const int y = base + lane;
-                float w = 0.0f;
-                if (y < a.V) w = draw_weight(D, beta, D.t[y], D.d[y]);
-                float incl = w;
-#pragma unroll
-                for (int o = 1; o < 32; o <<= 1) {
-                    const float n = __shfl_up_sync(0xffffffffu, incl, o);
-                    if (lane >= o) incl += n;
-                }
-                total += (double)__shfl_sync(0xffffffffu, incl, 31);
+                const float w = y < a.V ? draw_weight(D, beta, D.t[y], D.d[y]) : 0.0f;
+                total.add(__shfl_sync(0xffffffffu, warp_incl_scan(w, lane), 31));
             }
-            if (total > 0.0 || D.mode == 1) break;
+            if (total.value() > 0.0f || D.mode == 1) break;
             D.mode = 1;  // zero residual mass: draw from p_j
         }
-        const double target = (double)a.u_fin[s] * total;
-        double carry = 0.0;
+        const float target = a.u_fin[s] * total.value();
+        CSum carry;
         int y_sel = -1, last_pos = -1;
         for (int base = 0; base < a.V && y_sel < 0; base += 32) {
             const int y = base + lane;
-            float w = 0.0f;
-            if (y < a.V) w = draw_weight(D, beta, D.t[y], D.d[y]);
-            float incl = w;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const float n = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += n;
-            }
-            const unsigned hit = __ballot_sync(0xffffffffu, w > 0.0f && carry + (double)incl > target);
+            const float w = y < a.V ? draw_weight(D, beta, D.t[y], D.d[y]) : 0.0f;
+            const float incl = warp_incl_scan(w, lane);
+            const unsigned hit = __ballot_sync(0xffffffffu, w > 0.0f && carry.exceeds(incl, target));
             const unsigned pos = __ballot_sync(0xffffffffu, w > 0.0f);
             if (pos) last_pos = base + 31 - __clz(pos);
             if (hit) y_sel = base + __ffs(hit) - 1;
-            carry += (double)__shfl_sync(0xffffffffu, incl, 31);
+            carry.add(__shfl_sync(0xffffffffu, incl, 31));
         }
         if (y_sel < 0) y_sel = last_pos;
         if (lane == 0) write_tokens(a, s, j, y_sel);
@@ -214,6 +238,8 @@ __global__ void __launch_bounds__(kWarpTierWarps * 32) pqv_warp_kernel(PqArgs a)
 // rows w, w + nwarps, ...
 template <bool VEC>
 __global__ void __launch_bounds__(512) pqv_stats_kernel(PqArgs a, PqSplit sp) {
+    pdl_wait();
+    pdl_trigger();
     const int c = blockIdx.x, s = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
     const int R = 2 * a.k + 1;
@@ -259,10 +285,8 @@ __global__ void __launch_bounds__(512) pqv_stats_kernel(PqArgs a, PqSplit sp) {
                 }
             }
         }
-        const float M = warp_max_f(m);
-        float zz = (m > -INFINITY) ? z * ex2((m - M) * beta) : 0.0f;
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) zz += __shfl_xor_sync(0xffffffffu, zz, o);
+        const float M = warp_max(m);
+        const float zz = warp_sum((m > -INFINITY) ? z * ex2((m - M) * beta) : 0.0f);
         if (lane == 0) {
             float2 *st = reinterpret_cast<float2 *>(sp.stats) + ((size_t)s * R + r) * sp.C + c;
             *st = make_float2(M, zz);
@@ -270,13 +294,14 @@ __global__ void __launch_bounds__(512) pqv_stats_kernel(PqArgs a, PqSplit sp) {
     }
 }
 
-__device__ __forceinline__ double block_sum_d(double v, double *scratch) {
+// Sum over the block (tree in fp32); every thread gets the total.
+__device__ __forceinline__ float block_sum(float v, float *scratch) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    v = warp_sum_d(v);
+    v = warp_sum(v);
     __syncthreads();
     if (lane == 0) scratch[warp] = v;
     __syncthreads();
-    double t = 0.0;
+    float t = 0.0f;
     for (int w = 0; w < nw; ++w) t += scratch[w];
     return t;
 }
@@ -285,30 +310,32 @@ __device__ __forceinline__ double block_sum_d(double v, double *scratch) {
 template <bool VEC>
 __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
     __shared__ float rowM[kMaxRows];
-    __shared__ double rowL2Z[kMaxRows];
-    __shared__ double scratch[32];
+    __shared__ float rowL2Z[kMaxRows];
+    __shared__ float scratch[32];
     __shared__ int s_j, s_last, s_y, s_lastpos;
+    pdl_wait();
+    pdl_trigger();
     const int c = blockIdx.x, s = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
     const int R = 2 * a.k + 1;
     const float beta = a.beta;
     const int c0 = c * sp.L, c1 = min(a.V, c0 + sp.L);
 
-    // 1. row statistics from the chunk partials (fp64 sums)
+    // 1. row statistics from the chunk partials
     for (int r = warp; r < R; r += nwarps) {
         const float2 *st = reinterpret_cast<const float2 *>(sp.stats) + ((size_t)s * R + r) * sp.C;
         float m = -INFINITY;
         for (int cc = lane; cc < sp.C; cc += 32) m = fmaxf(m, st[cc].x);
-        m = warp_max_f(m);
-        double z = 0.0;
+        m = warp_max(m);
+        float z = 0.0f;
         for (int cc = lane; cc < sp.C; cc += 32) {
             const float2 v = st[cc];
-            if (v.x > -INFINITY) z += (double)v.y * exp2((double)(v.x - m) * a.beta64);
+            if (v.x > -INFINITY) z += v.y * ex2((v.x - m) * beta);
         }
-        z = warp_sum_d(z);
+        z = warp_sum(z);
         if (lane == 0) {
             rowM[r] = m;
-            rowL2Z[r] = log2(z);
+            rowL2Z[r] = log2f(z);
         }
     }
     __syncthreads();
@@ -321,7 +348,7 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
         for (int r = 0; r < R; ++r) {
             const float *x = row_ptr(a, s, r);
             float *o = a.probs + ((size_t)s * R + r) * a.V;
-            const float M = rowM[r], L2 = (float)rowL2Z[r];
+            const float M = rowM[r], L2 = rowL2Z[r];
             for (int y = c0 + tid; y < c1; y += blockDim.x) o[y] = ex2((x[y] - M) * beta - L2);
         }
     }
@@ -332,21 +359,7 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
         }
         return;
     }
-    DrawRows D;
-    D.t = row_ptr(a, s, j);
-    D.mt = rowM[j];
-    D.lt = (float)rowL2Z[j];
-    if (j < a.k) {
-        D.d = row_ptr(a, s, a.k + 1 + j);
-        D.md = rowM[a.k + 1 + j];
-        D.ld = (float)rowL2Z[a.k + 1 + j];
-        D.mode = 0;
-    } else {
-        D.d = D.t;
-        D.md = D.mt;
-        D.ld = D.lt;
-        D.mode = 1;
-    }
+    DrawRows D = draw_rows(a, s, j, rowM, rowL2Z);
     // 3. this chunk's draw mass (and p_j mass for the zero-residual fallback)
     float wsum = 0.0f, psum = 0.0f;
     if (VEC) {
@@ -370,8 +383,8 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
             if (D.mode == 0) psum += ex2((xt - D.mt) * beta - D.lt);
         }
     }
-    const double wtot = block_sum_d((double)wsum, scratch);
-    const double ptot = block_sum_d((double)psum, scratch);
+    const float wtot = block_sum(wsum, scratch);
+    const float ptot = block_sum(psum, scratch);
     if (tid == 0) {
         sp.mass[(size_t)s * sp.C + c] = wtot;
         sp.pmass[(size_t)s * sp.C + c] = ptot;
@@ -383,78 +396,108 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
     if (!s_last) return;
     __threadfence();
 
-    // 4. last CTA of the session: pick the chunk, then the token inside it
-    __shared__ double s_prefix, s_target;
+    // 4. last CTA of the session: pick the chunk (all chunk masses loaded in parallel, then
+    //    one warp scans them as 32 contiguous segments), then the token inside it
+    __shared__ float s_mass[kMaxChunks], s_pmass[kMaxChunks];
+    __shared__ float s_prefix_hi, s_prefix_lo, s_target;
     __shared__ int s_chunk, s_mode;
-    if (tid == 0) {
-        const volatile double *mm = sp.mass + (size_t)s * sp.C;
+    for (int cc = tid; cc < sp.C; cc += blockDim.x) {
+        s_mass[cc] = __ldcg(sp.mass + (size_t)s * sp.C + cc);
+        s_pmass[cc] = __ldcg(sp.pmass + (size_t)s * sp.C + cc);
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const int q = cdiv(sp.C, 32);
+        const int cs0 = min(sp.C, lane * q), cs1 = min(sp.C, cs0 + q);
         int mode = D.mode;
-        double total = 0.0;
-        for (int cc = 0; cc < sp.C; ++cc) total += mm[cc];
-        if (mode == 0 && !(total > 0.0)) {  // zero residual mass: draw from p_j
+        const float *mm = s_mass;
+        float seg = 0.0f;
+        for (int cc = cs0; cc < cs1; ++cc) seg += mm[cc];
+        float tot = warp_sum(seg);
+        if (mode == 0 && !(tot > 0.0f)) {  // zero residual mass: draw from p_j
             mode = 1;
-            mm = sp.pmass + (size_t)s * sp.C;
-            total = 0.0;
-            for (int cc = 0; cc < sp.C; ++cc) total += mm[cc];
+            mm = s_pmass;
+            seg = 0.0f;
+            for (int cc = cs0; cc < cs1; ++cc) seg += mm[cc];
+            tot = warp_sum(seg);
         }
-        const double target = (double)a.u_fin[s] * total;
-        double prefix = 0.0, last_prefix = 0.0;
-        int chunk = -1, last_nz = -1;
-        for (int cc = 0; cc < sp.C; ++cc) {
-            const double mc = mm[cc];
-            if (mc > 0.0) {
-                last_nz = cc;
-                last_prefix = prefix;
-                if (prefix + mc > target) {
-                    chunk = cc;
-                    break;
+        const float target = a.u_fin[s] * tot;
+        const float incl = warp_incl_scan(seg, lane);
+        float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+        if (lane == 0) excl = 0.0f;
+        const unsigned hit = __ballot_sync(0xffffffffu, seg > 0.0f && excl + seg > target);
+        const unsigned pos = __ballot_sync(0xffffffffu, seg > 0.0f);
+        // the lane whose segment holds the crossing; if rounding put the target past the
+        // end, the last lane with mass (its last chunk with mass is taken)
+        const int owner = hit ? (__ffs(hit) - 1) : (pos ? 31 - __clz(pos) : -1);
+        int chunk = -1;
+        CSum prefix;
+        if (lane == owner) {
+            CSum pre;
+            pre.add(excl);
+            int last_nz = -1;
+            CSum last_pre;
+            for (int cc = cs0; cc < cs1; ++cc) {
+                const float mc = mm[cc];
+                if (mc > 0.0f) {
+                    last_nz = cc;
+                    last_pre = pre;
+                    if (hit && pre.exceeds(mc, target)) {
+                        chunk = cc;
+                        prefix = pre;
+                        break;
+                    }
                 }
+                pre.add(mc);
             }
-            prefix += mc;
+            if (chunk < 0) {
+                chunk = last_nz;
+                prefix = last_pre;
+            }
         }
-        if (chunk < 0) {  // rounding put the target past the end: the last chunk with mass
-            chunk = last_nz;
-            prefix = last_prefix;
+        if (owner >= 0) {
+            chunk = __shfl_sync(0xffffffffu, chunk, owner);
+            prefix.hi = __shfl_sync(0xffffffffu, prefix.hi, owner);
+            prefix.lo = __shfl_sync(0xffffffffu, prefix.lo, owner);
         }
-        s_chunk = chunk;
-        s_prefix = prefix;
-        s_target = target;
-        s_mode = mode;
-        s_y = 0x7fffffff;
-        s_lastpos = -1;
+        if (lane == 0) {
+            s_chunk = chunk;
+            s_prefix_hi = prefix.hi;
+            s_prefix_lo = prefix.lo;
+            s_target = target;
+            s_mode = mode;
+            s_y = 0x7fffffff;
+            s_lastpos = -1;
+        }
     }
     __syncthreads();
     D.mode = s_mode;
     const int cs = s_chunk;
     if (cs >= 0) {
-        const double tgt = s_target;
+        const float tgt = s_target;
         const int y0 = cs * sp.L, y1 = min(a.V, y0 + sp.L);
-        double carry = s_prefix;
+        CSum carry;
+        carry.hi = s_prefix_hi;
+        carry.lo = s_prefix_lo;
         for (int base = y0; base < y1; base += blockDim.x) {
             const int y = base + tid;
-            float w = 0.0f;
-            if (y < y1) w = draw_weight(D, beta, D.t[y], D.d[y]);
-            // block inclusive scan of w in fp64 (thread order is token order)
-            double incl = (double)w;
-#pragma unroll
-            for (int o = 1; o < 32; o <<= 1) {
-                const double n = __shfl_up_sync(0xffffffffu, incl, o);
-                if (lane >= o) incl += n;
-            }
+            const float w = y < y1 ? draw_weight(D, beta, D.t[y], D.d[y]) : 0.0f;
+            // block inclusive scan of w (thread order is token order)
+            const float incl = warp_incl_scan(w, lane);
             if (lane == 31) scratch[warp] = incl;
             __syncthreads();
-            double woff = 0.0, tile_total = 0.0;
+            float woff = 0.0f, tile_total = 0.0f;
             for (int ww = 0; ww < nwarps; ++ww) {
                 if (ww < warp) woff += scratch[ww];
                 tile_total += scratch[ww];
             }
             if (w > 0.0f) {
                 atomicMax(&s_lastpos, y);
-                if (carry + woff + incl > tgt) atomicMin(&s_y, y);
+                if (carry.exceeds(woff + incl, tgt)) atomicMin(&s_y, y);
             }
             __syncthreads();
             if (s_y != 0x7fffffff) break;
-            carry += tile_total;
+            carry.add(tile_total);
         }
     }
     __syncthreads();
@@ -468,21 +511,21 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
 cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier, int num_sms, cudaStream_t st) {
     if (warp_tier) {
         const int blocks = max(1, min(cdiv(a.S, kWarpTierWarps), num_sms * 8));
-        pqv_warp_kernel<<<blocks, kWarpTierWarps * 32, 0, st>>>(a);
-        return cudaGetLastError();
+        return launch_pdl(pqv_warp_kernel, dim3(blocks), dim3(kWarpTierWarps * 32), st, a);
     }
     const bool vec = (a.V % 4) == 0 && (sp.L % 4) == 0;
     const int R = 2 * a.k + 1;
     const dim3 grid(sp.C, a.S);
     const int warps1 = min(R, 16);
+    cudaError_t e;
     if (vec) {
-        pqv_stats_kernel<true><<<grid, warps1 * 32, 0, st>>>(a, sp);
-        pqv_verify_kernel<true><<<grid, 256, 0, st>>>(a, sp);
+        e = launch_pdl(pqv_stats_kernel<true>, grid, dim3(warps1 * 32), st, a, sp);
+        if (e == cudaSuccess) e = launch_pdl(pqv_verify_kernel<true>, grid, dim3(256), st, a, sp);
     } else {
-        pqv_stats_kernel<false><<<grid, warps1 * 32, 0, st>>>(a, sp);
-        pqv_verify_kernel<false><<<grid, 256, 0, st>>>(a, sp);
+        e = launch_pdl(pqv_stats_kernel<false>, grid, dim3(warps1 * 32), st, a, sp);
+        if (e == cudaSuccess) e = launch_pdl(pqv_verify_kernel<false>, grid, dim3(256), st, a, sp);
     }
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace q2v
