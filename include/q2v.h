@@ -167,6 +167,28 @@ q2_status pq_verify(const float *target_logits, const float *draft_logits,
                     int32_t *out_tokens, float *probs_out, void *ws, size_t ws_bytes,
                     q2_stream_t stream);
 
+/*
+ * pq_verify without a workspace, for callers that cannot allocate device memory: e.g. a
+ * decode loop inside a host framework whose memory pool already owns the device, so it has
+ * no buffer to lend and must not call cudaMalloc (which can stall the device, or fail under
+ * a reserved pool).  The pages have no counterpart of this entry point; it is a library
+ * convenience.
+ *
+ * Arguments and results are those of pq_verify, minus ws/ws_bytes.  The scratch is a fixed
+ * 2 MiB array in device memory that the library holds on every device that loads it, until
+ * the process exits; nothing is allocated.  Sizes whose pq_verify_workspace(S, k, V) exceeds
+ * 2 MiB are refused with Q2_ERR_UNSUPPORTED before anything is enqueued (S = 24 sessions of
+ * k = 4 drafts at V = 129,280 fit).  The first call on a device looks up the array's device
+ * address once (make that first call before any stream capture).  Every call shares the one
+ * array and clears its status word; calls that may overlap on the GPU (other streams,
+ * other host threads) race on it and must be ordered by the caller.  Device-detected errors
+ * show in the outputs: a session with a draft token outside [0, V) gets n_accepted = -1.
+ */
+q2_status pq_verify_noalloc(const float *target_logits, const float *draft_logits,
+                            const int32_t *draft_tokens, const float *u_acc, const float *u_fin,
+                            int S, int k, int V, float temperature, int32_t *n_accepted,
+                            int32_t *out_tokens, float *probs_out, q2_stream_t stream);
+
 /* ------------------------------------------------------------------ status */
 
 /* Synchronise `stream`, read the device status word of workspace `ws`, clear it, and

@@ -22,7 +22,8 @@ STATUS_NAMES = {0: "Q2_OK", 1: "Q2_ERR_INVALID_ARG", 2: "Q2_ERR_ALIGNMENT", 3: "
                 8: "Q2_ERR_RANGE"}
 MOE_RENORMALIZE = 1
 EXPORTS = ("q2_tiny_gemm_workspace", "q2_tiny_gemm", "q2_moe_grouped_workspace", "q2_moe_grouped",
-           "pq_verify_workspace", "pq_verify", "q2_get_device_status", "q2_status_string", "q2_version")
+           "pq_verify_workspace", "pq_verify", "pq_verify_noalloc", "q2_get_device_status", "q2_status_string",
+           "q2_version")
 
 
 class Q2Error(RuntimeError):
@@ -57,6 +58,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pq_verify_workspace.restype = Z
     lib.pq_verify.argtypes = [P, P, P, P, P, I, I, I, F, P, P, P, P, Z, P]
     lib.pq_verify.restype = I
+    lib.pq_verify_noalloc.argtypes = [P, P, P, P, P, I, I, I, F, P, P, P, P]
+    lib.pq_verify_noalloc.restype = I
     lib.q2_get_device_status.argtypes = [P, P]
     lib.q2_get_device_status.restype = I
     lib.q2_status_string.argtypes = [I]
@@ -209,4 +212,29 @@ def pq_verify(target: torch.Tensor, draft: torch.Tensor | None, drafts: torch.Te
                           _ptr(n_acc), _ptr(tokens), _ptr(probs), _ptr(ws), ws.numel(),
                           ctypes.c_void_p(_stream(stream)))
     _raise(st, "pq_verify")
+    return n_acc, tokens
+
+
+def pq_verify_noalloc(target: torch.Tensor, draft: torch.Tensor | None, drafts: torch.Tensor | None,
+                      u_acc: torch.Tensor | None, u_fin: torch.Tensor, temperature: float,
+                      n_acc: torch.Tensor, tokens: torch.Tensor, probs: torch.Tensor | None = None,
+                      stream=None):
+    """pq_verify with the library's fixed scratch instead of a workspace, for callers that
+    cannot allocate device memory.  The caller provides every output tensor (nothing is
+    allocated here either).  Returns (n_acc, tokens)."""
+    _check(target, "target", torch.float32)
+    S, k1, V = target.shape
+    k = k1 - 1
+    if k > 0:
+        _check(draft, "draft", torch.float32)
+        _check(drafts, "drafts", torch.int32)
+        _check(u_acc, "u_acc", torch.float32)
+    _check(u_fin, "u_fin", torch.float32)
+    _check(n_acc, "n_acc", torch.int32)
+    _check(tokens, "tokens", torch.int32)
+    _check(probs, "probs", torch.float32, nullable=True)
+    st = load().pq_verify_noalloc(_ptr(target), _ptr(draft) if k > 0 else None, _ptr(drafts) if k > 0 else None,
+                                  _ptr(u_acc) if k > 0 else None, _ptr(u_fin), S, k, V, float(temperature),
+                                  _ptr(n_acc), _ptr(tokens), _ptr(probs), ctypes.c_void_p(_stream(stream)))
+    _raise(st, "pq_verify_noalloc")
     return n_acc, tokens
