@@ -73,8 +73,8 @@ PqCarve pq_carve(void *ws, int S, int k, int V) {
     PqCarve r{};
     const size_t R = 2 * (size_t)k + 1, C = pq_cmax(V);
     r.stats = static_cast<float *>(c.take((size_t)S * R * C * 2 * sizeof(float)));
-    r.mass = static_cast<float *>(c.take((size_t)S * C * sizeof(float)));
-    r.pmass = static_cast<float *>(c.take((size_t)S * C * sizeof(float)));
+    r.mass = static_cast<float *>(c.take((size_t)S * C * kSegsPerChunk * sizeof(float)));
+    r.pmass = static_cast<float *>(c.take((size_t)S * C * kSegsPerChunk * sizeof(float)));
     r.tickets = static_cast<unsigned int *>(c.take((size_t)S * sizeof(unsigned int)));
     r.bytes = c.off;
     return r;

@@ -86,7 +86,6 @@ __global__ void __launch_bounds__(kGemmWarps * 32) q2_gemm_mma_kernel(const uint
     pdl_wait();
     pdl_trigger();
     const SmemAct SA(L, ncols);
-    zero_column(sm_act, SA);
     bool range_bad = false;
     for (int m0 = 0; m0 < M; m0 += 8) {
         const int mc = min(8, M - m0);

@@ -20,6 +20,7 @@ constexpr int kMaxRows = 2 * kMaxDrafts + 1;
 constexpr int kWarpTierMaxV = 4096;   // sessions with V at most this use one warp each
 constexpr int kChunkAlign = 128;      // chunk lengths are multiples of this (float4 x 32 lanes)
 constexpr int kMaxChunks = 1024;      // chunks per session (workspace sizing bound)
+constexpr int kSegsPerChunk = 8;      // warp segments per chunk (one per warp of the verify CTA)
 
 struct PqArgs {
     const float *target;
@@ -39,8 +40,8 @@ struct PqSplit {
     int C;               // chunks per session
     int L;               // chunk length (multiple of kChunkAlign)
     float *stats;        // [S][2k+1][C] float2 (max, sum)
-    float *mass;         // [S][C] draw mass of each chunk
-    float *pmass;        // [S][C] p_j mass of each chunk (zero-residual fallback)
+    float *mass;         // [S][C][8] draw mass of each warp segment of each chunk
+    float *pmass;        // [S][C][8] p_j mass of each segment (zero-residual fallback)
     unsigned int *tickets;  // [S]
 };
 

@@ -76,6 +76,17 @@ __device__ __forceinline__ void load_tile(TileRegs &r, const uint8_t *__restrict
                                           int rows_valid, int nb, int tile, int lane) {
     const int g = lane >> 2, t = lane & 3;
     const int b0 = tile * kTileBlocks + 2 * t;
+    if (ALIGN8 && rows_valid == kRowsPerCta && (tile + 1) * kTileBlocks <= nb) {
+        // a whole tile: no predicates
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            const uint2 *p = reinterpret_cast<const uint2 *>(W0 + (size_t)(g + 8 * rr) * row_bytes + (size_t)b0 * kBlockBytes);
+            const uint2 x0 = __ldg(p), x1 = __ldg(p + 1), x2 = __ldg(p + 2);
+            r.w[rr][0][0] = x0.x; r.w[rr][0][1] = x0.y; r.w[rr][0][2] = x1.x;
+            r.w[rr][1][0] = x1.y; r.w[rr][1][1] = x2.x; r.w[rr][1][2] = x2.y;
+        }
+        return;
+    }
 #pragma unroll
     for (int rr = 0; rr < 2; ++rr) {
         const int row = g + 8 * rr;
@@ -105,10 +116,68 @@ __device__ __forceinline__ void load_tile(TileRegs &r, const uint8_t *__restrict
     }
 }
 
+// A whole tile from per-thread row pointers (blocks 2t, 2t+1 of rows g and g+8, 8-byte
+// aligned rows): three 8-byte loads per row, no predicates.
+__device__ __forceinline__ void load_tile_fast(TileRegs &r, const uint2 *__restrict__ pa, const uint2 *__restrict__ pb) {
+    const uint2 a0 = __ldg(pa), a1 = __ldg(pa + 1), a2 = __ldg(pa + 2);
+    const uint2 b0 = __ldg(pb), b1 = __ldg(pb + 1), b2 = __ldg(pb + 2);
+    r.w[0][0][0] = a0.x; r.w[0][0][1] = a0.y; r.w[0][0][2] = a1.x;
+    r.w[0][1][0] = a1.y; r.w[0][1][1] = a2.x; r.w[0][1][2] = a2.y;
+    r.w[1][0][0] = b0.x; r.w[1][0][1] = b0.y; r.w[1][0][2] = b1.x;
+    r.w[1][1][0] = b1.y; r.w[1][1][1] = b2.x; r.w[1][1][2] = b2.y;
+}
+
+// ---------------------------------------------------------------- asynchronous copies
+
+__device__ __forceinline__ void cp_async8(void *smem_dst, const void *gmem_src) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 8;\n" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void *smem_dst, const void *gmem_src) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(d), "l"(gmem_src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() { asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory"); }
+__device__ __forceinline__ void cp_async4(void *smem_dst, const void *gmem_src) {
+    const unsigned d = (unsigned)__cvta_generic_to_shared(smem_dst);
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;\n" ::"r"(d), "l"(gmem_src) : "memory");
+}
+
+// A weight tile staged in shared memory as 16 rows x 96 bytes (the tile's 8 blocks of each
+// row, copied with 16-byte asynchronous copies: lane l brings 48 bytes of row l/2).  Thread
+// (g, t) then reads blocks 2t, 2t+1 of rows g and g+8: three 8-byte loads per row; rows are
+// 24 words apart, so each load instruction touches every bank exactly twice.
+constexpr int kTileRowWords = 24;
+constexpr int kTileWords = kRowsPerCta * kTileRowWords;
+
+__device__ __forceinline__ void issue_tile_cpasync(uint32_t *stage, const uint8_t *W0, size_t row_bytes, int tile,
+                                                   int lane) {
+    const int row = lane >> 1, half = lane & 1;
+    const uint8_t *src = W0 + (size_t)row * row_bytes + (size_t)tile * (kTileBlocks * kBlockBytes) + half * 48;
+    uint32_t *dst = stage + row * kTileRowWords + half * 12;
+    cp_async16(dst, src);
+    cp_async16(dst + 4, src + 16);
+    cp_async16(dst + 8, src + 32);
+}
+
+__device__ __forceinline__ void read_tile_smem(TileRegs &r, const uint32_t *stage, int lane) {
+    const int g = lane >> 2, t = lane & 3;
+#pragma unroll
+    for (int rr = 0; rr < 2; ++rr) {
+        const uint2 *p = reinterpret_cast<const uint2 *>(stage + (g + 8 * rr) * kTileRowWords + 6 * t);
+        const uint2 x0 = p[0], x1 = p[1], x2 = p[2];
+        r.w[rr][0][0] = x0.x; r.w[rr][0][1] = x0.y; r.w[rr][0][2] = x1.x;
+        r.w[rr][1][0] = x1.y; r.w[rr][1][1] = x2.x; r.w[rr][1][2] = x2.y;
+    }
+}
+
 // ---------------------------------------------------------------- shared-memory B operand
 //
-// Staged activations for up to `ncols` columns plus one all-zero column (index ncols),
-// which every MMA column without a row reads.  Column c holds its blocks in pairs: block
+// Staged activations for up to `ncols` columns.  An MMA column without a row in the current
+// slice reads column 0: it only feeds its own output column, which is never stored (each
+// output of an MMA is one row of A times one column of B).  Column c holds its blocks in pairs: block
 // pair j = b/2 starts at word 34*j (32 words of data and 2 of skew), block b at
 // 34*(b/2) + 16*(b%2), pair slot p at + p.  A k16 step's 8-byte fragment load has threads
 // g = 0..7 on columns CS*g apart (CS == 8 mod 32) and t = 0..3 on block pairs 34 words
@@ -124,54 +193,53 @@ struct SmemAct {
         : CS((int)align_up((size_t)L.nbp / 2 * kPairWords, 32) + 8),
           SWW((int)align_up((size_t)L.nbp / 2, 32) + 4),
           ncols(ncols_) {}
-    __host__ __device__ size_t words() const { return (size_t)(ncols + 1) * (CS + 2 * SWW); }
+    __host__ __device__ size_t words() const { return (size_t)ncols * (CS + 2 * SWW); }
     __host__ __device__ size_t bytes() const { return words() * 4; }
     __device__ uint32_t *act(uint32_t *sm, int c) const { return sm + (size_t)c * CS; }
-    __device__ uint32_t *shi(uint32_t *sm, int c) const { return sm + (size_t)(ncols + 1) * CS + (size_t)c * SWW; }
-    __device__ uint32_t *slo(uint32_t *sm, int c) const {
-        return sm + (size_t)(ncols + 1) * (CS + SWW) + (size_t)c * SWW;
-    }
+    __device__ uint32_t *shi(uint32_t *sm, int c) const { return sm + (size_t)ncols * CS + (size_t)c * SWW; }
+    __device__ uint32_t *slo(uint32_t *sm, int c) const { return sm + (size_t)ncols * (CS + SWW) + (size_t)c * SWW; }
 };
 
-// Zero the all-zero column (once per CTA).  Block-wide; ends synchronised.
-__device__ __forceinline__ void zero_column(uint32_t *sm, const SmemAct &SA) {
-    for (int j = threadIdx.x; j < SA.CS; j += blockDim.x) SA.act(sm, SA.ncols)[j] = 0u;
-    for (int j = threadIdx.x; j < SA.SWW; j += blockDim.x) {
-        SA.shi(sm, SA.ncols)[j] = 0u;
-        SA.slo(sm, SA.ncols)[j] = 0u;
-    }
-    __syncthreads();
-}
-
-// Copy the prepared rows rows[0..n) (n <= ncols) into shared memory.  Block-wide; ends
-// synchronised.
-__device__ __forceinline__ void stage_act(uint32_t *sm, const SmemAct &SA, const PrepPtrs &P, const PrepLayout &L,
-                                          const int *rows, int n) {
+// Issue (and commit as one group) the asynchronous copies of the prepared rows rows[0..n)
+// (n <= ncols) into shared memory.  The caller waits for the group and synchronises.
+__device__ __forceinline__ void stage_act_issue(uint32_t *sm, const SmemAct &SA, const PrepPtrs &P,
+                                                const PrepLayout &L, const int *rows, int n) {
     const int n16 = L.nbp * 4;  // 16-byte groups per row
+    const FastDiv div16((uint32_t)n16);
     for (int j = threadIdx.x; j < n * n16; j += blockDim.x) {
-        const int c = j / n16, q = j - c * n16;
+        const int c = (int)div16.div((uint32_t)j), q = j - c * n16;
         const int b = q >> 2, grp = q & 3;
-        const uint4 v = __ldg(reinterpret_cast<const uint4 *>(P.act + (size_t)rows[c] * L.act_words_per_row()) + q);
-        uint2 *dst = reinterpret_cast<uint2 *>(SA.act(sm, c) + (b >> 1) * kPairWords + (b & 1) * 16 + 4 * grp);
-        dst[0] = make_uint2(v.x, v.y);
-        dst[1] = make_uint2(v.z, v.w);
+        const uint32_t *src = P.act + (size_t)rows[c] * L.act_words_per_row() + (size_t)q * 4;
+        uint32_t *dst = SA.act(sm, c) + (b >> 1) * kPairWords + (b & 1) * 16 + 4 * grp;
+        cp_async8(dst, src);
+        cp_async8(dst + 2, src + 2);
     }
     const int nw = L.nbp / 2;
+    const FastDiv divw((uint32_t)nw);
     for (int j = threadIdx.x; j < n * nw; j += blockDim.x) {
-        const int c = j / nw, i = j - c * nw;
-        SA.shi(sm, c)[i] = __ldg(P.shi + (size_t)rows[c] * L.sum_words_per_row() + i);
-        SA.slo(sm, c)[i] = __ldg(P.slo + (size_t)rows[c] * L.sum_words_per_row() + i);
+        const int c = (int)divw.div((uint32_t)j), i = j - c * nw;
+        cp_async4(SA.shi(sm, c) + i, P.shi + (size_t)rows[c] * L.sum_words_per_row() + i);
+        cp_async4(SA.slo(sm, c) + i, P.slo + (size_t)rows[c] * L.sum_words_per_row() + i);
     }
+    cp_async_commit();
+}
+
+// Copy the prepared rows rows[0..n) into shared memory (all copies in flight at once).
+// Block-wide; ends synchronised.
+__device__ __forceinline__ void stage_act(uint32_t *sm, const SmemAct &SA, const PrepPtrs &P, const PrepLayout &L,
+                                          const int *rows, int n) {
+    stage_act_issue(sm, SA, P, L, rows, n);
+    cp_async_wait<0>();
     __syncthreads();
 }
 
 // acc[0] += block 2t and the offsets' hi part, acc[1] += block 2t+1 and the lo part: two
 // independent MMA chains, issued alternately.  B fragments come from the staged operand,
-// column g (or the zero column when g has no row in the current slice of n columns).
+// column g (column 0 when g has no row in the current slice of n columns; see SmemAct).
 __device__ __forceinline__ void compute_tile_smem(const TileRegs &r, uint32_t *sm, const SmemAct &SA, int n,
                                                   int tile, int lane, float (&acc)[2][4], bool &range_bad) {
     const int g = lane >> 2, t = lane & 3;
-    const int cg = g < n ? g : SA.ncols;
+    const int cg = g < n ? g : 0;
     const uint32_t *base = SA.act(sm, cg) + (tile * 4 + t) * kPairWords;  // block pair (2t, 2t+1)
     uint32_t d2[2][2], nd[2][2];  // [block 2t | 2t+1][row g | g+8]
 #pragma unroll

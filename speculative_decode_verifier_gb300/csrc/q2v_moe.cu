@@ -195,10 +195,12 @@ struct UnitMap {
     }
 };
 
+constexpr int kRingStages = 4;  // weight tiles per warp in the shared-memory ring
+
 template <bool GATEUP, bool ALIGN8>
 __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, int KS, int ncols,
                                                             float *__restrict__ outp) {
-    extern __shared__ __align__(16) uint32_t sm_act[];
+    extern __shared__ __align__(16) uint32_t sm_dyn[];
     __shared__ int s_active[257];
     __shared__ int s_off[256];
     __shared__ int s_cnt[256];
@@ -220,7 +222,8 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
     const PrepLayout L(K);
     const SmemAct SA(L, ncols);
     const PrepPtrs &Pp0 = GATEUP ? w.prepX : w.prepH;
-    zero_column(sm_act, SA);
+    uint32_t *sm_act = sm_dyn;
+    uint32_t *ring = sm_dyn + SA.words() + (size_t)warp * kRingStages * kTileWords;
     UnitMap<GATEUP> um;
     um.Nrows = GATEUP ? a.F : a.H;
     const int groups = cdiv(um.Nrows, kRowsPerCta);
@@ -241,6 +244,8 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
     const int i0 = blockIdx.x * q, i1 = min(total, i0 + q);
     const int g = lane >> 2, t = lane & 3;
     const int mats = GATEUP ? 2 : 1;
+    // the ring path: whole 16-row groups, whole tiles, 16-byte aligned rows
+    const bool ring_path = (um.Nrows % kRowsPerCta) == 0 && L.nb == L.ntk * kTileBlocks && (L.nb % 4) == 0;
     bool range_bad = false;
 
     for (int seg0 = i0; seg0 < i1;) {
@@ -259,68 +264,87 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
                 s_exps[c] = r >= 0 ? Pp0.exps[r] : 0;
             }
             __syncthreads();
-            stage_act(sm_act, SA, Pp0, L, s_rows, mc);
-
-            // this warp's stream: units seg0 + warp, + nwarps, ...; each unit's tiles t0..t1-1.
-            // Two tile buffers with fixed names: while one is consumed the next is in flight.  A position carries what its load and its unit's epilogue need.
-            struct Pos {
-                int u, tile, t1, rv, n0, slot;  // slot = ks * mats + mat
-                const uint8_t *W0;
-            };
-            auto at_unit = [&](int uu) {
-                Pos p;
-                p.u = uu;
-                if (uu < seg1) {
-                    const UnitInfo ui = um(uu);
-                    p.tile = ui.t0;
-                    p.t1 = ui.t1;
-                    p.rv = ui.rows_valid;
-                    p.n0 = ui.n0;
-                    p.slot = ui.ks * mats + ui.mat;
-                    p.W0 = ui.W0;
-                }
-                return p;
-            };
-            auto next_pos = [&](Pos p) {
-                if (p.u >= seg1) return p;
-                if (++p.tile >= p.t1) return at_unit(p.u + nwarps);
-                return p;
-            };
-            auto issue = [&](TileRegs &buf, const Pos &p) {
-                if (p.u < seg1) load_tile<ALIGN8>(buf, p.W0, um.row_bytes, p.rv, L.nb, p.tile, lane);
-            };
-            float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            auto finish_unit = [&](const Pos &p) {
-                float *dst = outp + (size_t)p.slot * P * um.Nrows;
+            stage_act_issue(sm_act, SA, Pp0, L, s_rows, mc);  // the oldest async group
+            auto store_unit = [&](const UnitInfo &ui, float (&acc)[2][4]) {
+                float *dst = outp + (size_t)(ui.ks * mats + ui.mat) * P * um.Nrows;
 #pragma unroll
                 for (int qq = 0; qq < 4; ++qq) {
                     const int c = 2 * t + (qq & 1), rr = g + 8 * (qq >> 1);
-                    if (c < mc && rr < p.rv) {
+                    if (c < mc && rr < ui.rows_valid) {
                         const int pos = off + m0 + c;
-                        dst[(size_t)pos * um.Nrows + p.n0 + rr] = ldexpf(acc[0][qq] + acc[1][qq], s_exps[c]);
+                        dst[(size_t)pos * um.Nrows + ui.n0 + rr] = ldexpf(acc[0][qq] + acc[1][qq], s_exps[c]);
                     }
                     acc[0][qq] = 0.0f;
                     acc[1][qq] = 0.0f;
                 }
             };
-            Pos p0 = at_unit(seg0 + warp);
-            Pos p1 = next_pos(p0);
-            Pos last = p1;
-            TileRegs b0, b1;
-            issue(b0, p0);
-            issue(b1, p1);
-#define Q2V_CONSUME(BUF, POS)                                                      \
-    if (POS.u >= seg1) break;                                                      \
-    compute_tile_smem(BUF, sm_act, SA, mc, POS.tile, lane, acc, range_bad);        \
-    if (POS.tile + 1 >= POS.t1) finish_unit(POS);                                  \
-    POS = next_pos(last);                                                          \
-    last = POS;                                                                    \
-    issue(BUF, POS);
-            while (true) {
-                Q2V_CONSUME(b0, p0)
-                Q2V_CONSUME(b1, p1)
+            if (ring_path) {
+                // this warp's tiles, in order: units seg0 + warp, + nwarps, ...; tiles t0..t1-1.
+                // A producer cursor runs kRingStages-1 tiles ahead of the consumer.
+                int pu = seg0 + warp, ptile = 0, pt1 = 0;
+                const uint8_t *pW = nullptr;
+                if (pu < seg1) {
+                    const UnitInfo ui = um(pu);
+                    ptile = ui.t0;
+                    pt1 = ui.t1;
+                    pW = ui.W0;
+                }
+                auto produce = [&](int stage) {
+                    if (pu < seg1) {
+                        issue_tile_cpasync(ring + stage * kTileWords, pW, um.row_bytes, ptile, lane);
+                        if (++ptile >= pt1) {
+                            pu += nwarps;
+                            if (pu < seg1) {
+                                const UnitInfo ui = um(pu);
+                                ptile = ui.t0;
+                                pt1 = ui.t1;
+                                pW = ui.W0;
+                            }
+                        }
+                    }
+                    cp_async_commit();  // one group per slot, empty or not, keeps the count uniform
+                };
+#pragma unroll
+                for (int sidx = 0; sidx < kRingStages - 1; ++sidx) produce(sidx);
+                cp_async_wait<kRingStages - 1>();  // the activation group is done
+                __syncthreads();
+                int cu = seg0 + warp;
+                UnitInfo cui;
+                if (cu < seg1) cui = um(cu);
+                int ctile = cui.t0;
+                float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                for (int it = 0; cu < seg1; ++it) {
+                    produce((it + kRingStages - 1) % kRingStages);
+                    cp_async_wait<kRingStages - 1>();  // this tile's group has landed
+                    __syncwarp();
+                    TileRegs cur;
+                    read_tile_smem(cur, ring + (it % kRingStages) * kTileWords, lane);
+                    compute_tile_smem(cur, sm_act, SA, mc, ctile, lane, acc, range_bad);
+                    if (++ctile >= cui.t1) {
+                        store_unit(cui, acc);
+                        cu += nwarps;
+                        if (cu < seg1) {
+                            cui = um(cu);
+                            ctile = cui.t0;
+                        }
+                    }
+                    __syncwarp();  // every lane has read this stage before a later copy refills it
+                }
+                cp_async_wait<0>();
+            } else {
+                cp_async_wait<0>();
+                __syncthreads();
+                for (int u = seg0 + warp; u < seg1; u += nwarps) {
+                    const UnitInfo ui = um(u);
+                    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+                    for (int tile = ui.t0; tile < ui.t1; ++tile) {
+                        TileRegs b0;
+                        load_tile<ALIGN8>(b0, ui.W0, um.row_bytes, ui.rows_valid, L.nb, tile, lane);
+                        compute_tile_smem(b0, sm_act, SA, mc, tile, lane, acc, range_bad);
+                    }
+                    store_unit(ui, acc);
+                }
             }
-#undef Q2V_CONSUME
         }
         seg0 = seg1;
     }
@@ -382,7 +406,7 @@ cudaError_t launch_stream_variant(int idx, const MoeArgs &a, const MoeWs &w, int
 template <bool GU>
 cudaError_t launch_stream(const MoeArgs &a, const MoeWs &w, int KS, float *out, int num_sms, const PrepLayout &L,
                           cudaStream_t s) {
-    const size_t smem = SmemAct(L, min(8, a.M)).bytes();
+    const size_t smem = SmemAct(L, min(8, a.M)).bytes() + (size_t)8 * kRingStages * kTileWords * 4;
     if (L.nb % 2 == 0) return launch_stream_variant<GU, true>(GU ? 0 : 2, a, w, KS, out, num_sms, smem, s);
     return launch_stream_variant<GU, false>(GU ? 1 : 3, a, w, KS, out, num_sms, smem, s);
 }

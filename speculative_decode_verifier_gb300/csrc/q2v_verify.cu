@@ -252,7 +252,7 @@ __global__ void __launch_bounds__(512) pqv_stats_kernel(PqArgs a, PqSplit sp) {
         if (VEC) {
             const float4 *x4 = reinterpret_cast<const float4 *>(x + c0);
             const int n4 = (c1 - c0) >> 2;
-            constexpr int U = 4;
+            constexpr int U = 12;  // all of a lane's loads of a chunk row in one round at cfg3 sizes
             for (int base = 0; base < n4; base += 32 * U) {
                 float4 v[U];
 #pragma unroll
@@ -294,53 +294,87 @@ __global__ void __launch_bounds__(512) pqv_stats_kernel(PqArgs a, PqSplit sp) {
     }
 }
 
-// Sum over the block (tree in fp32); every thread gets the total.
-__device__ __forceinline__ float block_sum(float v, float *scratch) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-    v = warp_sum(v);
-    __syncthreads();
-    if (lane == 0) scratch[warp] = v;
-    __syncthreads();
-    float t = 0.0f;
-    for (int w = 0; w < nw; ++w) t += scratch[w];
-    return t;
-}
-
-// Kernel 2: combine, accept scan, chunk masses, last-arriver inverse-CDF search.
+// Kernel 2: combine, accept scan, per-warp chunk masses, last-arriver inverse-CDF search.
+//
+// Each chunk of L tokens is cut into 8 contiguous warp segments; warp w of the CTA owns
+// segment w and writes its draw mass (and its p_j mass, for the zero-residual fallback) to
+// the workspace.  The last CTA of the session to finish picks, with one warp, the segment
+// holding the crossing (a segmented scan over the session's C*8 masses) and then the token
+// inside it (a scan of that one segment): no block-wide barrier in the search.
 template <bool VEC>
 __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
     __shared__ float rowM[kMaxRows];
     __shared__ float rowL2Z[kMaxRows];
-    __shared__ float scratch[32];
-    __shared__ int s_j, s_last, s_y, s_lastpos;
+    __shared__ float s_wm[kMaxChunks * kSegsPerChunk];  // the last CTA's copy of the segment masses
+    __shared__ int s_j, s_last;
     pdl_wait();
     pdl_trigger();
     const int c = blockIdx.x, s = blockIdx.y;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nwarps = blockDim.x >> 5;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int R = 2 * a.k + 1;
     const float beta = a.beta;
     const int c0 = c * sp.L, c1 = min(a.V, c0 + sp.L);
+    const int Lw = sp.L / kSegsPerChunk;  // tokens per warp segment (a multiple of 16)
 
-    // 1. row statistics from the chunk partials
-    for (int r = warp; r < R; r += nwarps) {
-        const float2 *st = reinterpret_cast<const float2 *>(sp.stats) + ((size_t)s * R + r) * sp.C;
+    // 1. row statistics from the chunk partials: 16 lanes per row, partials held in
+    //    registers so the combine takes one round of loads
+    for (int r0 = 0; r0 < R; r0 += 16) {
+        const int r = r0 + (tid >> 4), sub = tid & 15;
+        float2 v[8];
         float m = -INFINITY;
-        for (int cc = lane; cc < sp.C; cc += 32) m = fmaxf(m, st[cc].x);
-        m = warp_max(m);
-        float z = 0.0f;
-        for (int cc = lane; cc < sp.C; cc += 32) {
-            const float2 v = st[cc];
-            if (v.x > -INFINITY) z += v.y * ex2((v.x - m) * beta);
+        const float2 *st = reinterpret_cast<const float2 *>(sp.stats) + ((size_t)s * R + min(r, R - 1)) * sp.C;
+        if (sp.C <= 16 * 8) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int cc = sub + 16 * u;
+                v[u] = (r < R && cc < sp.C) ? st[cc] : make_float2(-INFINITY, 0.0f);
+                m = fmaxf(m, v[u].x);
+            }
+        } else {
+            for (int cc = sub; r < R && cc < sp.C; cc += 16) m = fmaxf(m, st[cc].x);
         }
-        z = warp_sum(z);
-        if (lane == 0) {
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float z = 0.0f;
+        if (sp.C <= 16 * 8) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (v[u].x > -INFINITY) z += v[u].y * ex2((v[u].x - m) * beta);
+        } else {
+            for (int cc = sub; r < R && cc < sp.C; cc += 16) {
+                const float2 w = st[cc];
+                if (w.x > -INFINITY) z += w.y * ex2((w.x - m) * beta);
+            }
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        if (sub == 0 && r < R) {
             rowM[r] = m;
             rowL2Z[r] = log2f(z);
         }
     }
     __syncthreads();
-    // 2. accept scan
-    if (tid == 0) s_j = accept_scan(a, s, rowM, rowL2Z);
+    // 2. accept scan: lane i evaluates draft i (all loads in one round), a ballot finds
+    //    the first rejection
+    if (warp == 0) {
+        bool bad = false, rej = false;
+        if (lane < a.k) {
+            const int x = a.drafts[(size_t)s * a.k + lane];
+            if (x < 0 || x >= a.V) {
+                bad = true;
+            } else {
+                const float tx = row_ptr(a, s, lane)[x], dx = row_ptr(a, s, a.k + 1 + lane)[x];
+                const float u = a.u_acc[(size_t)s * a.k + lane];
+                if (dx != -INFINITY) {  // q(x) == 0 accepts
+                    const float lp = (tx - rowM[lane]) * beta - rowL2Z[lane];
+                    const float lq = (dx - rowM[a.k + 1 + lane]) * beta - rowL2Z[a.k + 1 + lane];
+                    rej = !(u < ex2(lp - lq));
+                }
+            }
+        }
+        const unsigned badm = __ballot_sync(0xffffffffu, bad), rejm = __ballot_sync(0xffffffffu, rej);
+        if (lane == 0) s_j = badm ? -1 : (rejm ? __ffs(rejm) - 1 : a.k);
+    }
     __syncthreads();
     const int j = s_j;
     // optional probabilities of every row of this chunk
@@ -360,152 +394,139 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
         return;
     }
     DrawRows D = draw_rows(a, s, j, rowM, rowL2Z);
-    // 3. this chunk's draw mass (and p_j mass for the zero-residual fallback)
-    float wsum = 0.0f, psum = 0.0f;
-    if (VEC) {
-        const float4 *t4 = reinterpret_cast<const float4 *>(D.t + c0);
-        const float4 *d4 = reinterpret_cast<const float4 *>(D.d + c0);
-        const int n4 = (c1 - c0) >> 2;
-        for (int i = tid; i < n4; i += blockDim.x) {
-            const float4 xt = t4[i];
-            const float4 xd = (D.mode == 0) ? d4[i] : xt;
-            wsum += draw_weight(D, beta, xt.x, xd.x) + draw_weight(D, beta, xt.y, xd.y) +
-                    draw_weight(D, beta, xt.z, xd.z) + draw_weight(D, beta, xt.w, xd.w);
-            if (D.mode == 0)
-                psum += ex2((xt.x - D.mt) * beta - D.lt) + ex2((xt.y - D.mt) * beta - D.lt) +
-                        ex2((xt.z - D.mt) * beta - D.lt) + ex2((xt.w - D.mt) * beta - D.lt);
+    // 3. this warp's segment masses
+    {
+        const int y0 = c0 + warp * Lw, y1 = min(c1, y0 + Lw);
+        float wsum = 0.0f, psum = 0.0f;
+        if (VEC) {
+            const float4 *t4 = reinterpret_cast<const float4 *>(D.t);
+            const float4 *d4 = reinterpret_cast<const float4 *>(D.d);
+            for (int i = (y0 >> 2) + lane; i < (y1 >> 2); i += 32) {
+                const float4 xt = t4[i];
+                const float4 xd = (D.mode == 0) ? d4[i] : xt;
+                wsum += draw_weight(D, beta, xt.x, xd.x) + draw_weight(D, beta, xt.y, xd.y) +
+                        draw_weight(D, beta, xt.z, xd.z) + draw_weight(D, beta, xt.w, xd.w);
+                if (D.mode == 0)
+                    psum += ex2((xt.x - D.mt) * beta - D.lt) + ex2((xt.y - D.mt) * beta - D.lt) +
+                            ex2((xt.z - D.mt) * beta - D.lt) + ex2((xt.w - D.mt) * beta - D.lt);
+            }
+        } else {
+            for (int y = y0 + lane; y < y1; y += 32) {
+                const float xt = D.t[y];
+                const float xd = (D.mode == 0) ? D.d[y] : xt;
+                wsum += draw_weight(D, beta, xt, xd);
+                if (D.mode == 0) psum += ex2((xt - D.mt) * beta - D.lt);
+            }
         }
-    } else {
-        for (int y = c0 + tid; y < c1; y += blockDim.x) {
-            const float xt = D.t[y];
-            const float xd = (D.mode == 0) ? D.d[y] : xt;
-            wsum += draw_weight(D, beta, xt, xd);
-            if (D.mode == 0) psum += ex2((xt - D.mt) * beta - D.lt);
+        wsum = warp_sum(wsum);
+        psum = warp_sum(psum);
+        if (lane == 0) {
+            const size_t e = ((size_t)s * sp.C + c) * kSegsPerChunk + warp;
+            sp.mass[e] = wsum;
+            sp.pmass[e] = psum;
         }
     }
-    const float wtot = block_sum(wsum, scratch);
-    const float ptot = block_sum(psum, scratch);
+    __syncthreads();
     if (tid == 0) {
-        sp.mass[(size_t)s * sp.C + c] = wtot;
-        sp.pmass[(size_t)s * sp.C + c] = ptot;
         __threadfence();
         const unsigned ticket = atomicAdd(sp.tickets + s, 1u);
         s_last = (ticket == (unsigned)(sp.C - 1));
     }
     __syncthreads();
-    if (!s_last) return;
+    if (!s_last || warp != 0) return;
     __threadfence();
 
-    // 4. last CTA of the session: pick the chunk (all chunk masses loaded in parallel, then
-    //    one warp scans them as 32 contiguous segments), then the token inside it
-    __shared__ float s_mass[kMaxChunks], s_pmass[kMaxChunks];
-    __shared__ float s_prefix_hi, s_prefix_lo, s_target;
-    __shared__ int s_chunk, s_mode;
-    for (int cc = tid; cc < sp.C; cc += blockDim.x) {
-        s_mass[cc] = __ldcg(sp.mass + (size_t)s * sp.C + cc);
-        s_pmass[cc] = __ldcg(sp.pmass + (size_t)s * sp.C + cc);
+    // 4. last CTA, one warp: pick the segment holding the crossing, then the token in it.
+    //    The session's segment masses are first copied to shared memory in one round.
+    const int nseg = sp.C * kSegsPerChunk;
+    float *sm = s_wm;
+    const float *wsrc = sp.mass + (size_t)s * nseg;
+    for (int e = lane; e < nseg; e += 32) sm[e] = __ldcg(wsrc + e);
+    __syncwarp();
+    const int q = cdiv(nseg, 32);
+    const int e0 = min(nseg, lane * q), e1 = min(nseg, e0 + q);
+    int mode = D.mode;
+    float seg = 0.0f;
+    for (int e = e0; e < e1; ++e) seg += sm[e];
+    float tot = warp_sum(seg);
+    if (mode == 0 && !(tot > 0.0f)) {  // zero residual mass: draw from p_j
+        mode = 1;
+        wsrc = sp.pmass + (size_t)s * nseg;
+        __syncwarp();
+        for (int e = lane; e < nseg; e += 32) sm[e] = __ldcg(wsrc + e);
+        __syncwarp();
+        seg = 0.0f;
+        for (int e = e0; e < e1; ++e) seg += sm[e];
+        tot = warp_sum(seg);
     }
-    __syncthreads();
-    if (warp == 0) {
-        const int q = cdiv(sp.C, 32);
-        const int cs0 = min(sp.C, lane * q), cs1 = min(sp.C, cs0 + q);
-        int mode = D.mode;
-        const float *mm = s_mass;
-        float seg = 0.0f;
-        for (int cc = cs0; cc < cs1; ++cc) seg += mm[cc];
-        float tot = warp_sum(seg);
-        if (mode == 0 && !(tot > 0.0f)) {  // zero residual mass: draw from p_j
-            mode = 1;
-            mm = s_pmass;
-            seg = 0.0f;
-            for (int cc = cs0; cc < cs1; ++cc) seg += mm[cc];
-            tot = warp_sum(seg);
-        }
-        const float target = a.u_fin[s] * tot;
-        const float incl = warp_incl_scan(seg, lane);
-        float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-        if (lane == 0) excl = 0.0f;
-        const unsigned hit = __ballot_sync(0xffffffffu, seg > 0.0f && excl + seg > target);
-        const unsigned pos = __ballot_sync(0xffffffffu, seg > 0.0f);
-        // the lane whose segment holds the crossing; if rounding put the target past the
-        // end, the last lane with mass (its last chunk with mass is taken)
-        const int owner = hit ? (__ffs(hit) - 1) : (pos ? 31 - __clz(pos) : -1);
-        int chunk = -1;
-        CSum prefix;
-        if (lane == owner) {
-            CSum pre;
-            pre.add(excl);
-            int last_nz = -1;
-            CSum last_pre;
-            for (int cc = cs0; cc < cs1; ++cc) {
-                const float mc = mm[cc];
-                if (mc > 0.0f) {
-                    last_nz = cc;
-                    last_pre = pre;
-                    if (hit && pre.exceeds(mc, target)) {
-                        chunk = cc;
-                        prefix = pre;
-                        break;
-                    }
+    D.mode = mode;
+    const float target = a.u_fin[s] * tot;
+    const float incl = warp_incl_scan(seg, lane);
+    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = 0.0f;
+    const unsigned hit = __ballot_sync(0xffffffffu, seg > 0.0f && excl + seg > target);
+    const unsigned pos = __ballot_sync(0xffffffffu, seg > 0.0f);
+    // the lane whose entries hold the crossing; if rounding put the target past the end,
+    // the last lane with mass (its last segment with mass is taken)
+    const int owner = hit ? (__ffs(hit) - 1) : (pos ? 31 - __clz(pos) : -1);
+    int ent = -1;
+    CSum prefix;
+    if (lane == owner) {
+        CSum pre, last_pre;
+        pre.add(excl);
+        int found = -1, last_nz = -1;
+        CSum found_pre;
+        for (int e = e0; e < e1; ++e) {
+            const float me = sm[e];
+            if (me > 0.0f) {
+                last_nz = e;
+                last_pre = pre;
+                if (hit && pre.exceeds(me, target)) {
+                    found = e;
+                    found_pre = pre;
+                    break;
                 }
-                pre.add(mc);
             }
-            if (chunk < 0) {
-                chunk = last_nz;
-                prefix = last_pre;
-            }
+            pre.add(me);
         }
-        if (owner >= 0) {
-            chunk = __shfl_sync(0xffffffffu, chunk, owner);
-            prefix.hi = __shfl_sync(0xffffffffu, prefix.hi, owner);
-            prefix.lo = __shfl_sync(0xffffffffu, prefix.lo, owner);
-        }
-        if (lane == 0) {
-            s_chunk = chunk;
-            s_prefix_hi = prefix.hi;
-            s_prefix_lo = prefix.lo;
-            s_target = target;
-            s_mode = mode;
-            s_y = 0x7fffffff;
-            s_lastpos = -1;
-        }
+        ent = found >= 0 ? found : last_nz;
+        prefix = found >= 0 ? found_pre : last_pre;
     }
-    __syncthreads();
-    D.mode = s_mode;
-    const int cs = s_chunk;
-    if (cs >= 0) {
-        const float tgt = s_target;
-        const int y0 = cs * sp.L, y1 = min(a.V, y0 + sp.L);
-        CSum carry;
-        carry.hi = s_prefix_hi;
-        carry.lo = s_prefix_lo;
-        for (int base = y0; base < y1; base += blockDim.x) {
-            const int y = base + tid;
-            const float w = y < y1 ? draw_weight(D, beta, D.t[y], D.d[y]) : 0.0f;
-            // block inclusive scan of w (thread order is token order)
-            const float incl = warp_incl_scan(w, lane);
-            if (lane == 31) scratch[warp] = incl;
-            __syncthreads();
-            float woff = 0.0f, tile_total = 0.0f;
-            for (int ww = 0; ww < nwarps; ++ww) {
-                if (ww < warp) woff += scratch[ww];
-                tile_total += scratch[ww];
+    int y_sel = -1;
+    if (owner >= 0) {
+        ent = __shfl_sync(0xffffffffu, ent, owner);
+        prefix.hi = __shfl_sync(0xffffffffu, prefix.hi, owner);
+        prefix.lo = __shfl_sync(0xffffffffu, prefix.lo, owner);
+        // the segment's tokens, 32 at a time in order; the loads of up to 8 rounds are
+        // issued together
+        const int sc = ent / kSegsPerChunk, sw = ent - sc * kSegsPerChunk;
+        const int y0 = sc * sp.L + sw * Lw, y1 = min(min(a.V, sc * sp.L + sp.L), y0 + Lw);
+        CSum carry = prefix;
+        int last_pos = -1;
+        for (int base0 = y0; base0 < y1 && y_sel < 0; base0 += 32 * 8) {
+            float wv[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int y = base0 + 32 * u + lane;
+                wv[u] = y < y1 ? draw_weight(D, beta, D.t[y], D.d[y]) : 0.0f;
             }
-            if (w > 0.0f) {
-                atomicMax(&s_lastpos, y);
-                if (carry.exceeds(woff + incl, tgt)) atomicMin(&s_y, y);
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int base = base0 + 32 * u;
+                if (base < y1 && y_sel < 0) {
+                    const float w = wv[u];
+                    const float inc = warp_incl_scan(w, lane);
+                    const unsigned h = __ballot_sync(0xffffffffu, w > 0.0f && carry.exceeds(inc, target));
+                    const unsigned pz = __ballot_sync(0xffffffffu, w > 0.0f);
+                    if (pz) last_pos = base + 31 - __clz(pz);
+                    if (h) y_sel = base + __ffs(h) - 1;
+                    carry.add(__shfl_sync(0xffffffffu, inc, 31));
+                }
             }
-            __syncthreads();
-            if (s_y != 0x7fffffff) break;
-            carry.add(tile_total);
         }
+        if (y_sel < 0) y_sel = last_pos;
     }
-    __syncthreads();
-    if (tid == 0) {
-        int y = s_y;
-        if (y == 0x7fffffff) y = s_lastpos;
-        write_tokens(a, s, j, y);
-    }
+    if (lane == 0) write_tokens(a, s, j, y_sel);
 }
 
 cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier, int num_sms, cudaStream_t st) {
