@@ -41,6 +41,37 @@ LAUNCHES_PER_STEP = 2 + 6 + 2   # prep+gemm; route, prep X, gate/up, prep h, dow
 EXPERT_BYTES = 3 * 2048 * (4096 // 32) * 12   # gate + up + down of one expert
 
 
+def _kernel_source_digest() -> str:
+    """sha256 (first 16 hex digits) of the source the gate+up stream kernel is built from: the
+    shared device headers and the kernel's own definition.  A traffic figure recorded under
+    profiles/ is only reported while this digest still matches the one recorded with it."""
+    import hashlib
+    import re
+    csrc = os.path.join(ROOT, "speculative_decode_verifier_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in ("q2v_common.cuh", "q2v_mma_core.cuh"):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(f.read())
+    with open(os.path.join(csrc, "q2v_moe.cu")) as f:
+        text = f.read()
+    m = re.search(r"^struct UnitInfo.*?^__global__[^\n]*moe_stream_kernel.*?^}\n", text, re.S | re.M)
+    h.update((m.group(0) if m else text).encode())
+    return h.hexdigest()[:16]
+
+
+def _traffic_record():
+    """The `traffic-record:` line of profiles/verifier_step_m5_launch_list.md, as a dict."""
+    path = os.path.join(ROOT, "profiles", "verifier_step_m5_launch_list.md")
+    try:
+        with open(path) as f:
+            for line in f:
+                if line.startswith("traffic-record:"):
+                    return dict(kv.split("=", 1) for kv in line.split(":", 1)[1].split())
+    except OSError:
+        pass
+    return None
+
+
 def _peaks():
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -229,6 +260,37 @@ def run_device(args, rank: int, world: int):
         t = torch.tensor([step_us], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         step_us = float(t.item())
+    # per-kernel device time inside the step: each timed step is its own graph whose launch of
+    # the kernel is bracketed by its own event pair (q2_set_probe); these steps replay back to
+    # back after warm-up, like the timed region above
+    def probe_pass(kernel):
+        n = args.warmup + args.steps
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+        for a, b in evs:  # create the event handles
+            a.record()
+            b.record()
+        torch.cuda.synchronize()
+        graphs = []
+        try:
+            for i in range(n):
+                q2v.q2_set_probe(kernel, *evs[i])
+                gr = torch.cuda.CUDAGraph()
+                with torch.cuda.graph(gr):
+                    step(sets[i % N_SETS])
+                graphs.append(gr)
+        finally:
+            q2v.q2_set_probe(q2v.PROBE_NONE)
+        torch.cuda.synchronize()
+        for gr in graphs:
+            gr.replay()
+        torch.cuda.synchronize()
+        return [a.elapsed_time(b) * 1000.0 for a, b in evs[args.warmup:]], [i % N_SETS for i in range(args.warmup, n)]
+
+    kern_us = {}
+    for name, kid in (("moe_gate_up", q2v.PROBE_MOE_GATE_UP), ("moe_down", q2v.PROBE_MOE_DOWN),
+                      ("gemm", q2v.PROBE_GEMM), ("pq_stats", q2v.PROBE_PQ_STATS), ("pq_verify", q2v.PROBE_PQ_VERIFY)):
+        kern_us[name] = probe_pass(kid)
+
     gemm_us, _ = timed(capture(part_gemm), args.steps, args.warmup)
     moe_us, _ = timed(capture(part_moe), args.steps, args.warmup)
     pq_us, _ = timed(capture(part_pq), args.steps, args.warmup)
@@ -286,13 +348,31 @@ def run_device(args, rank: int, world: int):
                       "rows_per_s": sh["S"] * (sh["k"] + 1) / (pq_us * 1e-6),
                       "draft_rows_per_s": sh["S"] * sh["k"] / (pq_us * 1e-6)},
     }
+    # algorithmic bytes per launch of each probed kernel, by input set
+    P = sh["M"] * sh["topk"]
+    kbytes = {
+        "moe_gate_up": lambda si: active[si] * 2 * sh["F"] * (sh["H"] // 32) * 12 + sh["M"] * sh["H"] * 2
+        + P * 2 * sh["F"] * 4,
+        "moe_down": lambda si: active[si] * sh["H"] * (sh["F"] // 32) * 12 + P * sh["F"] * 4 + sh["M"] * sh["H"] * 4,
+        "gemm": lambda si: gemm_bytes,
+        "pq_stats": lambda si: sh["S"] * (2 * sh["k"] + 1) * sh["V"] * 4,
+    }
+    kernels = {}
+    for name, (us, set_ids) in kern_us.items():
+        d = {"us": statistics.mean(us)}
+        if name in kbytes:
+            tot_b = sum(kbytes[name](si) for si in set_ids)
+            d["bytes"] = tot_b / len(set_ids)
+            d["GB/s"] = tot_b / (sum(us) * 1e-6) / 1e9
+            d["frac"] = d["GB/s"] / peak
+        kernels[name] = d
+    dom = kernels["moe_gate_up"]
+    # DRAM traffic of one launch from the recorded ncu capture, scaled to the mean launch by
+    # active experts; null when the kernel's source has changed since the capture
     traffic = None
-    tfile = os.path.join(ROOT, "profiles", "traffic.json")
-    if os.path.exists(tfile):
-        try:
-            traffic = json.load(open(tfile)).get("q2_moe_grouped")
-        except Exception:
-            traffic = None
+    rec = _traffic_record()
+    if rec and rec.get("sources") == _kernel_source_digest():
+        traffic = float(rec["bytes"]) * statistics.mean(active[si] for si in kern_us["moe_gate_up"][1]) / float(rec["units"])
     line = {
         "metric": METRIC, "value": step_us, "unit": "µs", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_us / 1000.0, "higher_is_better": False,
@@ -305,9 +385,11 @@ def run_device(args, rank: int, world: int):
         "q2_gemm_m5_frac_of_8TBs": gemm_gbs / 8000.0,
         "pq_verify_rows_per_s": parts["pq_verify"]["rows_per_s"],
         "parts": parts,
-        "roofline": {"bound": "hbm", "kernel": "q2_moe_grouped (the MoE FFN call; grouped dequant GEMMs dominate)",
-                     "achieved": moe_gbs, "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": moe_gbs / peak, "traffic": traffic},
+        "kernels": kernels,
+        "roofline": {"bound": "hbm", "kernel": "moe_stream_kernel<gate+up> (MoE gate+up grouped dequant GEMM)",
+                     "achieved": dom["GB/s"], "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+                     "frac": dom["frac"], "traffic": traffic,
+                     "algorithmic_bytes_per_launch": dom["bytes"], "us_per_launch": dom["us"]},
         "e2e": {"value": e2e_us, "unit": "µs", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "clocks": clocks,

@@ -189,6 +189,30 @@ q2_status pq_verify_noalloc(const float *target_logits, const float *draft_logit
                             int S, int k, int V, float temperature, int32_t *n_accepted,
                             int32_t *out_tokens, float *probs_out, q2_stream_t stream);
 
+/* ------------------------------------------------------------------ measurement hook */
+
+/* Kernels that q2_set_probe can bracket. */
+typedef enum {
+    Q2_PROBE_NONE = 0,
+    Q2_PROBE_MOE_GATE_UP = 1, /* q2_moe_grouped: the gate+up grouped dequant GEMM          */
+    Q2_PROBE_MOE_DOWN = 2,    /* q2_moe_grouped: the down grouped dequant GEMM             */
+    Q2_PROBE_GEMM = 3,        /* q2_tiny_gemm: the dequant GEMM kernel (not the prep)      */
+    Q2_PROBE_PQ_STATS = 4,    /* pq_verify: the per-row softmax statistics kernel          */
+    Q2_PROBE_PQ_VERIFY = 5    /* pq_verify: the accept-scan and draw kernel                */
+} q2_probe_kernel;
+
+/* Timing hook for measurement harnesses; the verifier method has no counterpart.  From this
+ * call on, every call that launches the kernel named by `kernel` records `ev_begin` on the
+ * call's stream just before that launch and `ev_end` just after it, so that the caller can
+ * read the kernel's own duration with cudaEventElapsedTime.  Under stream capture the two
+ * records become external event nodes of the graph (cudaEventRecordExternal).
+ *   ev_begin, ev_end: cudaEvent_t handles (passed as void *) created by the caller with
+ *                     timing enabled; the library keeps them until the next q2_set_probe.
+ *   kernel = Q2_PROBE_NONE turns the hook off (the events may then be NULL).
+ * Errors: Q2_ERR_INVALID_ARG for an unknown kernel or a NULL event.  Process-wide state,
+ * not thread-safe; a recording failure makes the bracketed call return Q2_ERR_CUDA. */
+q2_status q2_set_probe(int kernel, void *ev_begin, void *ev_end);
+
 /* ------------------------------------------------------------------ status */
 
 /* Synchronise `stream`, read the device status word of workspace `ws`, clear it, and

@@ -112,9 +112,35 @@ MoeCarve moe_carve(void *ws, int M, int E, int topk, int H, int F) {
 
 }  // namespace
 
+// ------------------------------------------------------------------ measurement hook
+
+namespace {
+int g_probe_kernel = 0;
+cudaEvent_t g_probe_ev[2] = {nullptr, nullptr};
+}  // namespace
+
+cudaError_t q2v::probe_mark(int kernel, int end, cudaStream_t s) {
+    if (g_probe_kernel == 0 || kernel != g_probe_kernel) return cudaSuccess;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    const cudaError_t e = cudaStreamIsCapturing(s, &cs);
+    if (e != cudaSuccess) return e;
+    if (cs == cudaStreamCaptureStatusActive)
+        return cudaEventRecordWithFlags(g_probe_ev[end], s, cudaEventRecordExternal);
+    return cudaEventRecord(g_probe_ev[end], s);
+}
+
 extern "C" {
 
 int q2_version(void) { return Q2V_VERSION; }
+
+q2_status q2_set_probe(int kernel, void *ev_begin, void *ev_end) {
+    if (kernel < Q2_PROBE_NONE || kernel > Q2_PROBE_PQ_VERIFY) return Q2_ERR_INVALID_ARG;
+    if (kernel != Q2_PROBE_NONE && (!ev_begin || !ev_end)) return Q2_ERR_INVALID_ARG;
+    g_probe_kernel = kernel;
+    g_probe_ev[0] = static_cast<cudaEvent_t>(ev_begin);
+    g_probe_ev[1] = static_cast<cudaEvent_t>(ev_end);
+    return Q2_OK;
+}
 
 const char *q2_status_string(q2_status s) {
     switch (s) {
@@ -166,7 +192,8 @@ q2_status q2_tiny_gemm(const void *W, int N, int K, const uint16_t *A, int M, in
     const PrepPtrs P = PrepPtrs::carve(c.take(L.bytes(M)), L, M);
     const cudaError_t e = launch_prep_bf16(A, lda, nullptr, M, K, P, L, s);
     if (e != cudaSuccess) return Q2_ERR_CUDA;
-    return cuda_status(launch_gemm_small(W, N, K, P, L, M, Y, ldy, status_word(ws), s));
+    return cuda_status(
+        probed(kProbeGemm, s, [&] { return launch_gemm_small(W, N, K, P, L, M, Y, ldy, status_word(ws), s); }));
 }
 
 // ---------------------------------------------------------------- routed MoE

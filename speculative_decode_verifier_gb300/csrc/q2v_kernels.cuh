@@ -78,4 +78,19 @@ struct MoeWs {
 
 cudaError_t launch_moe(const MoeArgs &a, const MoeWs &w, int num_sms, cudaStream_t s);
 
+// Measurement hook (q2_set_probe): records the caller's begin (end = 0) or end (end = 1)
+// event on s when `kernel` is the bracketed one; a no-op otherwise.
+enum ProbeKernel : int { kProbeMoeGateUp = 1, kProbeMoeDown = 2, kProbeGemm = 3, kProbePqStats = 4, kProbePqVerify = 5 };
+cudaError_t probe_mark(int kernel, int end, cudaStream_t s);
+
+// launch(), bracketed by the probe events of `kernel`.
+template <typename F>
+cudaError_t probed(int kernel, cudaStream_t s, F &&launch) {
+    cudaError_t e = probe_mark(kernel, 0, s);
+    if (e != cudaSuccess) return e;
+    e = launch();
+    if (e != cudaSuccess) return e;
+    return probe_mark(kernel, 1, s);
+}
+
 }  // namespace q2v

@@ -430,11 +430,11 @@ cudaError_t launch_moe(const MoeArgs &a, const MoeWs &w, int num_sms, cudaStream
     const int resident_warps = num_sms * 24;
     const int ks_gu = choose_ks(expect_active * 2 * cdiv(a.F, kRowsPerCta), LX.ntk, resident_warps);
     const int ks_d = choose_ks(expect_active * cdiv(a.H, kRowsPerCta), LH.ntk, resident_warps);
-    err = launch_stream<true>(a, w, ks_gu, w.h, num_sms, LX, s);
+    err = probed(kProbeMoeGateUp, s, [&] { return launch_stream<true>(a, w, ks_gu, w.h, num_sms, LX, s); });
     if (err != cudaSuccess) return err;
     err = launch_pdl(moe_prep_h_kernel, dim3(P), dim3(256), s, (const float *)w.h, P, a.F, ks_gu, w.prepH, LH);
     if (err != cudaSuccess) return err;
-    err = launch_stream<false>(a, w, ks_d, w.out, num_sms, LH, s);
+    err = probed(kProbeMoeDown, s, [&] { return launch_stream<false>(a, w, ks_d, w.out, num_sms, LH, s); });
     if (err != cudaSuccess) return err;
     return launch_pdl(moe_combine_kernel, dim3(max(1, min(cdiv(a.M * a.H, 256), 4 * num_sms))), dim3(256), s, a,
                       w, ks_d);

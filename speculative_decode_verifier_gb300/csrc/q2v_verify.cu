@@ -532,21 +532,23 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
 cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier, int num_sms, cudaStream_t st) {
     if (warp_tier) {
         const int blocks = max(1, min(cdiv(a.S, kWarpTierWarps), num_sms * 8));
-        return launch_pdl(pqv_warp_kernel, dim3(blocks), dim3(kWarpTierWarps * 32), st, a);
+        return probed(kProbePqVerify, st, [&] {
+            return launch_pdl(pqv_warp_kernel, dim3(blocks), dim3(kWarpTierWarps * 32), st, a);
+        });
     }
     const bool vec = (a.V % 4) == 0 && (sp.L % 4) == 0;
     const int R = 2 * a.k + 1;
     const dim3 grid(sp.C, a.S);
     const int warps1 = min(R, 16);
-    cudaError_t e;
-    if (vec) {
-        e = launch_pdl(pqv_stats_kernel<true>, grid, dim3(warps1 * 32), st, a, sp);
-        if (e == cudaSuccess) e = launch_pdl(pqv_verify_kernel<true>, grid, dim3(256), st, a, sp);
-    } else {
-        e = launch_pdl(pqv_stats_kernel<false>, grid, dim3(warps1 * 32), st, a, sp);
-        if (e == cudaSuccess) e = launch_pdl(pqv_verify_kernel<false>, grid, dim3(256), st, a, sp);
-    }
-    return e;
+    cudaError_t e = probed(kProbePqStats, st, [&] {
+        return vec ? launch_pdl(pqv_stats_kernel<true>, grid, dim3(warps1 * 32), st, a, sp)
+                   : launch_pdl(pqv_stats_kernel<false>, grid, dim3(warps1 * 32), st, a, sp);
+    });
+    if (e != cudaSuccess) return e;
+    return probed(kProbePqVerify, st, [&] {
+        return vec ? launch_pdl(pqv_verify_kernel<true>, grid, dim3(256), st, a, sp)
+                   : launch_pdl(pqv_verify_kernel<false>, grid, dim3(256), st, a, sp);
+    });
 }
 
 }  // namespace q2v

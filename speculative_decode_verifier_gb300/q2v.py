@@ -23,7 +23,10 @@ STATUS_NAMES = {0: "Q2_OK", 1: "Q2_ERR_INVALID_ARG", 2: "Q2_ERR_ALIGNMENT", 3: "
 MOE_RENORMALIZE = 1
 EXPORTS = ("q2_tiny_gemm_workspace", "q2_tiny_gemm", "q2_moe_grouped_workspace", "q2_moe_grouped",
            "pq_verify_workspace", "pq_verify", "pq_verify_noalloc", "q2_get_device_status", "q2_status_string",
-           "q2_version")
+           "q2_version", "q2_set_probe")
+
+# kernels that q2_set_probe can bracket (q2_probe_kernel)
+PROBE_NONE, PROBE_MOE_GATE_UP, PROBE_MOE_DOWN, PROBE_GEMM, PROBE_PQ_STATS, PROBE_PQ_VERIFY = range(6)
 
 
 class Q2Error(RuntimeError):
@@ -65,6 +68,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q2_status_string.argtypes = [I]
     lib.q2_status_string.restype = ctypes.c_char_p
     lib.q2_version.restype = I
+    lib.q2_set_probe.argtypes = [I, P, P]
+    lib.q2_set_probe.restype = I
     _lib = lib
     return lib
 
@@ -83,6 +88,14 @@ def q2_status_string(status: int) -> str:
 
 def q2_version() -> int:
     return version()
+
+
+def q2_set_probe(kernel: int, ev_begin=None, ev_end=None) -> None:
+    """Bracket every later launch of `kernel` (a PROBE_* id) with the two torch.cuda.Event
+    records; PROBE_NONE turns the hook off.  The events must be created with timing."""
+    b = None if ev_begin is None else ctypes.c_void_p(ev_begin.cuda_event)
+    e = None if ev_end is None else ctypes.c_void_p(ev_end.cuda_event)
+    _raise(load().q2_set_probe(int(kernel), b, e), "q2_set_probe")
 
 
 def _stream(stream=None) -> int:

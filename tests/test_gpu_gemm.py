@@ -126,3 +126,26 @@ def test_deterministic_and_ldy(env):
     q2v.q2_tiny_gemm(Wd, g["N"], g["K"], Ad, Y=Yp)
     assert torch.equal(Yp[:, :g["N"]].cpu(), Y1)
     assert torch.all(Yp[:, g["N"]:] == 7.0)
+
+
+def test_probe_brackets_the_gemm_kernel(env):
+    """q2_set_probe records the caller's events around the GEMM kernel alone."""
+    import torch
+    dev, q2v, _ = env
+    g = synth.config_gemm(1, M=5)
+    Wd = to_dev(g["W"].reshape(-1), dev)
+    Ad = to_dev(g["A"], dev)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    b.record()
+    q2v.q2_set_probe(q2v.PROBE_GEMM, a, b)
+    try:
+        q2v.q2_tiny_gemm(Wd, g["N"], g["K"], Ad)
+    finally:
+        q2v.q2_set_probe(q2v.PROBE_NONE)
+    torch.cuda.synchronize()
+    assert 0.0 < a.elapsed_time(b) < 100.0
+    with pytest.raises(q2v.Q2Error):
+        q2v.q2_set_probe(99, a, b)
+    with pytest.raises(q2v.Q2Error):
+        q2v.q2_set_probe(q2v.PROBE_GEMM, None, None)
