@@ -53,7 +53,7 @@ bool gemm_k_ok(int K) { return K >= kBlockK && K % kBlockK == 0 && K <= kMaxTile
 
 size_t gemm_ws_bytes(int M, int K) {
     Carver c(nullptr);
-    c.take(PrepLayout(K).bytes(M));
+    c.take(umma_gemm_supported(M, K) ? umma_gemm_ws_bytes(M, K) : PrepLayout(K).bytes(M));
     return c.off;
 }
 
@@ -188,6 +188,14 @@ q2_status q2_tiny_gemm(const void *W, int N, int K, const uint16_t *A, int M, in
     if (wst != Q2_OK) return wst;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     Carver c(ws);
+    if (umma_gemm_supported(M, K)) {
+        void *img = c.take(umma_gemm_ws_bytes(M, K));
+        if (launch_prep_umma(A, lda, M, K, img, s) != cudaSuccess) return Q2_ERR_CUDA;
+        const int sms = device_sms();
+        return cuda_status(probed(kProbeGemm, s, [&] {
+            return launch_gemm_umma(W, N, K, M, img, Y, ldy, status_word(ws), sms, s);
+        }));
+    }
     const PrepLayout L(K);
     const PrepPtrs P = PrepPtrs::carve(c.take(L.bytes(M)), L, M);
     const cudaError_t e = launch_prep_bf16(A, lda, nullptr, M, K, P, L, s);

@@ -78,6 +78,16 @@ struct MoeWs {
 
 cudaError_t launch_moe(const MoeArgs &a, const MoeWs &w, int num_sms, cudaStream_t s);
 
+// q2_tiny_gemm on the tcgen05 tensor cores (q2v_umma.cu): kUmmaMinRowsExclusive < M <= 64
+// and K % 128 == 0 (the weight rows then start on 16-byte boundaries, as TMA needs).  The
+// prep writes the activation operand image into a workspace region of umma_gemm_ws_bytes.
+constexpr int kUmmaMinRowsExclusive = 16;
+bool umma_gemm_supported(int M, int K);
+size_t umma_gemm_ws_bytes(int M, int K);
+cudaError_t launch_prep_umma(const uint16_t *A, int lda, int M, int K, void *ws_region, cudaStream_t s);
+cudaError_t launch_gemm_umma(const void *W, int N, int K, int M, const void *ws_region, float *Y, int ldy,
+                             unsigned int *status, int num_sms, cudaStream_t s);
+
 // Measurement hook (q2_set_probe): records the caller's begin (end = 0) or end (end = 1)
 // event on s when `kernel` is the bracketed one; a no-op otherwise.
 enum ProbeKernel : int { kProbeMoeGateUp = 1, kProbeMoeDown = 2, kProbeGemm = 3, kProbePqStats = 4, kProbePqVerify = 5 };

@@ -1,0 +1,636 @@
+// q2v_umma.cu -- the Q2B32 dequant GEMM on the fifth-generation tensor cores (tcgen05),
+// for the wider verify batches: 17..64 activation rows, such as 12 sessions x (k+1) = 60
+// rows against the vocabulary head ("projections and the vocabulary head" of the K+1-row
+// verify, "Optimizing DeepSeek-V4-Flash on a single NVIDIA GB10/GX10 with DSpark
+// speculative decoding", page 2, verifier-bottleneck reply).  At 60 rows the contraction
+// is as heavy as the weight stream (about 250 flop per weight byte), so both the tensor
+// cores and HBM have to run flat out, overlapped.
+//
+// One persistent CTA per SM walks 128-row weight tiles.  Per tile, the K dimension goes by
+// in stages of 4 Q2B32 blocks (128 k):
+//   * TMA warp: one 2-D tensor copy per stage brings the tile's raw Q2B32 bytes
+//     (128 rows x 48 B) into a deep ring (the weights do not depend on the previous
+//     kernel, so this warp starts before the programmatic wait);
+//   * 8 dequant warps: decode the raw stage into the f16 A operand (UMMA canonical K-major
+//     layout, no swizzle) with the same exact lop3 + f16x2 fma decode as the small-M path,
+//     write the block offsets m into one extra k-group, and have one bulk copy bring the
+//     prepared activation stage (the B operand, laid out by prep_umma_kernel);
+//   * MMA thread: 9 tcgen05.mma (M=128, N=NPAD, K=16) per stage into a TMEM accumulator,
+//     double-buffered across tiles, committing each stage back to its producers;
+//   * 4 epilogue warps: tcgen05.ld the finished accumulator, undo the per-row activation
+//     exponent and store Y.
+// Every wait is bounded: on a time-out the CTA records Q2_ERR_TIMEOUT, lets the copies and
+// MMAs it issued land, frees its TMEM and returns.
+#include <cuda.h>
+
+#include "q2v_kernels.cuh"
+#include "q2v_mma_core.cuh"
+
+namespace q2v {
+
+namespace {
+
+constexpr int kUmRows = 128;                                     // weight rows per tile (UMMA M)
+constexpr int kUmBlocks = 4;                                     // Q2B32 blocks per stage
+constexpr int kUmKg = 18;                                        // 16-byte k-groups per stage
+constexpr int kUmMmas = kUmKg / 2;                               // K=16 instructions per stage
+constexpr int kUmKgBytes = (kUmRows / 8) * 128;                  // one k-group of A: 2048 B
+constexpr int kUmAStage = kUmKg * kUmKgBytes;                    // 36,864 B
+constexpr int kUmRawRow = kUmBlocks * kBlockBytes;               // 48 B
+constexpr int kUmRawStage = kUmRows * kUmRawRow;                 // 6,144 B
+constexpr int kUmABStages = 3;                                   // dequantized A stages
+constexpr int kUmBStages = 3;                                    // activation (B) stages
+constexpr int kUmRawStages = 8;                                  // raw Q2B32 stages
+constexpr int kUmGroup = 4;                                      // weight tiles sharing a B stage
+constexpr int kUmEpiWarps = 4;
+constexpr int kUmTmaWarp = 4;
+constexpr int kUmBWarp = 5;
+constexpr int kUmMmaWarp = 6;
+constexpr int kUmDeqWarp0 = 7;
+constexpr int kUmDeqWarps = 8;
+constexpr int kUmThreads = (kUmDeqWarp0 + kUmDeqWarps) * 32;    // 480
+constexpr uint64_t kUmWaitNs = 1000000000ull;                    // 1 s per wait, then give up
+
+// The dequant warps form kUmDeqGroups groups that take the stages in turn (stage g goes to
+// group g % kUmDeqGroups), so that several stages are decoded at once.
+constexpr int kUmDeqGroups = 2;
+constexpr int kUmDeqGroupWarps = kUmDeqWarps / kUmDeqGroups;
+constexpr int kUmItemsPerLane = kUmRows * kUmBlocks / (kUmDeqGroupWarps * 32);
+static_assert(kUmItemsPerLane * kUmDeqGroupWarps * 32 == kUmRows * kUmBlocks, "whole (row, block) items per lane");
+
+__host__ __device__ constexpr int um_bstage(int npad) { return kUmKg * (npad / 8) * 128; }
+// TMEM columns between accumulators (a power of two >= NPAD) and in all: two groups of
+// kUmGroup accumulators (512 columns at NPAD > 32, the whole of TMEM: one CTA per SM).
+__host__ __device__ constexpr uint32_t um_acc_stride(int npad) { return npad <= 16 ? 16u : npad <= 32 ? 32u : 64u; }
+__host__ __device__ constexpr uint32_t um_tmem_cols(int npad) {
+    return 2u * kUmGroup * um_acc_stride(npad) < 32u ? 32u : 2u * kUmGroup * um_acc_stride(npad);
+}
+static_assert(um_tmem_cols(64) <= 512, "TMEM holds 512 columns");
+
+struct UmShared {
+    uint64_t raw_full[kUmRawStages];
+    uint64_t raw_empty[kUmRawStages];
+    uint64_t ab_full[kUmABStages];   // the dequant warps have written A
+    uint64_t ab_empty[kUmABStages];  // the MMAs reading the A stage are done
+    uint64_t b_full[kUmBStages];     // the activation stage has landed
+    uint64_t b_empty[kUmBStages];    // the MMAs reading the B stage are done
+    uint64_t acc_full[2];
+    uint64_t acc_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    uint32_t abort_flag;
+    int exps[64];
+};
+
+__host__ __device__ constexpr size_t um_smem_bytes(int npad) {
+    return 1024 + (size_t)kUmABStages * kUmAStage + (size_t)kUmBStages * um_bstage(npad) +
+           (size_t)kUmRawStages * kUmRawStage + sizeof(UmShared);
+}
+
+// ---------------------------------------------------------------- PTX wrappers
+
+__device__ __forceinline__ uint32_t smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_tx(uint64_t *bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+
+// Wait for the phase of `parity` to complete.  False if another role gave up first or this
+// wait ran out of time (then it records the time-out and tells the other roles to stop).
+__device__ __forceinline__ bool um_wait(uint64_t *bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                        unsigned int *status) {
+    if (mbar_try(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (;;) {
+        if (mbar_try(bar, parity)) return true;
+        if (*abort_flag) return false;
+        if (global_ns() - t0 > kUmWaitNs) {
+            *abort_flag = 1u;
+            set_status(status, Q2_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// um_wait by every lane of a warp, with one outcome for the whole warp.
+__device__ __forceinline__ bool um_wait_warp(uint64_t *bar, uint32_t parity, volatile uint32_t *abort_flag,
+                                             unsigned int *status) {
+    const bool ok = um_wait(bar, parity, abort_flag, status);
+    return __all_sync(0xffffffffu, ok);
+}
+
+// Bounded wait used when winding down: copies and MMAs already issued complete by
+// themselves, so this only waits for them to land.
+__device__ __forceinline__ void um_drain(uint64_t *bar, uint32_t parity) {
+    const uint64_t t0 = global_ns();
+    while (!mbar_try(bar, parity) && global_ns() - t0 < kUmWaitNs) {
+    }
+}
+
+__device__ __forceinline__ void fence_async_smem() { asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory"); }
+__device__ __forceinline__ void fence_mbar_init() { asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory"); }
+
+__device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, int x, int y, uint64_t *bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3}], [%4];\n" ::
+            "r"(smem_u32(dst)),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
+        : "memory");
+}
+__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
+    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                     smem_u32(dst)),
+                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
+__device__ __forceinline__ void tc_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;\n" ::: "memory"); }
+
+// UMMA shared-memory descriptor, canonical K-major layout without swizzle: 8-row x 16-byte
+// core matrices stored as 128 contiguous bytes; `lbo` = byte distance between core
+// matrices adjacent in K, `sbo` = between core matrices adjacent in M (or N).
+__device__ __forceinline__ uint64_t umma_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+    return (uint64_t)((saddr & 0x3FFFFu) >> 4) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(sbo >> 4) << 32) |
+           (1ull << 46);  // descriptor version 1 (bits 46-48 = 0b001), base offset 0, no swizzle
+}
+
+// Instruction descriptor, kind::f16: f32 accumulator, f16 A and B, both K-major.
+template <int NPAD>
+__device__ __forceinline__ constexpr uint32_t umma_idesc() {
+    return (1u << 4) | ((uint32_t)(NPAD >> 3) << 17) | ((uint32_t)(kUmRows >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint64_t *bar) {
+    asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
+    uint32_t r[16];
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+        "%15}, [%16];\n"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+        : "r"(taddr));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+__device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
+
+// ---------------------------------------------------------------- activation prep
+
+// B operand image of the activations, one contiguous stage after another.  Stage s (Q2B32
+// blocks 4s..4s+3) holds 18 k-groups; k-group g, activation row m sits at byte
+//   s * um_bstage(NPAD) + g * (NPAD/8) * 128 + (m / 8) * 128 + (m % 8) * 16.
+// k-groups 4j..4j+3 are block 4s+j's 16 f16x2 pair slots (the order and scaling of
+// prep_store_block); k-group 16 holds the blocks' activation sums, hi parts in slots 0..3
+// and lo parts in slots 4..7 (they meet the blocks' m in the A operand); k-group 17 is zero.
+// Rows m >= M and blocks past K hold zeros.  One CTA per row m < NPAD, one thread per block.
+__global__ void __launch_bounds__(256) prep_umma_kernel(const uint16_t *__restrict__ src, int ld, int M, int nb,
+                                                        int nst, int npad, uint8_t *__restrict__ img,
+                                                        int *__restrict__ exps) {
+    __shared__ float scratch[32];
+    pdl_wait();
+    pdl_trigger();
+    const int m = blockIdx.x;
+    const int b = threadIdx.x;
+    const bool live = b < nb && m < M;
+    float v[32];
+    float mx = 0.0f;
+    if (live) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(src + (size_t)m * ld + (size_t)b * kBlockK);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 q = __ldg(p + j);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[8 * j + 2 * i] = __uint_as_float(w[i] << 16);
+                v[8 * j + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fabsf(v[j]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+    }
+    const int e = act_exponent(block_max_nonneg(mx, scratch));
+    if (b == 0 && m < 64) exps[m] = m < M ? e : 0;
+    if (b >= nst * kUmBlocks) return;
+    // pair slots and the block sum exactly as prep_store_block forms them
+    uint32_t words[16];
+    __half hs[32];
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 32; ++j) {
+        hs[j] = __float2half_rn(ldexpf(v[j], -e - 2 * (j & 3)));
+        s += __half2float(__float2half_rn(ldexpf(v[j], -e)));
+    }
+#pragma unroll
+    for (int p = 0; p < 16; ++p) {
+        const int k0 = 16 * (p >> 3) + (p & 7);
+        words[p] = pack_half2(hs[k0], hs[k0 + 8]);
+    }
+    const int st = b / kUmBlocks, bl = b % kUmBlocks;
+    const size_t kg_bytes = (size_t)(npad / 8) * 128;
+    uint8_t *base = img + (size_t)st * um_bstage(npad) + (size_t)(m >> 3) * 128 + (size_t)(m & 7) * 16;
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        *reinterpret_cast<uint4 *>(base + (size_t)(4 * bl + j) * kg_bytes) =
+            make_uint4(words[4 * j], words[4 * j + 1], words[4 * j + 2], words[4 * j + 3]);
+    const __half hi = __float2half_rn(s);
+    const __half lo = __float2half_rn(s - __half2float(hi));
+    __half *sums = reinterpret_cast<__half *>(base + 16 * kg_bytes);
+    sums[bl] = hi;
+    sums[4 + bl] = lo;
+    if (bl == 0) *reinterpret_cast<uint4 *>(base + 17 * kg_bytes) = make_uint4(0u, 0u, 0u, 0u);
+}
+
+// ---------------------------------------------------------------- the GEMM
+
+// A CTA's tiles are blockIdx.x, blockIdx.x + gridDim.x, ...; they are processed in groups of
+// up to kUmGroup tiles that share each activation stage: for every stage s the group's tiles
+// are multiplied one after another, each into its own TMEM accumulator, so one copy of the
+// B stage serves kUmGroup weight tiles.  Accumulators are double-buffered across groups.
+template <int NPAD>
+__global__ void __launch_bounds__(kUmThreads, 1)
+    q2_gemm_umma_kernel(const __grid_constant__ CUtensorMap wmap, int N, int nst, const uint8_t *__restrict__ bimg,
+                        const int *__restrict__ exps, int M, float *__restrict__ Y, int ldy,
+                        unsigned int *status) {
+    constexpr int kB = um_bstage(NPAD);
+    constexpr uint32_t kStride = um_acc_stride(NPAD);
+    constexpr uint32_t kCols = um_tmem_cols(NPAD);
+    extern __shared__ uint8_t um_smem_raw[];
+    uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(um_smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t *sA = sm;
+    uint8_t *sB = sA + kUmABStages * kUmAStage;
+    uint8_t *sR = sB + kUmBStages * kB;
+    UmShared *sh = reinterpret_cast<UmShared *>(sR + kUmRawStages * kUmRawStage);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntiles = cdiv(N, kUmRows);
+    const int my_tiles = blockIdx.x < ntiles ? cdiv(ntiles - (int)blockIdx.x, (int)gridDim.x) : 0;
+    const int ngroups = cdiv(my_tiles, kUmGroup);
+
+    // ---- set-up: barriers, the zero k-group of every A stage, TMEM
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < kUmRawStages; ++i) {
+            mbar_init(&sh->raw_full[i], 1);
+            mbar_init(&sh->raw_empty[i], kUmDeqGroupWarps);
+        }
+        for (int i = 0; i < kUmABStages; ++i) {
+            mbar_init(&sh->ab_full[i], kUmDeqGroupWarps);
+            mbar_init(&sh->ab_empty[i], 1);
+        }
+        for (int i = 0; i < kUmBStages; ++i) {
+            mbar_init(&sh->b_full[i], 1);
+            mbar_init(&sh->b_empty[i], 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(&sh->acc_full[i], 1);
+            mbar_init(&sh->acc_empty[i], kUmEpiWarps);
+        }
+        mbar_init(&sh->drain, 1);
+        sh->abort_flag = 0u;
+        fence_mbar_init();
+    }
+    for (int i = threadIdx.x; i < kUmABStages * (kUmKgBytes / 16); i += blockDim.x) {
+        const int a = i / (kUmKgBytes / 16), j = i % (kUmKgBytes / 16);
+        *reinterpret_cast<uint4 *>(sA + (size_t)a * kUmAStage + 17 * kUmKgBytes + j * 16) = make_uint4(0u, 0u, 0u, 0u);
+    }
+    fence_async_smem();
+    if (warp == kUmMmaWarp) {
+        asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
+                         smem_u32(&sh->tmem_base)),
+                     "r"(kCols)
+                     : "memory");
+        asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = sh->tmem_base;
+    volatile uint32_t *abort_flag = &sh->abort_flag;
+
+    if (warp == kUmTmaWarp) {
+        // ---- raw weight stages, in the order the dequant warps consume them (independent of
+        // the previous kernel: no programmatic wait)
+        if (lane == 0) {
+            uint32_t g = 0;
+            bool ok = true;
+            for (int q = 0; ok && q < ngroups; ++q) {
+                const int t0 = q * kUmGroup, tn = min(kUmGroup, my_tiles - t0);
+                for (int s = 0; ok && s < nst; ++s) {
+                    for (int t = 0; t < tn; ++t) {
+                        const uint32_t r = g % kUmRawStages;
+                        if (!um_wait(&sh->raw_empty[r], ((g / kUmRawStages) & 1u) ^ 1u, abort_flag, status)) {
+                            ok = false;
+                            break;
+                        }
+                        mbar_arrive_tx(&sh->raw_full[r], kUmRawStage);
+                        tma_load_2d(sR + (size_t)r * kUmRawStage, &wmap, s * kUmRawRow,
+                                    ((int)blockIdx.x + (t0 + t) * (int)gridDim.x) * kUmRows, &sh->raw_full[r]);
+                        ++g;
+                    }
+                }
+            }
+            // every copy issued lands before the CTA can exit
+            for (uint32_t i = g > (uint32_t)kUmRawStages ? g - kUmRawStages : 0u; i < g; ++i)
+                um_drain(&sh->raw_full[i % kUmRawStages], (i / kUmRawStages) & 1u);
+        }
+    } else if (warp == kUmBWarp) {
+        // ---- activation stages (written by the prep kernel: after the programmatic wait)
+        if (lane == 0) {
+            pdl_wait();
+            uint32_t g = 0;
+            bool ok = true;
+            for (int q = 0; ok && q < ngroups; ++q) {
+                for (int s = 0; s < nst; ++s) {
+                    const uint32_t b = g % kUmBStages;
+                    if (!um_wait(&sh->b_empty[b], ((g / kUmBStages) & 1u) ^ 1u, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    mbar_arrive_tx(&sh->b_full[b], kB);
+                    bulk_load(sB + (size_t)b * kB, bimg + (size_t)s * kB, kB, &sh->b_full[b]);
+                    ++g;
+                }
+            }
+            for (uint32_t i = g > (uint32_t)kUmBStages ? g - kUmBStages : 0u; i < g; ++i)
+                um_drain(&sh->b_full[i % kUmBStages], (i / kUmBStages) & 1u);
+        }
+    } else if (warp == kUmMmaWarp) {
+        // ---- MMA issue (one thread)
+        if (lane == 0) {
+            constexpr uint32_t idesc = umma_idesc<NPAD>();
+            // descriptors of slot 0, k-step 0; a descriptor's low field is the start address
+            // / 16 (below 2^14 anywhere in shared memory), so other slots and k-steps are
+            // plain additions
+            const uint64_t adesc0 = umma_desc(smem_u32(sA), kUmKgBytes, 128);
+            const uint64_t bdesc0 = umma_desc(smem_u32(sB), (NPAD / 8) * 128, 128);
+            constexpr uint64_t kAStep = (2 * kUmKgBytes) >> 4, kBStep = (2 * (NPAD / 8) * 128) >> 4;
+            uint32_t ga = 0, gb = 0;
+            bool ok = true;
+            for (int q = 0; ok && q < ngroups; ++q) {
+                const int tn = min(kUmGroup, my_tiles - q * kUmGroup);
+                const uint32_t buf = (uint32_t)q & 1u;
+                if (!um_wait(&sh->acc_empty[buf], (((uint32_t)q >> 1) & 1u) ^ 1u, abort_flag, status)) break;
+                tc_fence_after();
+                for (int s = 0; ok && s < nst; ++s, ++gb) {
+                    const uint32_t b = gb % kUmBStages;
+                    if (!um_wait(&sh->b_full[b], (gb / kUmBStages) & 1u, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint64_t bd = bdesc0 + (uint64_t)((b * (uint32_t)kB) >> 4);
+                    for (int t = 0; t < tn; ++t, ++ga) {
+                        const uint32_t a = ga % kUmABStages;
+                        if (!um_wait(&sh->ab_full[a], (ga / kUmABStages) & 1u, abort_flag, status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint64_t ad = adesc0 + (uint64_t)((a * (uint32_t)kUmAStage) >> 4);
+                        const uint32_t d = tmem + (buf * kUmGroup + (uint32_t)t) * kStride;
+                        umma_f16(d, ad, bd, idesc, s != 0);
+#pragma unroll
+                        for (int j = 1; j < kUmMmas; ++j) umma_f16(d, ad + j * kAStep, bd + j * kBStep, idesc, 1u);
+                        umma_commit(&sh->ab_empty[a]);
+                    }
+                    if (!ok) break;
+                    umma_commit(&sh->b_empty[b]);
+                }
+                if (!ok) break;
+                umma_commit(&sh->acc_full[buf]);
+            }
+            // no MMA may still be running when the CTA frees TMEM or exits
+            umma_commit(&sh->drain);
+            um_drain(&sh->drain, 0u);
+        }
+    } else if (warp >= kUmDeqWarp0) {
+        // ---- dequant: raw Q2B32 stage -> f16 A stage (+ the m k-group)
+        const int grp = (warp - kUmDeqWarp0) / kUmDeqGroupWarps;
+        const int gw = (warp - kUmDeqWarp0) % kUmDeqGroupWarps;
+        bool bad = false;
+        const uint32_t total = (uint32_t)my_tiles * (uint32_t)nst;
+        for (uint32_t g = (uint32_t)grp; g < total; g += kUmDeqGroups) {
+            const uint32_t r = g % kUmRawStages, a = g % kUmABStages;
+            if (!um_wait_warp(&sh->raw_full[r], (g / kUmRawStages) & 1u, abort_flag, status) ||
+                !um_wait_warp(&sh->ab_empty[a], ((g / kUmABStages) & 1u) ^ 1u, abort_flag, status))
+                break;
+            const uint32_t *raw = reinterpret_cast<const uint32_t *>(sR + (size_t)r * kUmRawStage);
+            uint8_t *A = sA + (size_t)a * kUmAStage;
+#pragma unroll
+            for (int it = 0; it < kUmItemsPerLane; ++it) {
+                // lane -> (row = 8 consecutive rows, block = lane / 8): the raw words 12 row + 3 block
+                // fall in 32 distinct banks, and each quarter-warp stores one 128-byte run of a
+                // k-group (8 rows x 16 B): no bank conflicts either way
+                const int row = (it * kUmDeqGroupWarps + gw) * 8 + (lane & 7), bl = lane >> 3;
+                const int item = row * kUmBlocks + bl;
+                const uint32_t c0 = raw[3 * item], c1 = raw[3 * item + 1], dm = raw[3 * item + 2];
+                bad |= scale_out_of_range(dm);
+                uint32_t d2, nd;
+                scale_pair(dm, d2, nd);
+                const uint32_t h0 = c0 >> 8, h1 = c1 >> 8;
+                uint32_t w[16];
+                w[0] = dequant_pos<0>(c0, d2, nd);
+                w[1] = dequant_pos<2>(c0, d2, nd);
+                w[2] = dequant_pos<4>(c0, d2, nd);
+                w[3] = dequant_pos<6>(c0, d2, nd);
+                w[4] = dequant_pos<0>(h0, d2, nd);
+                w[5] = dequant_pos<2>(h0, d2, nd);
+                w[6] = dequant_pos<4>(h0, d2, nd);
+                w[7] = dequant_pos<6>(h0, d2, nd);
+                w[8] = dequant_pos<0>(c1, d2, nd);
+                w[9] = dequant_pos<2>(c1, d2, nd);
+                w[10] = dequant_pos<4>(c1, d2, nd);
+                w[11] = dequant_pos<6>(c1, d2, nd);
+                w[12] = dequant_pos<0>(h1, d2, nd);
+                w[13] = dequant_pos<2>(h1, d2, nd);
+                w[14] = dequant_pos<4>(h1, d2, nd);
+                w[15] = dequant_pos<6>(h1, d2, nd);
+                uint8_t *dst = A + (row >> 3) * 128 + (row & 7) * 16;
+#pragma unroll
+                for (int j = 0; j < 4; ++j)
+                    *reinterpret_cast<uint4 *>(dst + (4 * bl + j) * kUmKgBytes) =
+                        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+                const unsigned short mh = (unsigned short)(dm >> 16);
+                unsigned short *mk = reinterpret_cast<unsigned short *>(dst + 16 * kUmKgBytes);
+                mk[bl] = mh;
+                mk[4 + bl] = mh;
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(&sh->ab_full[a]);
+                mbar_arrive(&sh->raw_empty[r]);
+            }
+        }
+        if (bad) set_status(status, Q2_ERR_RANGE);
+    } else {
+        // ---- epilogue: TMEM -> registers -> Y (warp w reads TMEM lanes 32w..32w+31)
+        pdl_wait();
+        pdl_trigger();
+        if (threadIdx.x < 64) sh->exps[threadIdx.x] = threadIdx.x < M ? exps[threadIdx.x] : 0;
+        asm volatile("bar.sync 1, %0;\n" ::"n"(kUmEpiWarps * 32) : "memory");
+        for (int q = 0; q < ngroups; ++q) {
+            const int t0 = q * kUmGroup, tn = min(kUmGroup, my_tiles - t0);
+            const uint32_t buf = (uint32_t)q & 1u;
+            if (!um_wait_warp(&sh->acc_full[buf], ((uint32_t)q >> 1) & 1u, abort_flag, status)) break;
+            tc_fence_after();
+            for (int t = 0; t < tn; ++t) {
+                float v[NPAD];
+                const uint32_t col = (buf * kUmGroup + (uint32_t)t) * kStride;
+#pragma unroll
+                for (int c = 0; c < NPAD / 16; ++c)
+                    tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + col + (uint32_t)(c * 16), v + 16 * c);
+                tmem_wait_ld();
+                const int n = ((int)blockIdx.x + (t0 + t) * (int)gridDim.x) * kUmRows + warp * 32 + lane;
+                if (n < N) {
+#pragma unroll
+                    for (int m = 0; m < NPAD; ++m)
+                        if (m < M) Y[(size_t)m * ldy + n] = ldexpf(v[m], sh->exps[m]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh->acc_empty[buf]);
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == kUmMmaWarp) {
+        __syncwarp();
+        tc_fence_after();
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kCols) : "memory");
+    }
+}
+
+// ---------------------------------------------------------------- host side
+
+using EncodeTiledFn = CUresult (*)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *, const cuuint64_t *,
+                                   const cuuint64_t *, const cuuint32_t *, const cuuint32_t *, CUtensorMapInterleave,
+                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_tiled() {
+    static EncodeTiledFn fn = nullptr;
+    static bool tried = false;
+    if (!tried) {
+        tried = true;
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeTiledFn>(p);
+    }
+    return fn;
+}
+
+size_t g_umma_smem[4];  // dynamic shared memory each NPAD variant was configured for
+
+template <int NPAD>
+cudaError_t launch_umma_variant(const CUtensorMap &map, int N, int nst, const uint8_t *img, const int *exps, int M,
+                                float *Y, int ldy, unsigned int *status, int num_sms, cudaStream_t s) {
+    auto kern = q2_gemm_umma_kernel<NPAD>;
+    const size_t smem = um_smem_bytes(NPAD);
+    size_t &have = g_umma_smem[NPAD / 16 - 1];
+    if (have < smem) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        have = smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(min(cdiv(N, kUmRows), num_sms));
+    cfg.blockDim = dim3(kUmThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, map, N, nst, img, exps, M, Y, ldy, status);
+}
+
+}  // namespace
+
+bool umma_gemm_supported(int M, int K) { return M > kUmmaMinRowsExclusive && M <= 64 && K % 128 == 0; }
+
+size_t umma_gemm_ws_bytes(int M, int K) {
+    const int npad = cdiv(M, 16) * 16;
+    const int nst = cdiv(K / kBlockK, kUmBlocks);
+    return align_up((size_t)nst * um_bstage(npad), 256) + 256;
+}
+
+cudaError_t launch_prep_umma(const uint16_t *A, int lda, int M, int K, void *ws_region, cudaStream_t s) {
+    const int nb = K / kBlockK;
+    const int nst = cdiv(nb, kUmBlocks);
+    const int npad = cdiv(M, 16) * 16;
+    uint8_t *img = static_cast<uint8_t *>(ws_region);
+    int *exps = reinterpret_cast<int *>(img + align_up((size_t)nst * um_bstage(npad), 256));
+    return launch_pdl(prep_umma_kernel, dim3(npad), dim3(32 * cdiv(nst * kUmBlocks, 32)), s, A, lda, M, nb, nst,
+                      npad, img, exps);
+}
+
+cudaError_t launch_gemm_umma(const void *W, int N, int K, int M, const void *ws_region, float *Y, int ldy,
+                             unsigned int *status, int num_sms, cudaStream_t s) {
+    const EncodeTiledFn encode = encode_tiled();
+    if (!encode) return cudaErrorNotSupported;
+    const int nb = K / kBlockK;
+    const int nst = cdiv(nb, kUmBlocks);
+    const int npad = cdiv(M, 16) * 16;
+    const uint8_t *img = static_cast<const uint8_t *>(ws_region);
+    const int *exps = reinterpret_cast<const int *>(img + align_up((size_t)nst * um_bstage(npad), 256));
+    // the weights as a 2-D byte tensor [N rows][row_bytes]; one box = 48 B x 128 rows
+    CUtensorMap map;
+    const size_t row_bytes = (size_t)nb * kBlockBytes;
+    const cuuint64_t dims[2] = {(cuuint64_t)row_bytes, (cuuint64_t)N};
+    const cuuint64_t strides[1] = {(cuuint64_t)row_bytes};
+    const cuuint32_t box[2] = {(cuuint32_t)kUmRawRow, (cuuint32_t)kUmRows};
+    const cuuint32_t estr[2] = {1, 1};
+    if (encode(&map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(W), dims, strides, box, estr,
+               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return cudaErrorInvalidValue;
+    switch (npad) {
+        case 16: return launch_umma_variant<16>(map, N, nst, img, exps, M, Y, ldy, status, num_sms, s);
+        case 32: return launch_umma_variant<32>(map, N, nst, img, exps, M, Y, ldy, status, num_sms, s);
+        case 48: return launch_umma_variant<48>(map, N, nst, img, exps, M, Y, ldy, status, num_sms, s);
+        default: return launch_umma_variant<64>(map, N, nst, img, exps, M, Y, ldy, status, num_sms, s);
+    }
+}
+
+}  // namespace q2v

@@ -149,3 +149,84 @@ def test_probe_brackets_the_gemm_kernel(env):
         q2v.q2_set_probe(99, a, b)
     with pytest.raises(q2v.Q2Error):
         q2v.q2_set_probe(q2v.PROBE_GEMM, None, None)
+
+
+# ---- the tcgen05 path (17 <= M <= 64 with K % 128 == 0); other K fall back to mma.sync
+
+@pytest.mark.parametrize("M,N,K", [
+    (17, 129, 128),     # one stage, ragged N just past one 128-row tile, 32-row padding
+    (24, 300, 256),
+    (32, 128, 4096),    # exactly one tile
+    (33, 1, 128),       # a single output row (the rest of the tile is TMA zero fill)
+    (40, 257, 1024),    # 48-row padding
+    (48, 1000, 512),
+    (60, 2049, 4096),   # the cohort row count, many tiles per CTA, ragged tail
+    (64, 4096, 8192),   # the largest M and K
+    (20, 127, 384),     # three stages, fewer rows than a tile
+    (24, 100000, 256),  # 782 tiles: 5-6 per CTA, a full group of 4 then a partial one
+    (48, 160000, 128),  # 1250 tiles: 8-9 per CTA, two full groups and a one-tile group
+    (33, 50, 160),      # K % 128 != 0: the mma.sync path
+])
+def test_umma_shapes(env, M, N, K):
+    st = synth.Streams(5000 + M * 7 + N + K)
+    W = synth.q2b32_weights(st, N, K)
+    A = synth.activations_bf16(st, M, K)
+    Y = _run(env, W, N, K, A)
+    Yo, absY = env[2].gemm(W, N, K, A)
+    check_gemm(Y, Yo, absY, f"M={M} N={N} K={K}")
+
+
+def test_umma_activation_and_scale_extremes(env):
+    """Per-row exponents far apart within one tile, a zero row, and the largest in-range
+    scales, on the tcgen05 path."""
+    st = synth.Streams(81)
+    M, N, K = 24, 200, 512
+    codes = st["codes"].integers(0, 4, size=(N, K), dtype=np.uint8)
+    d = st["d"].uniform(0.01, 0.05, size=(N, K // 32))
+    d[0:16] = 0.0
+    d[16:40] = 60.0
+    m = st["m"].normal(0, 0.02, size=(N, K // 32))
+    W = synth.pack_q2b32(codes, synth.fp16_bits(d), synth.fp16_bits(m))
+    a = st["A"].normal(0, 1, size=(M, K))
+    a[0] *= 1e30
+    a[1] *= 1e-30
+    a[2] = 0.0
+    a[3] *= 7e4
+    A = synth.bf16_bits(a)
+    Y = _run(env, W, N, K, A)
+    Yo, absY = env[2].gemm(W, N, K, A)
+    assert np.all(Y[2] == 0.0)
+    rows = [r for r in range(M) if r != 2]
+    check_gemm(Y[rows], Yo[rows], absY[rows], "umma extremes")
+
+
+def test_umma_scale_out_of_range_sets_status(env):
+    dev, q2v, _ = env
+    st = synth.Streams(82)
+    N, K, M = 160, 256, 20
+    codes = st["codes"].integers(0, 4, size=(N, K), dtype=np.uint8)
+    d = np.full((N, K // 32), 0.02)
+    d[150, 5] = -64.0
+    W = synth.pack_q2b32(codes, synth.fp16_bits(d), synth.fp16_bits(np.zeros((N, K // 32))))
+    A = synth.activations_bf16(st, M, K)
+    ws = q2v.workspace(q2v.q2_tiny_gemm_workspace(M, N, K), dev)
+    _run(env, W, N, K, A, ws=ws)
+    assert q2v.q2_get_device_status(ws) == 8  # Q2_ERR_RANGE
+    assert q2v.q2_get_device_status(ws) == 0
+
+
+def test_umma_deterministic_and_ldy(env):
+    import torch
+    dev, q2v, _ = env
+    st = synth.Streams(83)
+    M, N, K = 60, 700, 1024
+    W = synth.q2b32_weights(st, N, K)
+    A = synth.activations_bf16(st, M, K)
+    Wd, Ad = to_dev(W.reshape(-1), dev), to_dev(A, dev)
+    Y1 = q2v.q2_tiny_gemm(Wd, N, K, Ad).cpu()
+    Y2 = q2v.q2_tiny_gemm(Wd, N, K, Ad).cpu()
+    assert torch.equal(Y1, Y2)
+    Yp = torch.full((M, N + 5), 7.0, device=dev)
+    q2v.q2_tiny_gemm(Wd, N, K, Ad, Y=Yp)
+    assert torch.equal(Yp[:, :N].cpu(), Y1)
+    assert torch.all(Yp[:, N:] == 7.0)
