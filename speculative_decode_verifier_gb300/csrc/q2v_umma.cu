@@ -9,18 +9,22 @@
 // One persistent CTA per SM walks 128-row weight tiles.  Per tile, the K dimension goes by
 // in stages of 4 Q2B32 blocks (128 k):
 //   * TMA warp: one 2-D tensor copy per stage brings the tile's raw Q2B32 bytes
-//     (128 rows x 48 B) into a deep ring (the weights do not depend on the previous
-//     kernel, so this warp starts before the programmatic wait);
-//   * 8 dequant warps: decode the raw stage into the f16 A operand (UMMA canonical K-major
-//     layout, no swizzle) with the same exact lop3 + f16x2 fma decode as the small-M path,
-//     write the block offsets m into one extra k-group, and have one bulk copy bring the
-//     prepared activation stage (the B operand, laid out by prep_umma_kernel);
-//   * MMA thread: 9 tcgen05.mma (M=128, N=NPAD, K=16) per stage into a TMEM accumulator,
-//     double-buffered across tiles, committing each stage back to its producers;
-//   * 4 epilogue warps: tcgen05.ld the finished accumulator, undo the per-row activation
+//     (128 rows x 48 B) into a deep shared-memory ring (the weights do not depend on the
+//     previous kernel, so this warp starts before the programmatic wait);
+//   * B warp: one bulk copy per stage brings the prepared activation stage (the B operand,
+//     laid out by prep_umma_kernel) into a shared-memory ring;
+//   * 8 dequant warps, in two groups that take the stages in turn: each thread decodes one
+//     weight row of the stage with the exact lop3 + f16x2 fma decode and writes it straight
+//     from registers into tensor memory (tcgen05.st) as the MMA's A operand; the blocks'
+//     offsets m go to a small shared-memory tile;
+//   * MMA thread: per stage 8 tcgen05.mma (M=128, N=NPAD, K=16) with A read from TMEM plus
+//     one with A = the m tile against the activation block sums, into a TMEM accumulator;
+//     two tiles share each activation stage, and accumulators are double-buffered;
+//   * 4 epilogue warps: tcgen05.ld the finished accumulators, undo the per-row activation
 //     exponent and store Y.
-// Every wait is bounded: on a time-out the CTA records Q2_ERR_TIMEOUT, lets the copies and
-// MMAs it issued land, frees its TMEM and returns.
+// Keeping A in TMEM leaves only the 2 KB activation operand to be read from shared memory
+// per MMA.  Every wait is bounded: on a time-out the CTA records Q2_ERR_TIMEOUT, lets the
+// copies and MMAs it issued land, frees its TMEM and returns.
 #include <cuda.h>
 
 #include "q2v_kernels.cuh"
@@ -32,46 +36,43 @@ namespace {
 
 constexpr int kUmRows = 128;                                     // weight rows per tile (UMMA M)
 constexpr int kUmBlocks = 4;                                     // Q2B32 blocks per stage
-constexpr int kUmKg = 18;                                        // 16-byte k-groups per stage
-constexpr int kUmMmas = kUmKg / 2;                               // K=16 instructions per stage
-constexpr int kUmKgBytes = (kUmRows / 8) * 128;                  // one k-group of A: 2048 B
-constexpr int kUmAStage = kUmKg * kUmKgBytes;                    // 36,864 B
-constexpr int kUmRawRow = kUmBlocks * kBlockBytes;               // 48 B
-constexpr int kUmRawStage = kUmRows * kUmRawRow;                 // 6,144 B
-constexpr int kUmABStages = 3;                                   // dequantized A stages
-constexpr int kUmBStages = 3;                                    // activation (B) stages
-constexpr int kUmRawStages = 8;                                  // raw Q2B32 stages
-constexpr int kUmGroup = 4;                                      // weight tiles sharing a B stage
+constexpr int kUmKg = 18;                                        // 16-byte k-groups per B stage
+constexpr int kUmDataMmas = 8;                                   // K=16 MMAs on the weights per stage
+constexpr int kUmKgBytes = (kUmRows / 8) * 128;                  // one k-group of a 128-row tile
+constexpr int kUmMTile = 2 * kUmKgBytes;                         // m k-group + zero k-group: 4,096 B
+constexpr int kUmACols = kUmBlocks * 16;                         // TMEM columns of one A stage (64)
+constexpr int kUmRawSpan = 4;                                    // stages per raw copy
+constexpr int kUmStageRaw = kUmBlocks * kBlockBytes;             // 48 raw bytes of a row per stage
+constexpr int kUmRawRow = kUmRawSpan * kUmStageRaw;              // 192 B of each row per raw copy
+constexpr int kUmRawStage = kUmRows * kUmRawRow;                 // 24,576 B
+constexpr int kUmAStages = 4;                                    // A stages in TMEM (+ m tiles)
+constexpr int kUmBStages = 4;                                    // activation (B) stages
+constexpr int kUmBLag = 2;                                       // B stages in flight before signalling
+constexpr int kUmRawStages = 5;                                  // raw copies in flight
+constexpr int kUmGroup = 2;                                      // weight tiles sharing a B stage
+constexpr int kUmAccStride = 64;                                 // TMEM columns per accumulator
+constexpr int kUmAccBase = kUmAStages * kUmACols;                // accumulators after the A stages
+constexpr uint32_t kUmCols = 512;                                // all of TMEM: one CTA per SM
 constexpr int kUmEpiWarps = 4;
 constexpr int kUmTmaWarp = 4;
 constexpr int kUmBWarp = 5;
-constexpr int kUmMmaWarp = 6;
-constexpr int kUmDeqWarp0 = 7;
-constexpr int kUmDeqWarps = 8;
-constexpr int kUmThreads = (kUmDeqWarp0 + kUmDeqWarps) * 32;    // 480
+constexpr int kUmMmaWarp = 6;                                    // MMA thread of the group's tile 0 (+1: tile 1)
+constexpr int kUmDeqWarp0 = kUmMmaWarp + kUmGroup;
+constexpr int kUmDeqGroups = 2;                                  // groups take the stages in turn
+constexpr int kUmDeqWarps = 4 * kUmDeqGroups;                   // a group: one warp per TMEM lane quarter
+constexpr int kUmThreads = (kUmDeqWarp0 + kUmDeqWarps) * 32;    // 512
 constexpr uint64_t kUmWaitNs = 1000000000ull;                    // 1 s per wait, then give up
 
-// The dequant warps form kUmDeqGroups groups that take the stages in turn (stage g goes to
-// group g % kUmDeqGroups), so that several stages are decoded at once.
-constexpr int kUmDeqGroups = 2;
-constexpr int kUmDeqGroupWarps = kUmDeqWarps / kUmDeqGroups;
-constexpr int kUmItemsPerLane = kUmRows * kUmBlocks / (kUmDeqGroupWarps * 32);
-static_assert(kUmItemsPerLane * kUmDeqGroupWarps * 32 == kUmRows * kUmBlocks, "whole (row, block) items per lane");
+static_assert(kUmAccBase + 2 * kUmGroup * kUmAccStride <= (int)kUmCols, "TMEM holds 512 columns");
+static_assert(kUmGroup == 2, "one MMA-issuing warp per tile of a group");
 
 __host__ __device__ constexpr int um_bstage(int npad) { return kUmKg * (npad / 8) * 128; }
-// TMEM columns between accumulators (a power of two >= NPAD) and in all: two groups of
-// kUmGroup accumulators (512 columns at NPAD > 32, the whole of TMEM: one CTA per SM).
-__host__ __device__ constexpr uint32_t um_acc_stride(int npad) { return npad <= 16 ? 16u : npad <= 32 ? 32u : 64u; }
-__host__ __device__ constexpr uint32_t um_tmem_cols(int npad) {
-    return 2u * kUmGroup * um_acc_stride(npad) < 32u ? 32u : 2u * kUmGroup * um_acc_stride(npad);
-}
-static_assert(um_tmem_cols(64) <= 512, "TMEM holds 512 columns");
 
 struct UmShared {
     uint64_t raw_full[kUmRawStages];
     uint64_t raw_empty[kUmRawStages];
-    uint64_t ab_full[kUmABStages];   // the dequant warps have written A
-    uint64_t ab_empty[kUmABStages];  // the MMAs reading the A stage are done
+    uint64_t ab_full[kUmAStages];    // the dequant warps have written A (TMEM) and the m tile
+    uint64_t ab_empty[kUmAStages];   // the MMAs reading the A stage are done
     uint64_t b_full[kUmBStages];     // the activation stage has landed
     uint64_t b_empty[kUmBStages];    // the MMAs reading the B stage are done
     uint64_t acc_full[2];
@@ -83,7 +84,7 @@ struct UmShared {
 };
 
 __host__ __device__ constexpr size_t um_smem_bytes(int npad) {
-    return 1024 + (size_t)kUmABStages * kUmAStage + (size_t)kUmBStages * um_bstage(npad) +
+    return 1024 + (size_t)kUmBStages * um_bstage(npad) + (size_t)kUmAStages * kUmMTile +
            (size_t)kUmRawStages * kUmRawStage + sizeof(UmShared);
 }
 
@@ -96,6 +97,9 @@ __device__ __forceinline__ void mbar_init(uint64_t *bar, uint32_t count) {
 }
 __device__ __forceinline__ void mbar_arrive(uint64_t *bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_n(uint64_t *bar, uint32_t n) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(n) : "memory");
 }
 __device__ __forceinline__ void mbar_arrive_tx(uint64_t *bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(smem_u32(bar)), "r"(bytes)
@@ -190,6 +194,15 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
         "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
         : "memory");
 }
+// Same, with A read from tensor memory (a_tmem = its first column, lane 0).
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+        " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
 __device__ __forceinline__ void umma_commit(uint64_t *bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(smem_u32(bar))
                  : "memory");
@@ -206,6 +219,12 @@ __device__ __forceinline__ void tmem_ld16(uint32_t taddr, float *v) {
 #pragma unroll
     for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
+// This thread's TMEM lane, 32 consecutive columns from taddr: r[i] -> column i.
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};\n" ::"r"(taddr), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]), "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]), "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+                 : "memory");
+}
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
 // ---------------------------------------------------------------- activation prep
@@ -280,60 +299,87 @@ __global__ void __launch_bounds__(256) prep_umma_kernel(const uint16_t *__restri
 
 // ---------------------------------------------------------------- the GEMM
 
+// Decode one weight row of a stage (4 Q2B32 blocks = 48 raw bytes) into 64 f16x2 words, word
+// 16*b + p = pair slot p of block b (the order prep_store_block gives the activations).
+__device__ __forceinline__ void um_decode_blocks(const uint32_t *raw, uint32_t *w, bool &bad) {
+#pragma unroll
+    for (int b = 0; b < 2; ++b) {
+        const uint32_t c0 = raw[3 * b], c1 = raw[3 * b + 1], dm = raw[3 * b + 2];
+        bad |= scale_out_of_range(dm);
+        uint32_t d2, nd;
+        scale_pair(dm, d2, nd);
+        const uint32_t h0 = c0 >> 8, h1 = c1 >> 8;
+        uint32_t *o = w + 16 * b;
+        o[0] = dequant_pos<0>(c0, d2, nd);
+        o[1] = dequant_pos<2>(c0, d2, nd);
+        o[2] = dequant_pos<4>(c0, d2, nd);
+        o[3] = dequant_pos<6>(c0, d2, nd);
+        o[4] = dequant_pos<0>(h0, d2, nd);
+        o[5] = dequant_pos<2>(h0, d2, nd);
+        o[6] = dequant_pos<4>(h0, d2, nd);
+        o[7] = dequant_pos<6>(h0, d2, nd);
+        o[8] = dequant_pos<0>(c1, d2, nd);
+        o[9] = dequant_pos<2>(c1, d2, nd);
+        o[10] = dequant_pos<4>(c1, d2, nd);
+        o[11] = dequant_pos<6>(c1, d2, nd);
+        o[12] = dequant_pos<0>(h1, d2, nd);
+        o[13] = dequant_pos<2>(h1, d2, nd);
+        o[14] = dequant_pos<4>(h1, d2, nd);
+        o[15] = dequant_pos<6>(h1, d2, nd);
+    }
+}
+
 // A CTA's tiles are blockIdx.x, blockIdx.x + gridDim.x, ...; they are processed in groups of
 // up to kUmGroup tiles that share each activation stage: for every stage s the group's tiles
-// are multiplied one after another, each into its own TMEM accumulator, so one copy of the
-// B stage serves kUmGroup weight tiles.  Accumulators are double-buffered across groups.
+// are multiplied one after another, each into its own TMEM accumulator.
 template <int NPAD>
 __global__ void __launch_bounds__(kUmThreads, 1)
     q2_gemm_umma_kernel(const __grid_constant__ CUtensorMap wmap, int N, int nst, const uint8_t *__restrict__ bimg,
                         const int *__restrict__ exps, int M, float *__restrict__ Y, int ldy,
                         unsigned int *status) {
     constexpr int kB = um_bstage(NPAD);
-    constexpr uint32_t kStride = um_acc_stride(NPAD);
-    constexpr uint32_t kCols = um_tmem_cols(NPAD);
     extern __shared__ uint8_t um_smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(um_smem_raw) + 1023) & ~uintptr_t(1023));
-    uint8_t *sA = sm;
-    uint8_t *sB = sA + kUmABStages * kUmAStage;
-    uint8_t *sR = sB + kUmBStages * kB;
+    uint8_t *sB = sm;
+    uint8_t *sM = sB + kUmBStages * kB;
+    uint8_t *sR = sM + kUmAStages * kUmMTile;
     UmShared *sh = reinterpret_cast<UmShared *>(sR + kUmRawStages * kUmRawStage);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int ntiles = cdiv(N, kUmRows);
     const int my_tiles = blockIdx.x < ntiles ? cdiv(ntiles - (int)blockIdx.x, (int)gridDim.x) : 0;
     const int ngroups = cdiv(my_tiles, kUmGroup);
 
-    // ---- set-up: barriers, the zero k-group of every A stage, TMEM
+    // ---- set-up: barriers, the zero k-group of every m tile, TMEM
     if (threadIdx.x == 0) {
         for (int i = 0; i < kUmRawStages; ++i) {
             mbar_init(&sh->raw_full[i], 1);
-            mbar_init(&sh->raw_empty[i], kUmDeqGroupWarps);
+            mbar_init(&sh->raw_empty[i], 4 * kUmRawSpan);  // 4 warps x kUmRawSpan uses
         }
-        for (int i = 0; i < kUmABStages; ++i) {
-            mbar_init(&sh->ab_full[i], kUmDeqGroupWarps);
+        for (int i = 0; i < kUmAStages; ++i) {
+            mbar_init(&sh->ab_full[i], 4);
             mbar_init(&sh->ab_empty[i], 1);
         }
         for (int i = 0; i < kUmBStages; ++i) {
-            mbar_init(&sh->b_full[i], 1);
-            mbar_init(&sh->b_empty[i], 1);
+            mbar_init(&sh->b_full[i], 1);  // the B warp, once its copies have landed
+            mbar_init(&sh->b_empty[i], kUmGroup);  // one commit per MMA thread
         }
         for (int i = 0; i < 2; ++i) {
-            mbar_init(&sh->acc_full[i], 1);
+            mbar_init(&sh->acc_full[i], kUmGroup);
             mbar_init(&sh->acc_empty[i], kUmEpiWarps);
         }
-        mbar_init(&sh->drain, 1);
+        mbar_init(&sh->drain, kUmGroup);
         sh->abort_flag = 0u;
         fence_mbar_init();
     }
-    for (int i = threadIdx.x; i < kUmABStages * (kUmKgBytes / 16); i += blockDim.x) {
+    for (int i = threadIdx.x; i < kUmAStages * (kUmKgBytes / 16); i += blockDim.x) {
         const int a = i / (kUmKgBytes / 16), j = i % (kUmKgBytes / 16);
-        *reinterpret_cast<uint4 *>(sA + (size_t)a * kUmAStage + 17 * kUmKgBytes + j * 16) = make_uint4(0u, 0u, 0u, 0u);
+        *reinterpret_cast<uint4 *>(sM + (size_t)a * kUmMTile + kUmKgBytes + j * 16) = make_uint4(0u, 0u, 0u, 0u);
     }
     fence_async_smem();
     if (warp == kUmMmaWarp) {
         asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(
                          smem_u32(&sh->tmem_base)),
-                     "r"(kCols)
+                     "r"(kUmCols)
                      : "memory");
         asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;\n" ::: "memory");
     }
@@ -349,9 +395,10 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         if (lane == 0) {
             uint32_t g = 0;
             bool ok = true;
+            const int nsup = cdiv(nst, kUmRawSpan);
             for (int q = 0; ok && q < ngroups; ++q) {
                 const int t0 = q * kUmGroup, tn = min(kUmGroup, my_tiles - t0);
-                for (int s = 0; ok && s < nst; ++s) {
+                for (int S = 0; ok && S < nsup; ++S) {
                     for (int t = 0; t < tn; ++t) {
                         const uint32_t r = g % kUmRawStages;
                         if (!um_wait(&sh->raw_empty[r], ((g / kUmRawStages) & 1u) ^ 1u, abort_flag, status)) {
@@ -359,7 +406,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
                             break;
                         }
                         mbar_arrive_tx(&sh->raw_full[r], kUmRawStage);
-                        tma_load_2d(sR + (size_t)r * kUmRawStage, &wmap, s * kUmRawRow,
+                        tma_load_2d(sR + (size_t)r * kUmRawStage, &wmap, S * kUmRawRow,
                                     ((int)blockIdx.x + (t0 + t) * (int)gridDim.x) * kUmRows, &sh->raw_full[r]);
                         ++g;
                     }
@@ -370,36 +417,57 @@ __global__ void __launch_bounds__(kUmThreads, 1)
                 um_drain(&sh->raw_full[i % kUmRawStages], (i / kUmRawStages) & 1u);
         }
     } else if (warp == kUmBWarp) {
-        // ---- activation stages (written by the prep kernel: after the programmatic wait)
-        if (lane == 0) {
-            pdl_wait();
-            uint32_t g = 0;
-            bool ok = true;
-            for (int q = 0; ok && q < ngroups; ++q) {
-                for (int s = 0; s < nst; ++s) {
-                    const uint32_t b = g % kUmBStages;
-                    if (!um_wait(&sh->b_empty[b], ((g / kUmBStages) & 1u) ^ 1u, abort_flag, status)) {
-                        ok = false;
-                        break;
-                    }
-                    mbar_arrive_tx(&sh->b_full[b], kB);
-                    bulk_load(sB + (size_t)b * kB, bimg + (size_t)s * kB, kB, &sh->b_full[b]);
-                    ++g;
+        // ---- activation stages (written by the prep kernel: after the programmatic wait).
+        // They are small and L2-resident, so they go by cp.async on the load/store path rather
+        // than queueing behind the weight stream's TMA copies.  A stage is signalled once it
+        // has landed, kUmBLag stages behind the newest copy (kUmBLag < kUmBStages, so the MMA
+        // always has the stage it waits for signalled before this warp waits on it in turn).
+        pdl_wait();
+        constexpr int kChunks = kB / 16;
+        uint32_t g = 0, done = 0;
+        bool ok = true;
+        auto signal_oldest = [&](bool all) {
+            if (all)
+                asm volatile("cp.async.wait_group 0;\n" ::: "memory");
+            else
+                asm volatile("cp.async.wait_group %0;\n" ::"n"(kUmBLag) : "memory");
+            fence_async_smem();  // cp.async wrote through the generic proxy; the MMA reads via the async proxy
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sh->b_full[done % kUmBStages]);
+            ++done;
+        };
+        for (int q = 0; ok && q < ngroups; ++q) {
+            for (int s = 0; s < nst; ++s) {
+                const uint32_t b = g % kUmBStages;
+                if (!um_wait_warp(&sh->b_empty[b], ((g / kUmBStages) & 1u) ^ 1u, abort_flag, status)) {
+                    ok = false;
+                    break;
                 }
+                const uint32_t dst = smem_u32(sB + (size_t)b * kB);
+                const uint8_t *src = bimg + (size_t)s * kB;
+                for (int c = lane; c < kChunks; c += 32)
+                    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(dst + 16u * c), "l"(src + 16 * c)
+                                 : "memory");
+                asm volatile("cp.async.commit_group;\n" ::: "memory");
+                ++g;
+                if (g - done > (uint32_t)kUmBLag) signal_oldest(false);
             }
-            for (uint32_t i = g > (uint32_t)kUmBStages ? g - kUmBStages : 0u; i < g; ++i)
-                um_drain(&sh->b_full[i % kUmBStages], (i / kUmBStages) & 1u);
         }
-    } else if (warp == kUmMmaWarp) {
-        // ---- MMA issue (one thread)
+        // every copy issued lands (and is signalled) before the warp leaves
+        while (done < g) signal_oldest(true);
+    } else if (warp >= kUmMmaWarp && warp < kUmMmaWarp + kUmGroup) {
+        // ---- MMA issue: one thread per tile slot of a group (tile t of every group), so
+        // that one thread's commit and barrier round trips overlap the other's issue.  Both
+        // commit every B stage and every group, with or without a tile of their own.
         if (lane == 0) {
+            const int me = warp - kUmMmaWarp;
             constexpr uint32_t idesc = umma_idesc<NPAD>();
             // descriptors of slot 0, k-step 0; a descriptor's low field is the start address
             // / 16 (below 2^14 anywhere in shared memory), so other slots and k-steps are
             // plain additions
-            const uint64_t adesc0 = umma_desc(smem_u32(sA), kUmKgBytes, 128);
             const uint64_t bdesc0 = umma_desc(smem_u32(sB), (NPAD / 8) * 128, 128);
-            constexpr uint64_t kAStep = (2 * kUmKgBytes) >> 4, kBStep = (2 * (NPAD / 8) * 128) >> 4;
+            const uint64_t mdesc0 = umma_desc(smem_u32(sM), kUmKgBytes, 128);
+            constexpr uint64_t kBStep = (2 * (NPAD / 8) * 128) >> 4;
             uint32_t ga = 0, gb = 0;
             bool ok = true;
             for (int q = 0; ok && q < ngroups; ++q) {
@@ -407,28 +475,34 @@ __global__ void __launch_bounds__(kUmThreads, 1)
                 const uint32_t buf = (uint32_t)q & 1u;
                 if (!um_wait(&sh->acc_empty[buf], (((uint32_t)q >> 1) & 1u) ^ 1u, abort_flag, status)) break;
                 tc_fence_after();
-                for (int s = 0; ok && s < nst; ++s, ++gb) {
+                const uint32_t d = tmem + kUmAccBase + (buf * kUmGroup + (uint32_t)me) * kUmAccStride;
+                for (int s = 0; ok && s < nst; ++s, ++gb, ga += (uint32_t)tn) {
+                    // both threads wait for the B stage, a thread without a tile too: its
+                    // release of the B slot must not run ahead of the stage (b_empty counts
+                    // one arrival per thread per stage)
                     const uint32_t b = gb % kUmBStages;
                     if (!um_wait(&sh->b_full[b], (gb / kUmBStages) & 1u, abort_flag, status)) {
                         ok = false;
                         break;
                     }
-                    const uint64_t bd = bdesc0 + (uint64_t)((b * (uint32_t)kB) >> 4);
-                    for (int t = 0; t < tn; ++t, ++ga) {
-                        const uint32_t a = ga % kUmABStages;
-                        if (!um_wait(&sh->ab_full[a], (ga / kUmABStages) & 1u, abort_flag, status)) {
+                    if (me < tn) {
+                        const uint32_t gm = ga + (uint32_t)me;  // this thread's A stage
+                        const uint32_t a = gm % kUmAStages;
+                        if (!um_wait(&sh->ab_full[a], (gm / kUmAStages) & 1u, abort_flag, status)) {
                             ok = false;
                             break;
                         }
                         tc_fence_after();
-                        const uint64_t ad = adesc0 + (uint64_t)((a * (uint32_t)kUmAStage) >> 4);
-                        const uint32_t d = tmem + (buf * kUmGroup + (uint32_t)t) * kStride;
-                        umma_f16(d, ad, bd, idesc, s != 0);
+                        const uint64_t bd = bdesc0 + (uint64_t)((b * (uint32_t)kB) >> 4);
+                        const uint32_t ta = tmem + a * kUmACols;
+                        umma_f16_ts(d, ta, bd, idesc, s != 0);
 #pragma unroll
-                        for (int j = 1; j < kUmMmas; ++j) umma_f16(d, ad + j * kAStep, bd + j * kBStep, idesc, 1u);
+                        for (int j = 1; j < kUmDataMmas; ++j) umma_f16_ts(d, ta + 8 * j, bd + j * kBStep, idesc, 1u);
+                        // the blocks' offsets: m (A, shared memory) x the blocks' activation sums
+                        umma_f16(d, mdesc0 + (uint64_t)((a * (uint32_t)kUmMTile) >> 4), bd + kUmDataMmas * kBStep,
+                                 idesc, 1u);
                         umma_commit(&sh->ab_empty[a]);
                     }
-                    if (!ok) break;
                     umma_commit(&sh->b_empty[b]);
                 }
                 if (!ok) break;
@@ -439,63 +513,65 @@ __global__ void __launch_bounds__(kUmThreads, 1)
             um_drain(&sh->drain, 0u);
         }
     } else if (warp >= kUmDeqWarp0) {
-        // ---- dequant: raw Q2B32 stage -> f16 A stage (+ the m k-group)
-        const int grp = (warp - kUmDeqWarp0) / kUmDeqGroupWarps;
-        const int gw = (warp - kUmDeqWarp0) % kUmDeqGroupWarps;
+        // ---- dequant: thread = one weight row of the stage; A goes to TMEM, m to the m tile
+        const int grp = (warp - kUmDeqWarp0) / 4;
+        const int quarter = warp & 3;  // this warp's TMEM lanes: 32 * quarter ..
+        const int row = 32 * quarter + lane;
         bool bad = false;
-        const uint32_t total = (uint32_t)my_tiles * (uint32_t)nst;
-        for (uint32_t g = (uint32_t)grp; g < total; g += kUmDeqGroups) {
-            const uint32_t r = g % kUmRawStages, a = g % kUmABStages;
-            if (!um_wait_warp(&sh->raw_full[r], (g / kUmRawStages) & 1u, abort_flag, status) ||
-                !um_wait_warp(&sh->ab_empty[a], ((g / kUmABStages) & 1u) ^ 1u, abort_flag, status))
-                break;
-            const uint32_t *raw = reinterpret_cast<const uint32_t *>(sR + (size_t)r * kUmRawStage);
-            uint8_t *A = sA + (size_t)a * kUmAStage;
+        const int nsup = cdiv(nst, kUmRawSpan);
+        uint32_t g = 0, rq = 0;  // A stages so far; raw copies of the groups before q
+        bool ok = true;
+        for (int q = 0; ok && q < ngroups; ++q) {
+            const int tn = min(kUmGroup, my_tiles - q * kUmGroup);
+            for (int s = 0; ok && s < nst; ++s) {
+                for (int t = 0; t < tn; ++t, ++g) {
+                    if ((int)(g % kUmDeqGroups) != grp) continue;
+                    // raw copy of (tile t, stages 4 (s/4) ..): released after its last use
+                    const uint32_t gr = rq + (uint32_t)((s / kUmRawSpan) * tn + t);
+                    const uint32_t r = gr % kUmRawStages, a = g % kUmAStages;
+                    const int first = s - s % kUmRawSpan;
+                    const int uses = min(kUmRawSpan, nst - first);
+                    const uint32_t release = (s == first + uses - 1) ? 1u + (uint32_t)(kUmRawSpan - uses) : 1u;
+                    if (!um_wait_warp(&sh->raw_full[r], (gr / kUmRawStages) & 1u, abort_flag, status) ||
+                        !um_wait_warp(&sh->ab_empty[a], ((g / kUmAStages) & 1u) ^ 1u, abort_flag, status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    // the row's 48 raw bytes of stage s
+                    const uint4 *src = reinterpret_cast<const uint4 *>(sR + (size_t)r * kUmRawStage + row * kUmRawRow +
+                                                                       (s % kUmRawSpan) * kUmStageRaw);
+                    uint32_t raw[12];
 #pragma unroll
-            for (int it = 0; it < kUmItemsPerLane; ++it) {
-                // lane -> (row = 8 consecutive rows, block = lane / 8): the raw words 12 row + 3 block
-                // fall in 32 distinct banks, and each quarter-warp stores one 128-byte run of a
-                // k-group (8 rows x 16 B): no bank conflicts either way
-                const int row = (it * kUmDeqGroupWarps + gw) * 8 + (lane & 7), bl = lane >> 3;
-                const int item = row * kUmBlocks + bl;
-                const uint32_t c0 = raw[3 * item], c1 = raw[3 * item + 1], dm = raw[3 * item + 2];
-                bad |= scale_out_of_range(dm);
-                uint32_t d2, nd;
-                scale_pair(dm, d2, nd);
-                const uint32_t h0 = c0 >> 8, h1 = c1 >> 8;
-                uint32_t w[16];
-                w[0] = dequant_pos<0>(c0, d2, nd);
-                w[1] = dequant_pos<2>(c0, d2, nd);
-                w[2] = dequant_pos<4>(c0, d2, nd);
-                w[3] = dequant_pos<6>(c0, d2, nd);
-                w[4] = dequant_pos<0>(h0, d2, nd);
-                w[5] = dequant_pos<2>(h0, d2, nd);
-                w[6] = dequant_pos<4>(h0, d2, nd);
-                w[7] = dequant_pos<6>(h0, d2, nd);
-                w[8] = dequant_pos<0>(c1, d2, nd);
-                w[9] = dequant_pos<2>(c1, d2, nd);
-                w[10] = dequant_pos<4>(c1, d2, nd);
-                w[11] = dequant_pos<6>(c1, d2, nd);
-                w[12] = dequant_pos<0>(h1, d2, nd);
-                w[13] = dequant_pos<2>(h1, d2, nd);
-                w[14] = dequant_pos<4>(h1, d2, nd);
-                w[15] = dequant_pos<6>(h1, d2, nd);
-                uint8_t *dst = A + (row >> 3) * 128 + (row & 7) * 16;
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    *reinterpret_cast<uint4 *>(dst + (4 * bl + j) * kUmKgBytes) =
-                        make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-                const unsigned short mh = (unsigned short)(dm >> 16);
-                unsigned short *mk = reinterpret_cast<unsigned short *>(dst + 16 * kUmKgBytes);
-                mk[bl] = mh;
-                mk[4 + bl] = mh;
+                    for (int i = 0; i < 3; ++i) {
+                        const uint4 v = src[i];
+                        raw[4 * i] = v.x;
+                        raw[4 * i + 1] = v.y;
+                        raw[4 * i + 2] = v.z;
+                        raw[4 * i + 3] = v.w;
+                    }
+                    const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + a * kUmACols;
+                    uint32_t w[32];
+                    um_decode_blocks(raw, w, bad);
+                    tmem_st32(taddr, w);
+                    um_decode_blocks(raw + 6, w, bad);
+                    tmem_st32(taddr + 32, w);
+                    // m tile, k-group 16: slots 0..3 and 4..7 both hold the 4 blocks' m
+                    const uint32_t m01 = (raw[2] >> 16) | (raw[5] & 0xFFFF0000u);
+                    const uint32_t m23 = (raw[8] >> 16) | (raw[11] & 0xFFFF0000u);
+                    *reinterpret_cast<uint4 *>(sM + (size_t)a * kUmMTile + (row >> 3) * 128 + (row & 7) * 16) =
+                        make_uint4(m01, m23, m01, m23);
+                    tmem_wait_st();
+                    fence_async_smem();
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&sh->ab_full[a]);
+                        mbar_arrive_n(&sh->raw_empty[r], release);
+                    }
+                }
             }
-            fence_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                mbar_arrive(&sh->ab_full[a]);
-                mbar_arrive(&sh->raw_empty[r]);
-            }
+            rq += (uint32_t)(nsup * tn);
         }
         if (bad) set_status(status, Q2_ERR_RANGE);
     } else {
@@ -511,7 +587,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
             tc_fence_after();
             for (int t = 0; t < tn; ++t) {
                 float v[NPAD];
-                const uint32_t col = (buf * kUmGroup + (uint32_t)t) * kStride;
+                const uint32_t col = kUmAccBase + (buf * kUmGroup + (uint32_t)t) * kUmAccStride;
 #pragma unroll
                 for (int c = 0; c < NPAD / 16; ++c)
                     tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + col + (uint32_t)(c * 16), v + 16 * c);
@@ -534,7 +610,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
     if (warp == kUmMmaWarp) {
         __syncwarp();
         tc_fence_after();
-        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kCols) : "memory");
+        asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;\n" ::"r"(tmem), "r"(kUmCols) : "memory");
     }
 }
 
