@@ -151,6 +151,18 @@ def run_device(args, rank: int, world: int):
             a = a.view(np.int16)
         return torch.from_numpy(a).to(dev)
 
+    if args.profile_cohort:
+        # eager calls of the M=60 vocabulary-head GEMM (tcgen05 path), for an ncu capture
+        gc = synth.config_gemm(4)
+        Wc, Ac = D(gc["W"].reshape(-1)), D(gc["A"])
+        Yc = torch.empty((gc["M"], gc["N"]), dtype=torch.float32, device=dev)
+        wsc = q2v.workspace(q2v.q2_tiny_gemm_workspace(gc["M"], gc["N"], gc["K"]), dev)
+        for _ in range(args.warmup + args.steps):
+            q2v.q2_tiny_gemm(Wc, gc["N"], gc["K"], Ac, Y=Yc, ws=wsc)
+        torch.cuda.synchronize()
+        assert q2v.q2_get_device_status(wsc) == 0
+        return None
+
     # resident inputs, N_SETS rotating sets
     sets = []
     for i in range(N_SETS):
@@ -295,6 +307,88 @@ def run_device(args, rank: int, world: int):
     moe_us, _ = timed(capture(part_moe), args.steps, args.warmup)
     pq_us, _ = timed(capture(part_pq), args.steps, args.warmup)
 
+    def graph_us(fn, reps):
+        """Mean µs of fn() replayed from one CUDA graph (3 warm-up replays first)."""
+        fn()
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        side = torch.cuda.Stream(device=dev)
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            fn()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        with torch.cuda.graph(gr):
+            fn()
+        for _ in range(3):
+            gr.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            gr.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / reps * 1000.0
+
+    peak_x, _ = _peaks()
+    lin_bytes = sh["N"] * (sh["K"] // 32) * 12 + sh["M"] * sh["K"] * 2 + sh["M"] * sh["N"] * 4
+
+    # the verifier-layer shape: 8 distinct 4096 x 4096 Q2B32 linears back to back (PDL, the
+    # weight stream of each starting before its activation prep is done), 4 rotating layer
+    # sets (200 MB, larger than L2)
+    chain = None
+    if not args.no_extras:
+        layers = [[D(synth.q2b32_weights(synth.Streams(9000 + 8 * j + i), sh["N"], sh["K"]).reshape(-1))
+                   for i in range(8)] for j in range(N_SETS)]
+        Yc = torch.empty((sh["M"], sh["N"]), dtype=torch.float32, device=dev)
+        wsc = q2v.workspace(q2v.q2_tiny_gemm_workspace(sh["M"], sh["N"], sh["K"]), dev)
+
+        def chain_all():
+            for j in range(N_SETS):
+                for Wl in layers[j]:
+                    q2v.q2_tiny_gemm(Wl, sh["N"], sh["K"], sets[0]["A"], Y=Yc, ws=wsc)
+
+        c_us = graph_us(chain_all, max(3, args.steps // 4)) / N_SETS
+        chain = {"layers": 8, "us_per_8": c_us, "us_per_linear": c_us / 8,
+                 "GB/s": 8 * lin_bytes / (c_us * 1e-6) / 1e9, "frac": 8 * lin_bytes / (c_us * 1e-6) / 1e9 / peak_x}
+        del layers
+
+    # the cohort verify: 12 sessions x 5 rows = M=60 against a 129,280 x 4096 Q2B32 vocabulary
+    # head on the tcgen05 path, then pq_verify (S=12, k=4) over those logits
+    cohort = None
+    if not args.no_extras:
+        gc = synth.config_gemm(4)
+        Wc, Ac = D(gc["W"].reshape(-1)), D(gc["A"])
+        Mc, Nc, Kc = gc["M"], gc["N"], gc["K"]
+        Yco = torch.empty((Mc, Nc), dtype=torch.float32, device=dev)
+        wsg = q2v.workspace(q2v.q2_tiny_gemm_workspace(Mc, Nc, Kc), dev)
+        vc = synth.verify_inputs(synth.streams(4, salt=1), 12, 4, Nc, 0.0, 1.0, 1.0,
+                                 target=np.zeros((12, 5, Nc), np.float32))
+        Dc, xc, uac, ufc = D(vc["draft"]), D(vc["drafts"]), D(vc["u_acc"]), D(vc["u_fin"])
+        nc = torch.empty(12, dtype=torch.int32, device=dev)
+        tc = torch.empty((12, 5), dtype=torch.int32, device=dev)
+        wsv = q2v.workspace(q2v.pq_verify_workspace(12, 4, Nc), dev)
+
+        def c_gemm():
+            q2v.q2_tiny_gemm(Wc, Nc, Kc, Ac, Y=Yco, ws=wsg)
+
+        def c_pq():
+            q2v.pq_verify(Yco.view(12, 5, Nc), Dc, xc, uac, ufc, 1.0, n_acc=nc, tokens=tc, ws=wsv)
+
+        def c_both():
+            c_gemm()
+            c_pq()
+
+        g_us, p_us, b_us = (graph_us(f, max(5, args.steps // 2)) for f in (c_gemm, c_pq, c_both))
+        wbytes = Nc * (Kc // 32) * 12
+        cohort = {"workload": "M=60 x N=129280 x K=4096 Q2B32 GEMM (tcgen05) + pq_verify S=12 k=4 V=129280",
+                  "gemm_us": g_us, "pq_verify_us": p_us, "gemm_plus_verify_us": b_us,
+                  "gemm_GB/s": (wbytes + Mc * Kc * 2 + Mc * Nc * 4) / (g_us * 1e-6) / 1e9,
+                  "gemm_TFLOP/s": 2.0 * Mc * Nc * Kc / (g_us * 1e-6) / 1e12,
+                  "gemm_frac_hbm": (wbytes + Mc * Kc * 2 + Mc * Nc * 4) / (g_us * 1e-6) / 1e9 / peak_x}
+        del Wc
+
     # e2e: through the binding, pinned host inputs in, results out, every step
     pin = []
     for s in sets:
@@ -392,6 +486,8 @@ def run_device(args, rank: int, world: int):
                      "algorithmic_bytes_per_launch": dom["bytes"], "us_per_launch": dom["us"]},
         "e2e": {"value": e2e_us, "unit": "µs", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "chained_linears_m5": chain,
+        "cohort_m60": cohort,
         "clocks": clocks,
     }
     return line
@@ -441,6 +537,10 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-cohort", action="store_true",
+                    help="eager calls of the M=60 x 129280 x 4096 GEMM only (for ncu); prints nothing")
+    ap.add_argument("--no-extras", action="store_true",
+                    help="skip the chained-linear and cohort (M=60) measurements")
     ap.add_argument("--profile", action="store_true",
                     help="run warmup+steps eager steps only (for an ncu launch list); prints nothing")
     args = ap.parse_args()
