@@ -62,7 +62,7 @@ typedef enum {
     Q2_ERR_CUDA = 5,        /* a CUDA runtime call (launch, attribute, copy) failed        */
     Q2_ERR_TIMEOUT = 6,     /* a bounded device-side wait gave up                          */
     Q2_ERR_BAD_TOKEN = 7,   /* device: a draft token is outside [0, V)                     */
-    Q2_ERR_RANGE = 8        /* device: a Q2B32 scale |d| >= 64 (outside the exact path)    */
+    Q2_ERR_RANGE = 8        /* device: a Q2B32 scale |d| >= 64 or infinite (outside the exact path) */
 } q2_status;
 
 #define Q2_WORKSPACE_HEADER_BYTES 256
@@ -90,7 +90,8 @@ size_t q2_tiny_gemm_workspace(int M, int N, int K);
  * exactly, and activations converted to fp16 under an exact per-row power-of-two scale, so
  * |Y - exact| stays far below 2e-3 * sum_k |a_k w_k|.  Scales must satisfy |d| < 64 (real
  * 2-bit block scales are orders of magnitude smaller).
- * Device errors: Q2_ERR_RANGE if a block has a finite |d| >= 64.
+ * Device errors: Q2_ERR_RANGE if a block has |d| >= 64 (infinity included; a NaN scale is not
+ * flagged and propagates to the outputs it touches).
  */
 q2_status q2_tiny_gemm(const void *W, int N, int K, const uint16_t *A, int M, int lda,
                        float *Y, int ldy, void *ws, size_t ws_bytes, q2_stream_t stream);
@@ -158,8 +159,9 @@ size_t pq_verify_workspace(int S, int k, int V);
  *   n_accepted    int32 [S]: j, in [0, k].
  *   out_tokens    int32 [S][k+1]: x_0..x_{j-1}, y, then -1.
  *   probs_out     optional fp32 [S][2k+1][V]: rows p_0..p_k then q_0..q_{k-1} (for tests).
- * Arithmetic is fp32 with fp64 cross-chunk sums; tokens equal the exact (fp64) result
- * except when a uniform lies within about 1e-6 of a decision boundary.
+ * Arithmetic is fp32, with compensated (two-sum) fp32 cross-chunk and cross-segment sums;
+ * tokens equal the exact (fp64) result except when a uniform lies within about 1e-6 of a
+ * decision boundary.
  */
 q2_status pq_verify(const float *target_logits, const float *draft_logits,
                     const int32_t *draft_tokens, const float *u_acc, const float *u_fin,

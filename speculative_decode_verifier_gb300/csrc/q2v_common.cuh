@@ -121,13 +121,11 @@ __device__ __forceinline__ uint32_t dequant_pos(uint32_t v, uint32_t d2, uint32_
     return r;
 }
 
-// f16x2 {d, d} and {-1024 d, -1024 d} from a block's packed (d | m << 16) word.
+// f16x2 {d, d} and {-1024 d, -1024 d} from a block's packed (d | m << 16) word: one byte
+// permute and one f16x2 multiply (-1024 = 0xE400).
 __device__ __forceinline__ void scale_pair(uint32_t dm, uint32_t &d2, uint32_t &nd1024) {
-    const uint32_t d = dm & 0xFFFFu;
-    d2 = d | (d << 16);
-    const __half nd = __hmul(__ushort_as_half((unsigned short)d), __ushort_as_half((unsigned short)0xE400u));  // * -1024
-    const uint32_t n = __half_as_ushort(nd);
-    nd1024 = n | (n << 16);
+    d2 = prmt(dm, dm, 0x1010u);
+    asm("mul.rn.f16x2 %0, %1, %2;\n" : "=r"(nd1024) : "r"(d2), "r"(0xE400E400u));
 }
 
 // Division by a run-time constant d >= 1 for 0 <= u < 2^31 (round-up multiply-shift:
@@ -143,10 +141,16 @@ struct FastDiv {
     __device__ __forceinline__ uint32_t div(uint32_t u) const { return (__umulhi(u, m) + u) >> s; }
 };
 
-// |d| >= 64 (finite) is outside the exact range of dequant_pos: flag it.
-__device__ __forceinline__ bool scale_out_of_range(uint32_t dm) {
-    const uint32_t mag = dm & 0x7FFFu;
-    return mag >= 0x5400u && mag < 0x7C00u;  // 0x5400 = 64.0; >= 0x7C00 is inf/nan (propagates)
+// Range of the scales.  dequant_pos is exact for |d| < 64 (-1024 d must be a finite f16).
+// Kernels keep a running f16x2 maximum of |d|, |m| over the blocks they decode (two
+// instructions per block; a NaN scale is skipped by the maximum and propagates to the
+// outputs instead) and flag Q2_ERR_RANGE at the end if the |d| half reached 64 (0x5400),
+// infinity included.
+__device__ __forceinline__ uint32_t scale_mag_max(uint32_t acc, uint32_t dm) {
+    uint32_t r;
+    asm("max.f16x2 %0, %1, %2;\n" : "=r"(r) : "r"(dm & 0x7FFF7FFFu), "r"(acc));
+    return r;
 }
+__device__ __forceinline__ bool scale_mag_out_of_range(uint32_t acc) { return (acc & 0xFFFFu) >= 0x5400u; }
 
 }  // namespace q2v

@@ -86,7 +86,7 @@ __global__ void __launch_bounds__(kGemmWarps * 32) q2_gemm_mma_kernel(const uint
     pdl_wait();
     pdl_trigger();
     const SmemAct SA(L, ncols);
-    bool range_bad = false;
+    uint32_t scale_max = 0u;  // running max of |d|, |m| (f16x2)
     for (int m0 = 0; m0 < M; m0 += 8) {
         const int mc = min(8, M - m0);
         if (threadIdx.x < 8) s_rows[threadIdx.x] = m0 + threadIdx.x;
@@ -102,7 +102,7 @@ __global__ void __launch_bounds__(kGemmWarps * 32) q2_gemm_mma_kernel(const uint
 #pragma unroll
                 for (int q = 0; q < 12; ++q)
                     (&cur.w[0][0][0])[q] = i ? (&wr1.w[0][0][0])[q] : (&wr0.w[0][0][0])[q];
-                compute_tile_smem(cur, sm_act, SA, mc, tile, lane, acc, range_bad);
+                compute_tile_smem(cur, sm_act, SA, mc, tile, lane, acc, scale_max);
             }
         }
         store_fragments(red + warp * kRowsPerCta * 8, acc, lane);
@@ -115,7 +115,7 @@ __global__ void __launch_bounds__(kGemmWarps * 32) q2_gemm_mma_kernel(const uint
         }
         __syncthreads();
     }
-    if (range_bad) set_status(status, Q2_ERR_RANGE);
+    if (scale_mag_out_of_range(scale_max)) set_status(status, Q2_ERR_RANGE);
 }
 
 namespace {

@@ -177,20 +177,22 @@ __device__ __forceinline__ void read_tile_smem(TileRegs &r, const uint32_t *stag
 //
 // Staged activations for up to `ncols` columns.  An MMA column without a row in the current
 // slice reads column 0: it only feeds its own output column, which is never stored (each
-// output of an MMA is one row of A times one column of B).  Column c holds its blocks in pairs: block
-// pair j = b/2 starts at word 34*j (32 words of data and 2 of skew), block b at
-// 34*(b/2) + 16*(b%2), pair slot p at + p.  A k16 step's 8-byte fragment load has threads
-// g = 0..7 on columns CS*g apart (CS == 8 mod 32) and t = 0..3 on block pairs 34 words
-// (2 banks) apart, so the warp's 64 words cover all 32 banks twice: two wavefronts, the
-// minimum for 256 bytes.  Each thread's base address is fixed for a tile; every step's
-// offset is a compile-time constant.  Block sums follow: shi/slo[c][SWW] words,
-// SWW == 4 (mod 32), word j = f16x2 (S[2j], S[2j+1]).
-constexpr int kPairWords = 34;
+// output of an MMA is one row of A times one column of B).  Column c holds its blocks in
+// pairs: block pair j = b/2 starts at word 36*j (32 words of data and 4 of skew).  Inside a
+// pair the 8-byte B fragments of the two blocks are interleaved: fragment u = 4w + pp of block
+// b%2 (k16 step w, slot pair pp) sits at word 4u + 2(b%2), so one 16-byte load brings the
+// fragments of both blocks for one step.  A warp's 16-byte load has threads g = 0..7 on
+// columns CS*g apart (CS == 16 mod 32) and t = 0..3 on block pairs 36 words (4 banks) apart:
+// each quarter-warp covers the 32 banks once, so 4 wavefronts, the minimum for 512 bytes.
+// Each thread's base address is fixed for a tile; every step's offset is a compile-time
+// constant.  Block sums follow: shi/slo[c][SWW] words, SWW == 4 (mod 32), word j = f16x2
+// (S[2j], S[2j+1]).
+constexpr int kPairWords = 36;
 
 struct SmemAct {
     int CS, SWW, ncols;
     __host__ __device__ SmemAct(const PrepLayout &L, int ncols_)
-        : CS((int)align_up((size_t)L.nbp / 2 * kPairWords, 32) + 8),
+        : CS((int)align_up((size_t)L.nbp / 2 * kPairWords, 32) + 16),
           SWW((int)align_up((size_t)L.nbp / 2, 32) + 4),
           ncols(ncols_) {}
     __host__ __device__ size_t words() const { return (size_t)ncols * (CS + 2 * SWW); }
@@ -210,9 +212,10 @@ __device__ __forceinline__ void stage_act_issue(uint32_t *sm, const SmemAct &SA,
         const int c = (int)div16.div((uint32_t)j), q = j - c * n16;
         const int b = q >> 2, grp = q & 3;
         const uint32_t *src = P.act + (size_t)rows[c] * L.act_words_per_row() + (size_t)q * 4;
-        uint32_t *dst = SA.act(sm, c) + (b >> 1) * kPairWords + (b & 1) * 16 + 4 * grp;
+        // fragments 2 grp and 2 grp + 1 of block b
+        uint32_t *dst = SA.act(sm, c) + (b >> 1) * kPairWords + 8 * grp + 2 * (b & 1);
         cp_async8(dst, src);
-        cp_async8(dst + 2, src + 2);
+        cp_async8(dst + 4, src + 2);
     }
     const int nw = L.nbp / 2;
     const FastDiv divw((uint32_t)nw);
@@ -237,7 +240,7 @@ __device__ __forceinline__ void stage_act(uint32_t *sm, const SmemAct &SA, const
 // independent MMA chains, issued alternately.  B fragments come from the staged operand,
 // column g (column 0 when g has no row in the current slice of n columns; see SmemAct).
 __device__ __forceinline__ void compute_tile_smem(const TileRegs &r, uint32_t *sm, const SmemAct &SA, int n,
-                                                  int tile, int lane, float (&acc)[2][4], bool &range_bad) {
+                                                  int tile, int lane, float (&acc)[2][4], uint32_t &scale_max) {
     const int g = lane >> 2, t = lane & 3;
     const int cg = g < n ? g : 0;
     const uint32_t *base = SA.act(sm, cg) + (tile * 4 + t) * kPairWords;  // block pair (2t, 2t+1)
@@ -246,15 +249,17 @@ __device__ __forceinline__ void compute_tile_smem(const TileRegs &r, uint32_t *s
     for (int bi = 0; bi < 2; ++bi) {
         scale_pair(r.w[0][bi][2], d2[bi][0], nd[bi][0]);
         scale_pair(r.w[1][bi][2], d2[bi][1], nd[bi][1]);
-        range_bad |= scale_out_of_range(r.w[0][bi][2]) | scale_out_of_range(r.w[1][bi][2]);
+        scale_max = scale_mag_max(scale_max, r.w[0][bi][2]);
+        scale_max = scale_mag_max(scale_max, r.w[1][bi][2]);
     }
 #pragma unroll
     for (int w = 0; w < 2; ++w) {
 #pragma unroll
         for (int pp = 0; pp < 4; ++pp) {
+            // the step's B fragments of both blocks of the pair
+            const uint4 bb = *reinterpret_cast<const uint4 *>(base + 4 * (4 * w + pp));
 #pragma unroll
             for (int bi = 0; bi < 2; ++bi) {
-                const uint2 bb = *reinterpret_cast<const uint2 *>(base + bi * 16 + 8 * w + 2 * pp);
                 const uint32_t c0 = r.w[0][bi][w], c1 = r.w[1][bi][w];
                 const uint32_t va = pp < 2 ? c0 : (c0 >> 8), vb = pp < 2 ? c1 : (c1 >> 8);
                 uint32_t a0, a1, a2, a3;
@@ -269,7 +274,7 @@ __device__ __forceinline__ void compute_tile_smem(const TileRegs &r, uint32_t *s
                     a1 = dequant_pos<0>(vb, d2[bi][1], nd[bi][1]);
                     a3 = dequant_pos<2>(vb, d2[bi][1], nd[bi][1]);
                 }
-                mma_16816(acc[bi], a0, a1, a2, a3, bb.x, bb.y);
+                mma_16816(acc[bi], a0, a1, a2, a3, bi ? bb.z : bb.x, bi ? bb.w : bb.y);
             }
         }
     }

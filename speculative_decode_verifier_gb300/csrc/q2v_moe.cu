@@ -246,7 +246,7 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
     const int mats = GATEUP ? 2 : 1;
     // the ring path: whole 16-row groups, whole tiles, 16-byte aligned rows
     const bool ring_path = (um.Nrows % kRowsPerCta) == 0 && L.nb == L.ntk * kTileBlocks && (L.nb % 4) == 0;
-    bool range_bad = false;
+    uint32_t scale_max = 0u;  // running max of |d|, |m| (f16x2)
 
     for (int seg0 = i0; seg0 < i1;) {
         // the run of units of one expert
@@ -319,7 +319,7 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
                     __syncwarp();
                     TileRegs cur;
                     read_tile_smem(cur, ring + (it % kRingStages) * kTileWords, lane);
-                    compute_tile_smem(cur, sm_act, SA, mc, ctile, lane, acc, range_bad);
+                    compute_tile_smem(cur, sm_act, SA, mc, ctile, lane, acc, scale_max);
                     if (++ctile >= cui.t1) {
                         store_unit(cui, acc);
                         cu += nwarps;
@@ -340,7 +340,7 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
                     for (int tile = ui.t0; tile < ui.t1; ++tile) {
                         TileRegs b0;
                         load_tile<ALIGN8>(b0, ui.W0, um.row_bytes, ui.rows_valid, L.nb, tile, lane);
-                        compute_tile_smem(b0, sm_act, SA, mc, tile, lane, acc, range_bad);
+                        compute_tile_smem(b0, sm_act, SA, mc, tile, lane, acc, scale_max);
                     }
                     store_unit(ui, acc);
                 }
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
         }
         seg0 = seg1;
     }
-    if (range_bad) set_status(a.status, Q2_ERR_RANGE);
+    if (scale_mag_out_of_range(scale_max)) set_status(a.status, Q2_ERR_RANGE);
 }
 
 __global__ void __launch_bounds__(256) moe_combine_kernel(MoeArgs a, MoeWs w, int KS) {

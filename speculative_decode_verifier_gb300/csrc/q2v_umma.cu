@@ -301,11 +301,11 @@ __global__ void __launch_bounds__(256) prep_umma_kernel(const uint16_t *__restri
 
 // Decode one weight row of a stage (4 Q2B32 blocks = 48 raw bytes) into 64 f16x2 words, word
 // 16*b + p = pair slot p of block b (the order prep_store_block gives the activations).
-__device__ __forceinline__ void um_decode_blocks(const uint32_t *raw, uint32_t *w, bool &bad) {
+__device__ __forceinline__ void um_decode_blocks(const uint32_t *raw, uint32_t *w, uint32_t &scale_max) {
 #pragma unroll
     for (int b = 0; b < 2; ++b) {
         const uint32_t c0 = raw[3 * b], c1 = raw[3 * b + 1], dm = raw[3 * b + 2];
-        bad |= scale_out_of_range(dm);
+        scale_max = scale_mag_max(scale_max, dm);
         uint32_t d2, nd;
         scale_pair(dm, d2, nd);
         const uint32_t h0 = c0 >> 8, h1 = c1 >> 8;
@@ -517,7 +517,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         const int grp = (warp - kUmDeqWarp0) / 4;
         const int quarter = warp & 3;  // this warp's TMEM lanes: 32 * quarter ..
         const int row = 32 * quarter + lane;
-        bool bad = false;
+        uint32_t scale_max = 0u;  // running max of |d|, |m| (f16x2)
         const int nsup = cdiv(nst, kUmRawSpan);
         uint32_t g = 0, rq = 0;  // A stages so far; raw copies of the groups before q
         bool ok = true;
@@ -552,9 +552,9 @@ __global__ void __launch_bounds__(kUmThreads, 1)
                     }
                     const uint32_t taddr = tmem + ((uint32_t)(32 * quarter) << 16) + a * kUmACols;
                     uint32_t w[32];
-                    um_decode_blocks(raw, w, bad);
+                    um_decode_blocks(raw, w, scale_max);
                     tmem_st32(taddr, w);
-                    um_decode_blocks(raw + 6, w, bad);
+                    um_decode_blocks(raw + 6, w, scale_max);
                     tmem_st32(taddr + 32, w);
                     // m tile, k-group 16: slots 0..3 and 4..7 both hold the 4 blocks' m
                     const uint32_t m01 = (raw[2] >> 16) | (raw[5] & 0xFFFF0000u);
@@ -573,7 +573,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
             }
             rq += (uint32_t)(nsup * tn);
         }
-        if (bad) set_status(status, Q2_ERR_RANGE);
+        if (scale_mag_out_of_range(scale_max)) set_status(status, Q2_ERR_RANGE);
     } else {
         // ---- epilogue: TMEM -> registers -> Y (warp w reads TMEM lanes 32w..32w+31)
         pdl_wait();
