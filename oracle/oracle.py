@@ -56,6 +56,9 @@ def _load():
         lib.orc_pq_verify.argtypes = [P, P, P, P, P, i32, i32, i32, f64,
                                       P, P, P, P, P, P, P, i32]
         lib.orc_pq_verify.restype = i32
+        lib.orc_pq_verify_ex.argtypes = [P, P, P, P, P, i32, i32, i32, f64, P,
+                                         P, P, P, P, P, P, P, i32]
+        lib.orc_pq_verify_ex.restype = i32
         lib.orc_moe.argtypes = [P, P, P, i32, i32, i32, i32, i32, P, i32, P, P, P, P, P, i32]
         lib.orc_version.restype = i32
         _lib = lib
@@ -124,9 +127,10 @@ def inverse_cdf(w: np.ndarray, u: float):
 
 
 def pq_verify(target, draft, drafts, u_acc, u_fin, T: float, want_probs: bool = False,
-              threads: int | None = None) -> dict:
+              threads: int | None = None, temps=None) -> dict:
     """The p/q verify for S sessions.  target [S,k+1,V] fp32, draft [S,k,V] fp32,
-    drafts [S,k] int32, u_acc [S,k] fp32, u_fin [S] fp32."""
+    drafts [S,k] int32, u_acc [S,k] fp32, u_fin [S] fp32.  temps: optional [S] per-session
+    temperatures (0 = the greedy verify); T is used for every session when it is None."""
     target = _c(target, np.float32)
     S, k1, V = target.shape
     k = k1 - 1
@@ -141,12 +145,13 @@ def pq_verify(target, draft, drafts, u_acc, u_fin, T: float, want_probs: bool = 
     lo = np.empty(S, np.float64)
     hi = np.empty(S, np.float64)
     src = np.empty(S, np.int32)
-    bad = _load().orc_pq_verify(_ptr(target), _ptr(draft), _ptr(drafts), _ptr(u_acc), _ptr(u_fin),
-                                S, k, V, float(T), _ptr(n_acc), _ptr(tokens), _ptr(probs),
-                                _ptr(ratio), _ptr(lo), _ptr(hi), _ptr(src),
-                                threads or default_threads())
+    tv = None if temps is None else _c(temps, np.float64).reshape(S)
+    bad = _load().orc_pq_verify_ex(_ptr(target), _ptr(draft), _ptr(drafts), _ptr(u_acc), _ptr(u_fin),
+                                   S, k, V, float(T), _ptr(tv), _ptr(n_acc), _ptr(tokens), _ptr(probs),
+                                   _ptr(ratio), _ptr(lo), _ptr(hi), _ptr(src),
+                                   threads or default_threads())
     return dict(n_acc=n_acc, tokens=tokens, probs=probs, ratio=ratio, cell_lo=lo, cell_hi=hi,
-                fin_src=src, bad_token=bool(bad))
+                fin_src=src, bad_token=bool(bad & 1), bad_temperature=bool(bad & 2))
 
 
 def moe(Wg, Wu, Wd, E: int, H: int, F: int, topk: int, X_bits, router, renorm: bool = False,

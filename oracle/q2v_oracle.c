@@ -195,10 +195,54 @@ int orc_inverse_cdf(const double *w, int V, double u, double *cell_lo, double *c
  *   fin_src [S]: 0 = residual, 1 = bonus from p_k, 2 = residual mass zero, drawn from p_j.
  * Returns 0, or 1 if a draft token lies outside [0, V) (that session's outputs are -1).
  */
-int orc_pq_verify(const float *target, const float *draft, const int32_t *drafts,
-                  const float *u_acc, const float *u_fin, int S, int k, int V, double T,
-                  int32_t *n_acc, int32_t *tokens, double *probs, double *ratio,
-                  double *cell_lo, double *cell_hi, int32_t *fin_src, int nthreads)
+/* Lowest index of the largest value of x[0..V) (the greedy choice; ties go to the lower
+ * token, the plainest deterministic reading). */
+static int orc_argmax(const float *x, int V)
+{
+    int best = 0;
+    for (int y = 1; y < V; ++y)
+        if (x[y] > x[best]) best = y;
+    return best;
+}
+
+/*
+ * The greedy verify of session s (temperature 0): p_i and q_i become one-hot at the
+ * argmax of their logits, so a draft is accepted iff it equals argmax t_i, and the token
+ * after the first rejection j (or the bonus, j = k) is argmax t_j.  Neither the draft
+ * logits' values beyond their argmax nor the uniforms are used.
+ */
+static void orc_verify_greedy(const float *ts, const float *ds, const int32_t *xs, int k, int V,
+                              int32_t *n_acc, int32_t *tok, double *ps, double *ratio,
+                              double *cell_lo, double *cell_hi, int32_t *fin_src)
+{
+    if (ps) {
+        for (size_t e = 0; e < (size_t)(2 * k + 1) * V; ++e) ps[e] = 0.0;
+        for (int i = 0; i <= k; ++i) ps[(size_t)i * V + orc_argmax(ts + (size_t)i * V, V)] = 1.0;
+        for (int i = 0; i < k; ++i) ps[(size_t)(k + 1 + i) * V + orc_argmax(ds + (size_t)i * V, V)] = 1.0;
+    }
+    int j = k;
+    for (int i = 0; i < k; ++i) {
+        const int am = orc_argmax(ts + (size_t)i * V, V);
+        if (ratio) ratio[i] = (xs[i] == am) ? INFINITY : 0.0;
+        if (xs[i] != am) { j = i; break; }
+    }
+    for (int i = 0; i < j; ++i) tok[i] = xs[i];
+    tok[j] = orc_argmax(ts + (size_t)j * V, V);
+    *n_acc = j;
+    if (cell_lo) *cell_lo = NAN;
+    if (cell_hi) *cell_hi = NAN;
+    if (fin_src) *fin_src = 3;
+}
+
+/*
+ * orc_pq_verify with one temperature per session: temps[s] (NULL: T for every session).
+ * temps[s] = 0 selects the greedy verify for that session; a negative or non-finite
+ * temperature marks the session bad (n_acc -1, tokens -1) and sets bit 2 of the return.
+ */
+int orc_pq_verify_ex(const float *target, const float *draft, const int32_t *drafts,
+                     const float *u_acc, const float *u_fin, int S, int k, int V, double T,
+                     const double *temps, int32_t *n_acc, int32_t *tokens, double *probs,
+                     double *ratio, double *cell_lo, double *cell_hi, int32_t *fin_src, int nthreads)
 {
     int bad = 0;
     if (nthreads < 1) nthreads = 1;
@@ -211,27 +255,42 @@ int orc_pq_verify(const float *target, const float *draft, const int32_t *drafts
         for (int s = 0; s < S; ++s) {
             const float *ts = target + (size_t)s * (k + 1) * V;
             const float *ds = draft + (size_t)s * k * V;
-            for (int i = 0; i <= k; ++i) orc_softmax(ts + (size_t)i * V, V, T, p + (size_t)i * V);
-            for (int i = 0; i < k; ++i) orc_softmax(ds + (size_t)i * V, V, T, q + (size_t)i * V);
+            const double Ts = temps ? temps[s] : T;
+            for (int i = 0; i <= k; ++i) tokens[(size_t)s * (k + 1) + i] = -1;
+            if (ratio)
+                for (int i = 0; i < k; ++i) ratio[(size_t)s * k + i] = NAN;
+            if (!(Ts >= 0.0) || !isfinite(Ts)) {
+                bad |= 2;
+                n_acc[s] = -1;
+                if (fin_src) fin_src[s] = -1;
+                continue;
+            }
+            {
+                int token_ok = 1;
+                for (int i = 0; i < k; ++i) {
+                    int32_t x = drafts[(size_t)s * k + i];
+                    if (x < 0 || x >= V) token_ok = 0;
+                }
+                if (!token_ok) {
+                    bad |= 1;
+                    n_acc[s] = -1;
+                    if (fin_src) fin_src[s] = -1;
+                    continue;
+                }
+            }
+            if (Ts == 0.0) {
+                orc_verify_greedy(ts, ds, drafts + (size_t)s * k, k, V, n_acc + s, tokens + (size_t)s * (k + 1),
+                                  probs ? probs + (size_t)s * (2 * k + 1) * V : NULL,
+                                  ratio ? ratio + (size_t)s * k : NULL, cell_lo ? cell_lo + s : NULL,
+                                  cell_hi ? cell_hi + s : NULL, fin_src ? fin_src + s : NULL);
+                continue;
+            }
+            for (int i = 0; i <= k; ++i) orc_softmax(ts + (size_t)i * V, V, Ts, p + (size_t)i * V);
+            for (int i = 0; i < k; ++i) orc_softmax(ds + (size_t)i * V, V, Ts, q + (size_t)i * V);
             if (probs) {
                 double *ps = probs + (size_t)s * (2 * k + 1) * V;
                 memcpy(ps, p, sizeof(double) * (size_t)V * (k + 1));
                 if (k > 0) memcpy(ps + (size_t)(k + 1) * V, q, sizeof(double) * (size_t)V * k);
-            }
-            for (int i = 0; i <= k; ++i) tokens[(size_t)s * (k + 1) + i] = -1;
-            if (ratio)
-                for (int i = 0; i < k; ++i) ratio[(size_t)s * k + i] = NAN;
-
-            int token_ok = 1;
-            for (int i = 0; i < k; ++i) {
-                int32_t x = drafts[(size_t)s * k + i];
-                if (x < 0 || x >= V) token_ok = 0;
-            }
-            if (!token_ok) {
-                bad = 1;
-                n_acc[s] = -1;
-                if (fin_src) fin_src[s] = -1;
-                continue;
             }
 
             int j = k;
@@ -275,6 +334,15 @@ int orc_pq_verify(const float *target, const float *draft, const int32_t *drafts
         free(w);
     }
     return bad;
+}
+
+int orc_pq_verify(const float *target, const float *draft, const int32_t *drafts,
+                  const float *u_acc, const float *u_fin, int S, int k, int V, double T,
+                  int32_t *n_acc, int32_t *tokens, double *probs, double *ratio,
+                  double *cell_lo, double *cell_hi, int32_t *fin_src, int nthreads)
+{
+    return orc_pq_verify_ex(target, draft, drafts, u_acc, u_fin, S, k, V, T, NULL, n_acc, tokens, probs,
+                            ratio, cell_lo, cell_hi, fin_src, nthreads) & 1;
 }
 
 /* ------------------------------------------------------------------ routed MoE */

@@ -473,3 +473,82 @@ def test_pq_verify_strict_comparison_at_zero_ratio(orc):
     out = orc.pq_verify(tl, dl, np.array([[2]], np.int32), np.array([[0.0]], np.float32),
                         np.array([0.25], np.float32), 1.0)
     assert out["n_acc"][0] == 0 and out["tokens"][0, 0] != 2
+
+
+# ---------------------------------------------------------------- greedy and per-session T
+
+def _greedy_case(seed, S=6, k=4, V=40):
+    """Logits on a 0.5 grid (distinct values, gaps >= 0.5) and drafts that are the argmax of
+    their draft logits, which agree with the target argmax for a random prefix."""
+    rng = np.random.default_rng(seed)
+    t = np.stack([np.stack([rng.permutation(V) * 0.5 for _ in range(k + 1)]) for _ in range(S)]).astype(np.float32)
+    d = np.stack([np.stack([rng.permutation(V) * 0.5 for _ in range(k)]) for _ in range(S)]).astype(np.float32)
+    for s in range(S):
+        agree = rng.integers(0, k + 1)
+        for i in range(agree):
+            d[s, i] = t[s, i]
+    x = np.argmax(d, axis=2).astype(np.int32)
+    ua = rng.random((S, k)).astype(np.float32)
+    uf = rng.random(S).astype(np.float32)
+    return t, d, x, ua, uf
+
+
+def test_greedy_is_the_zero_temperature_limit(orc):
+    """At T = 1e-4 every softmax of these logits is exactly one-hot in fp64 (the next value is
+    5000 nats down), so the sampling verify must emit the greedy verify's tokens."""
+    for seed in range(5):
+        t, d, x, ua, uf = _greedy_case(seed)
+        S = t.shape[0]
+        g = orc.pq_verify(t, d, x, ua, uf, 1.0, temps=np.zeros(S), want_probs=True)
+        sm = orc.pq_verify(t, d, x, ua, uf, 1e-4, want_probs=True)
+        assert np.array_equal(g["n_acc"], sm["n_acc"]) and np.array_equal(g["tokens"], sm["tokens"])
+        assert np.array_equal(g["probs"], sm["probs"])  # one-hot rows both ways
+        assert np.all(g["fin_src"] == 3)
+        assert 0 < g["n_acc"].min() or g["n_acc"].max() > 0  # the cases accept something
+
+
+def test_greedy_ties_go_to_the_lower_index(orc):
+    V, k = 8, 2
+    t = np.zeros((1, k + 1, V), np.float32)
+    t[0, 0, [2, 5]] = 3.0     # tie: argmax is 2
+    t[0, 1, [1, 6]] = 1.0     # tie: argmax is 1
+    t[0, 2, :] = -1.0         # all equal: argmax is 0
+    d = np.zeros((1, k, V), np.float32)
+    g = orc.pq_verify(t, d, np.array([[2, 6]], np.int32), np.zeros((1, k), np.float32),
+                      np.zeros(1, np.float32), 1.0, temps=np.zeros(1))
+    assert g["n_acc"][0] == 1 and list(g["tokens"][0]) == [2, 1, -1]
+    g = orc.pq_verify(t, d, np.array([[2, 1]], np.int32), np.zeros((1, k), np.float32),
+                      np.zeros(1, np.float32), 1.0, temps=np.zeros(1))
+    assert g["n_acc"][0] == 2 and list(g["tokens"][0]) == [2, 1, 0]
+
+
+def test_per_session_temperature_matches_the_scalar_verify(orc):
+    st = synth.streams(0)
+    S, k, V = 6, 4, 256
+    v = synth.verify_inputs(st, S, k, V, 2.0, 0.5, 1.0)
+    temps = np.array([0.5, 1.0, 2.0, 0.0, 0.7, 1.0])
+    got = orc.pq_verify(v["target"], v["draft"], v["drafts"], v["u_acc"], v["u_fin"], 1.0, temps=temps,
+                        want_probs=True)
+    for s in range(S):
+        sl = slice(s, s + 1)
+        if temps[s] > 0:
+            ref = orc.pq_verify(v["target"][sl], v["draft"][sl], v["drafts"][sl], v["u_acc"][sl], v["u_fin"][sl],
+                                float(temps[s]), want_probs=True)
+        else:
+            ref = orc.pq_verify(v["target"][sl], v["draft"][sl], v["drafts"][sl], v["u_acc"][sl], v["u_fin"][sl],
+                                1.0, temps=np.zeros(1), want_probs=True)
+        assert got["n_acc"][s] == ref["n_acc"][0]
+        assert np.array_equal(got["tokens"][s], ref["tokens"][0])
+        assert np.array_equal(got["probs"][s], ref["probs"][0])
+
+
+def test_bad_temperature_marks_only_its_session(orc):
+    st = synth.streams(0)
+    S, k, V = 4, 3, 64
+    v = synth.verify_inputs(st, S, k, V, 2.0, 0.5, 1.0)
+    temps = np.array([1.0, -0.5, np.nan, 1.0])
+    got = orc.pq_verify(v["target"], v["draft"], v["drafts"], v["u_acc"], v["u_fin"], 1.0, temps=temps)
+    assert got["bad_temperature"] and not got["bad_token"]
+    assert list(got["n_acc"][1:3]) == [-1, -1] and np.all(got["tokens"][1:3] == -1)
+    ref = orc.pq_verify(v["target"], v["draft"], v["drafts"], v["u_acc"], v["u_fin"], 1.0)
+    assert np.array_equal(got["tokens"][[0, 3]], ref["tokens"][[0, 3]])
