@@ -62,7 +62,8 @@ typedef enum {
     Q2_ERR_CUDA = 5,        /* a CUDA runtime call (launch, attribute, copy) failed        */
     Q2_ERR_TIMEOUT = 6,     /* a bounded device-side wait gave up                          */
     Q2_ERR_BAD_TOKEN = 7,   /* device: a draft token is outside [0, V)                     */
-    Q2_ERR_RANGE = 8        /* device: a Q2B32 scale |d| >= 64 or infinite (outside the exact path) */
+    Q2_ERR_RANGE = 8,       /* device: a Q2B32 scale |d| >= 64 or infinite (outside the exact path) */
+    Q2_ERR_BAD_TEMPERATURE = 9 /* device: a per-session temperature is negative or not finite */
 } q2_status;
 
 #define Q2_WORKSPACE_HEADER_BYTES 256
@@ -168,6 +169,27 @@ q2_status pq_verify(const float *target_logits, const float *draft_logits,
                     int S, int k, int V, float temperature, int32_t *n_accepted,
                     int32_t *out_tokens, float *probs_out, void *ws, size_t ws_bytes,
                     q2_stream_t stream);
+
+/*
+ * pq_verify with one temperature per session, and the greedy verify.
+ *   temperatures  fp32 [S] in device memory, 4-byte aligned: T_s for session s (p and q of a
+ *                 session share it, as in pq_verify).  T_s = 0 selects the greedy verify for
+ *                 that session (the T -> 0 limit, bit-exact decoding: "1x Spark tuned DSpark
+ *                 ...", the reply on the decode arc; "Optimizing DeepSeek-V4-Flash ...", post
+ *                 #20): draft x_i is accepted iff it is argmax p_i, the token after the first
+ *                 rejection j (or the extra token, j = k) is argmax p_j, ties going to the lower
+ *                 token index; the draft logits' values and the uniforms are then not used, and
+ *                 probs_out rows are one-hot at each row's argmax.
+ * Every other argument is as for pq_verify, and required as there (greedy sessions ignore
+ * their uniforms and draft logits).  Device errors: as pq_verify, plus Q2_ERR_BAD_TEMPERATURE for a
+ * negative, NaN or infinite T_s (that session gets n_accepted = -1 and tokens -1; the others are
+ * unaffected).  The workspace is pq_verify_workspace(S, k, V).
+ */
+q2_status pq_verify_ex(const float *target_logits, const float *draft_logits,
+                       const int32_t *draft_tokens, const float *u_acc, const float *u_fin,
+                       int S, int k, int V, const float *temperatures, int32_t *n_accepted,
+                       int32_t *out_tokens, float *probs_out, void *ws, size_t ws_bytes,
+                       q2_stream_t stream);
 
 /*
  * pq_verify without a workspace, for callers that cannot allocate device memory: e.g. a

@@ -129,6 +129,13 @@ cudaError_t q2v::probe_mark(int kernel, int end, cudaStream_t s) {
     return cudaEventRecord(g_probe_ev[end], s);
 }
 
+namespace {
+q2_status pq_verify_impl(const float *target_logits, const float *draft_logits, const int32_t *draft_tokens,
+                         const float *u_acc, const float *u_fin, int S, int k, int V, float temperature,
+                         const float *temps, int32_t *n_accepted, int32_t *out_tokens, float *probs_out, void *ws,
+                         size_t ws_bytes, q2_stream_t stream);
+}  // namespace
+
 extern "C" {
 
 int q2_version(void) { return Q2V_VERSION; }
@@ -153,6 +160,7 @@ const char *q2_status_string(q2_status s) {
         case Q2_ERR_TIMEOUT: return "device wait timed out";
         case Q2_ERR_BAD_TOKEN: return "draft token out of range";
         case Q2_ERR_RANGE: return "Q2B32 scale outside the exact range";
+        case Q2_ERR_BAD_TEMPERATURE: return "per-session temperature negative or not finite";
     }
     return "unknown status";
 }
@@ -254,8 +262,29 @@ q2_status pq_verify(const float *target_logits, const float *draft_logits, const
                     const float *u_acc, const float *u_fin, int S, int k, int V, float temperature,
                     int32_t *n_accepted, int32_t *out_tokens, float *probs_out, void *ws, size_t ws_bytes,
                     q2_stream_t stream) {
-    if (S < 1 || k < 0 || V < 1 || !target_logits || !u_fin || !n_accepted || !out_tokens ||
-        !(temperature > 0.0f) || !isfinite(temperature))
+    if (!(temperature > 0.0f) || !isfinite(temperature)) return Q2_ERR_INVALID_ARG;
+    return pq_verify_impl(target_logits, draft_logits, draft_tokens, u_acc, u_fin, S, k, V, temperature, nullptr,
+                          n_accepted, out_tokens, probs_out, ws, ws_bytes, stream);
+}
+
+q2_status pq_verify_ex(const float *target_logits, const float *draft_logits, const int32_t *draft_tokens,
+                       const float *u_acc, const float *u_fin, int S, int k, int V, const float *temperatures,
+                       int32_t *n_accepted, int32_t *out_tokens, float *probs_out, void *ws, size_t ws_bytes,
+                       q2_stream_t stream) {
+    if (!temperatures) return Q2_ERR_INVALID_ARG;
+    if (!aligned(temperatures, 4)) return Q2_ERR_ALIGNMENT;
+    return pq_verify_impl(target_logits, draft_logits, draft_tokens, u_acc, u_fin, S, k, V, 1.0f, temperatures,
+                          n_accepted, out_tokens, probs_out, ws, ws_bytes, stream);
+}
+
+}  // extern "C"
+
+namespace {
+q2_status pq_verify_impl(const float *target_logits, const float *draft_logits, const int32_t *draft_tokens,
+                         const float *u_acc, const float *u_fin, int S, int k, int V, float temperature,
+                         const float *temps, int32_t *n_accepted, int32_t *out_tokens, float *probs_out, void *ws,
+                         size_t ws_bytes, q2_stream_t stream) {
+    if (S < 1 || k < 0 || V < 1 || !target_logits || !u_fin || !n_accepted || !out_tokens)
         return Q2_ERR_INVALID_ARG;
     if (k > 0 && (!draft_logits || !draft_tokens || !u_acc)) return Q2_ERR_INVALID_ARG;
     if (k > kMaxDrafts || V > (1 << 28)) return Q2_ERR_UNSUPPORTED;
@@ -276,6 +305,7 @@ q2_status pq_verify(const float *target_logits, const float *draft_logits, const
     a.u_fin = u_fin;
     a.S = S; a.k = k; a.V = V;
     a.beta = (float)(1.4426950408889634 / (double)temperature);
+    a.temps = temps;
     a.n_acc = n_accepted;
     a.tokens = out_tokens;
     a.probs = probs_out;
@@ -296,5 +326,4 @@ q2_status pq_verify(const float *target_logits, const float *draft_logits, const
     }
     return cuda_status(launch_pq_verify(a, sp, warp_tier, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
-
-}  // extern "C"
+}  // namespace

@@ -29,7 +29,8 @@ struct PqArgs {
     const float *u_acc;
     const float *u_fin;
     int S, k, V;
-    float beta;     // log2(e) / T
+    float beta;     // log2(e) / T (every session, when temps is null)
+    const float *temps;  // [S] per-session temperatures, nullable: 0 = greedy
     int32_t *n_acc;
     int32_t *tokens;
     float *probs;

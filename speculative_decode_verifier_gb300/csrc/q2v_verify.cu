@@ -84,7 +84,7 @@ __device__ __forceinline__ const float *row_ptr(const PqArgs &a, int s, int r) {
 // lp = (t(x) - max_t) * beta - log2 Z_t (likewise lq), so neither probability underflows on
 // its own; q(x) == 0 exactly (a -inf draft logit) accepts.  Returns j in [0, k], or -1 if
 // a draft token is out of range.
-__device__ int accept_scan(const PqArgs &a, int s, const float *rowM, const float *rowL2Z) {
+__device__ int accept_scan(const PqArgs &a, int s, float beta, const float *rowM, const float *rowL2Z) {
     for (int i = 0; i < a.k; ++i) {
         const int x = a.drafts[(size_t)s * a.k + i];
         if (x < 0 || x >= a.V) return -1;
@@ -93,11 +93,67 @@ __device__ int accept_scan(const PqArgs &a, int s, const float *rowM, const floa
         const int x = a.drafts[(size_t)s * a.k + i];
         const float tx = row_ptr(a, s, i)[x], dx = row_ptr(a, s, a.k + 1 + i)[x];
         if (dx == -INFINITY) continue;  // q(x) == 0 accepts
-        const float lp = (tx - rowM[i]) * a.beta - rowL2Z[i];
-        const float lq = (dx - rowM[a.k + 1 + i]) * a.beta - rowL2Z[a.k + 1 + i];
+        const float lp = (tx - rowM[i]) * beta - rowL2Z[i];
+        const float lq = (dx - rowM[a.k + 1 + i]) * beta - rowL2Z[a.k + 1 + i];
         const float ratio = ex2(lp - lq);
         if (!(a.u_acc[(size_t)s * a.k + i] < ratio)) return i;
     }
+    return a.k;
+}
+
+// How session s is verified: 1 = sampling with *beta = log2(e) / T, 0 = greedy (T = 0),
+// -1 = a negative or non-finite temperature (the session is marked bad).
+__device__ __forceinline__ int session_mode(const PqArgs &a, int s, float *beta) {
+    if (!a.temps) {
+        *beta = a.beta;
+        return 1;
+    }
+    const float T = a.temps[s];
+    *beta = 0.0f;
+    if (T == 0.0f) return 0;
+    if (!(T > 0.0f) || !(T < INFINITY)) return -1;
+    *beta = (float)(1.4426950408889634 / (double)T);  // as the host computes it for pq_verify
+    return 1;
+}
+
+// The greedy choice: the largest value, ties to the lower token index.  (m, i) pairs from
+// lanes or chunks combine with better_arg.
+__device__ __forceinline__ bool better_arg(float m2, int i2, float m1, int i1) {
+    return m2 > m1 || (m2 == m1 && i2 < i1);
+}
+__device__ __forceinline__ void warp_argmax(float &m, int &i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+        const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+        if (better_arg(m2, i2, m, i)) {
+            m = m2;
+            i = i2;
+        }
+    }
+}
+// A lane's (max, first index of it) over y = y0 + lane, y0 + lane + 32, ... < y1.
+__device__ __forceinline__ void lane_argmax(const float *x, int y0, int y1, int lane, float &m, int &i) {
+    m = -INFINITY;
+    i = 0x7FFFFFFF;
+    for (int y = y0 + lane; y < y1; y += 32) {
+        const float v = x[y];
+        if (i == 0x7FFFFFFF || v > m) {
+            m = v;
+            i = y;
+        }
+    }
+}
+
+// The greedy verify's outcome from the target rows' argmaxes am[0..k]: j = the first draft
+// that is not argmax p_i (k if none), the token after it argmax p_j.  -1: a bad draft token.
+__device__ __forceinline__ int greedy_scan(const PqArgs &a, int s, const int *am) {
+    for (int i = 0; i < a.k; ++i) {
+        const int x = a.drafts[(size_t)s * a.k + i];
+        if (x < 0 || x >= a.V) return -1;
+    }
+    for (int i = 0; i < a.k; ++i)
+        if (a.drafts[(size_t)s * a.k + i] != am[i]) return i;
     return a.k;
 }
 
@@ -155,12 +211,48 @@ constexpr int kWarpTierWarps = 8;
 __global__ void __launch_bounds__(kWarpTierWarps * 32) pqv_warp_kernel(PqArgs a) {
     __shared__ float sM[kWarpTierWarps][kMaxRows];
     __shared__ float sL2Z[kWarpTierWarps][kMaxRows];
+    __shared__ int sArg[kWarpTierWarps][kMaxRows];
     pdl_wait();
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int R = 2 * a.k + 1;
-    const float beta = a.beta;
     for (int s = blockIdx.x * kWarpTierWarps + warp; s < a.S; s += gridDim.x * kWarpTierWarps) {
+        float beta;
+        const int smode = session_mode(a, s, &beta);
+        if (smode < 0) {
+            if (lane == 0) {
+                set_status(a.status, Q2_ERR_BAD_TEMPERATURE);
+                write_tokens(a, s, -1, -1);
+            }
+            __syncwarp();
+            continue;
+        }
+        if (smode == 0) {
+            // greedy: the argmax of every row (the target rows decide; all rows for probs)
+            for (int r = 0; r < R; ++r) {
+                float m;
+                int i;
+                lane_argmax(row_ptr(a, s, r), 0, a.V, lane, m, i);
+                warp_argmax(m, i);
+                if (lane == 0) sArg[warp][r] = i;
+            }
+            __syncwarp();
+            int j = 0;
+            if (lane == 0) j = greedy_scan(a, s, sArg[warp]);
+            j = __shfl_sync(0xffffffffu, j, 0);
+            if (a.probs)
+                for (int r = 0; r < R; ++r) {
+                    float *o = a.probs + ((size_t)s * R + r) * a.V;
+                    const int am = sArg[warp][r];
+                    for (int y = lane; y < a.V; y += 32) o[y] = (y == am) ? 1.0f : 0.0f;
+                }
+            if (lane == 0) {
+                if (j < 0) set_status(a.status, Q2_ERR_BAD_TOKEN);
+                write_tokens(a, s, j, j < 0 ? -1 : sArg[warp][j]);
+            }
+            __syncwarp();
+            continue;
+        }
         for (int r = 0; r < R; ++r) {
             const float *x = row_ptr(a, s, r);
             float m = -INFINITY, z = 0.0f;
@@ -182,7 +274,7 @@ __global__ void __launch_bounds__(kWarpTierWarps * 32) pqv_warp_kernel(PqArgs a)
         }
         __syncwarp();
         int j = 0;
-        if (lane == 0) j = accept_scan(a, s, sM[warp], sL2Z[warp]);
+        if (lane == 0) j = accept_scan(a, s, beta, sM[warp], sL2Z[warp]);
         j = __shfl_sync(0xffffffffu, j, 0);
         if (a.probs) {
             for (int r = 0; r < R; ++r) {
@@ -244,8 +336,23 @@ __global__ void __launch_bounds__(512) pqv_stats_kernel(PqArgs a, PqSplit sp) {
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, nwarps = blockDim.x >> 5;
     const int R = 2 * a.k + 1;
     const int c0 = c * sp.L, c1 = min(a.V, c0 + sp.L);
-    const float beta = a.beta;
+    float beta;
+    const int smode = session_mode(a, s, &beta);
     if (c == 0 && threadIdx.x == 0) sp.tickets[s] = 0u;
+    if (smode < 0) return;
+    if (smode == 0) {
+        // greedy: (max, first index of it) of every row's chunk; the index travels as the
+        // bits of the partial's second float
+        for (int r = warp; r < R; r += nwarps) {
+            float m;
+            int i;
+            lane_argmax(row_ptr(a, s, r), c0, c1, lane, m, i);
+            warp_argmax(m, i);
+            if (lane == 0)
+                reinterpret_cast<float2 *>(sp.stats)[((size_t)s * R + r) * sp.C + c] = make_float2(m, __int_as_float(i));
+        }
+        return;
+    }
     for (int r = warp; r < R; r += nwarps) {
         const float *x = row_ptr(a, s, r);
         float m = -INFINITY, z = 0.0f;
@@ -312,9 +419,62 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
     const int c = blockIdx.x, s = blockIdx.y;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int R = 2 * a.k + 1;
-    const float beta = a.beta;
+    float beta;
+    const int smode = session_mode(a, s, &beta);
     const int c0 = c * sp.L, c1 = min(a.V, c0 + sp.L);
     const int Lw = sp.L / kSegsPerChunk;  // tokens per warp segment (a multiple of 16)
+    if (smode < 0) {
+        if (c == 0 && tid == 0) {
+            set_status(a.status, Q2_ERR_BAD_TEMPERATURE);
+            write_tokens(a, s, -1, -1);
+        }
+        return;
+    }
+    if (smode == 0) {
+        // greedy: every row's argmax from the chunk partials (16 lanes per row; chunk order
+        // and better_arg keep the lowest index among equal maxima), one-hot probabilities for
+        // this chunk, and CTA 0 decides the tokens
+        __shared__ int s_arg[kMaxRows];
+        for (int r0 = 0; r0 < R; r0 += 16) {
+            const int r = r0 + (tid >> 4), sub = tid & 15;
+            float m = -INFINITY;
+            int i = 0x7FFFFFFF;
+            if (r < R) {
+                const float2 *st = reinterpret_cast<const float2 *>(sp.stats) + ((size_t)s * R + r) * sp.C;
+                for (int cc = sub; cc < sp.C; cc += 16) {
+                    const float2 w = st[cc];
+                    const int wi = __float_as_int(w.y);
+                    if (better_arg(w.x, wi, m, i)) {
+                        m = w.x;
+                        i = wi;
+                    }
+                }
+            }
+#pragma unroll
+            for (int o = 8; o > 0; o >>= 1) {
+                const float m2 = __shfl_xor_sync(0xffffffffu, m, o);
+                const int i2 = __shfl_xor_sync(0xffffffffu, i, o);
+                if (better_arg(m2, i2, m, i)) {
+                    m = m2;
+                    i = i2;
+                }
+            }
+            if (sub == 0 && r < R) s_arg[r] = i;
+        }
+        __syncthreads();
+        if (a.probs)
+            for (int r = 0; r < R; ++r) {
+                float *o = a.probs + ((size_t)s * R + r) * a.V;
+                const int am = s_arg[r];
+                for (int y = c0 + tid; y < c1; y += blockDim.x) o[y] = (y == am) ? 1.0f : 0.0f;
+            }
+        if (c == 0 && tid == 0) {
+            const int j = greedy_scan(a, s, s_arg);
+            if (j < 0) set_status(a.status, Q2_ERR_BAD_TOKEN);
+            write_tokens(a, s, j, j < 0 ? -1 : s_arg[j]);
+        }
+        return;
+    }
 
     // 1. row statistics from the chunk partials: 16 lanes per row, partials held in
     //    registers so the combine takes one round of loads

@@ -19,11 +19,11 @@ LIB_PATH = os.path.join(_HERE, "_build", "libq2v.so")
 Q2_OK = 0
 STATUS_NAMES = {0: "Q2_OK", 1: "Q2_ERR_INVALID_ARG", 2: "Q2_ERR_ALIGNMENT", 3: "Q2_ERR_UNSUPPORTED",
                 4: "Q2_ERR_WORKSPACE", 5: "Q2_ERR_CUDA", 6: "Q2_ERR_TIMEOUT", 7: "Q2_ERR_BAD_TOKEN",
-                8: "Q2_ERR_RANGE"}
+                8: "Q2_ERR_RANGE", 9: "Q2_ERR_BAD_TEMPERATURE"}
 MOE_RENORMALIZE = 1
 EXPORTS = ("q2_tiny_gemm_workspace", "q2_tiny_gemm", "q2_moe_grouped_workspace", "q2_moe_grouped",
            "pq_verify_workspace", "pq_verify", "pq_verify_noalloc", "q2_get_device_status", "q2_status_string",
-           "q2_version", "q2_set_probe")
+           "q2_version", "q2_set_probe", "pq_verify_ex")
 
 # kernels that q2_set_probe can bracket (q2_probe_kernel)
 PROBE_NONE, PROBE_MOE_GATE_UP, PROBE_MOE_DOWN, PROBE_GEMM, PROBE_PQ_STATS, PROBE_PQ_VERIFY = range(6)
@@ -61,6 +61,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.pq_verify_workspace.restype = Z
     lib.pq_verify.argtypes = [P, P, P, P, P, I, I, I, F, P, P, P, P, Z, P]
     lib.pq_verify.restype = I
+    lib.pq_verify_ex.argtypes = [P, P, P, P, P, I, I, I, P, P, P, P, P, Z, P]
+    lib.pq_verify_ex.restype = I
     lib.pq_verify_noalloc.argtypes = [P, P, P, P, P, I, I, I, F, P, P, P, P]
     lib.pq_verify_noalloc.restype = I
     lib.q2_get_device_status.argtypes = [P, P]
@@ -225,6 +227,39 @@ def pq_verify(target: torch.Tensor, draft: torch.Tensor | None, drafts: torch.Te
                           _ptr(n_acc), _ptr(tokens), _ptr(probs), _ptr(ws), ws.numel(),
                           ctypes.c_void_p(_stream(stream)))
     _raise(st, "pq_verify")
+    return n_acc, tokens
+
+
+def pq_verify_ex(target: torch.Tensor, draft: torch.Tensor | None, drafts: torch.Tensor | None,
+                 u_acc: torch.Tensor | None, u_fin: torch.Tensor, temperatures: torch.Tensor,
+                 n_acc: torch.Tensor | None = None, tokens: torch.Tensor | None = None,
+                 probs: torch.Tensor | None = None, ws: torch.Tensor | None = None, stream=None):
+    """pq_verify with one temperature per session (fp32 [S] on the device; 0 = the greedy
+    verify).  Returns (n_acc [S] int32, tokens [S,k+1] int32)."""
+    _check(target, "target", torch.float32)
+    S, k1, V = target.shape
+    k = k1 - 1
+    if k > 0:
+        _check(draft, "draft", torch.float32)
+        _check(drafts, "drafts", torch.int32)
+        _check(u_acc, "u_acc", torch.float32)
+    _check(u_fin, "u_fin", torch.float32)
+    _check(temperatures, "temperatures", torch.float32)
+    dev = target.device
+    if n_acc is None:
+        n_acc = torch.empty(S, dtype=torch.int32, device=dev)
+    if tokens is None:
+        tokens = torch.empty((S, k + 1), dtype=torch.int32, device=dev)
+    _check(n_acc, "n_acc", torch.int32)
+    _check(tokens, "tokens", torch.int32)
+    _check(probs, "probs", torch.float32, nullable=True)
+    if ws is None:
+        ws = workspace(pq_verify_workspace(S, k, V), dev)
+    st = load().pq_verify_ex(_ptr(target), _ptr(draft) if k > 0 else None, _ptr(drafts) if k > 0 else None,
+                             _ptr(u_acc) if k > 0 else None, _ptr(u_fin), S, k, V, _ptr(temperatures),
+                             _ptr(n_acc), _ptr(tokens), _ptr(probs), _ptr(ws), ws.numel(),
+                             ctypes.c_void_p(_stream(stream)))
+    _raise(st, "pq_verify_ex")
     return n_acc, tokens
 
 

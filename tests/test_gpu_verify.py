@@ -156,3 +156,88 @@ def test_chi_square_emitted_law_on_gpu(env):
                                v["u_acc"][diff], v["u_fin"][diff], k)
         assert stats["mismatches_at_near_ties"] == diff.size
     assert diff.size <= 200
+
+
+# ---------------------------------------------------------------- per-session temperature, greedy
+
+def _gpu_ex(env, v, temps, want_probs=False):
+    import torch
+    dev, q2v, _ = env
+    S, k1, V = v["target"].shape
+    k = k1 - 1
+    t = {n: to_dev(v[n], dev) for n in ("target", "draft", "drafts", "u_acc", "u_fin")}
+    tt = torch.tensor(np.asarray(temps, np.float32), device=dev)
+    probs = torch.empty((S, 2 * k + 1, V), dtype=torch.float32, device=dev) if want_probs else None
+    ws = q2v.workspace(q2v.pq_verify_workspace(S, k, V), dev)
+    n_acc, toks = q2v.pq_verify_ex(t["target"], t["draft"] if k else None, t["drafts"] if k else None,
+                                   t["u_acc"] if k else None, t["u_fin"], tt, probs=probs, ws=ws)
+    st = q2v.q2_get_device_status(ws)
+    return n_acc.cpu().numpy(), toks.cpu().numpy(), (probs.cpu().numpy() if want_probs else None), st
+
+
+def _greedy_inputs(seed, S, k, V):
+    """Seeded logits whose drafts agree with the target argmax for a random prefix."""
+    st = synth.Streams(seed)
+    v = synth.verify_inputs(st, S, k, V, 3.0, 1.0, 1.0)
+    am = np.argmax(v["target"], axis=2)
+    rng = np.random.default_rng(seed)
+    for s in range(S):
+        agree = rng.integers(0, k + 1)
+        v["drafts"][s, :agree] = am[s, :agree]
+    return v
+
+
+@pytest.mark.parametrize("S,k,V", [(8, 4, 1024), (3, 4, 129280), (5, 3, 8192), (4, 0, 5000)])
+def test_greedy_matches_oracle_exactly(env, S, k, V):
+    v = _greedy_inputs(400 + V, S, k, V)
+    n, toks, probs, st = _gpu_ex(env, v, np.zeros(S), want_probs=True)
+    o = env[2].pq_verify(v["target"], v["draft"], v["drafts"], v["u_acc"], v["u_fin"], 1.0, temps=np.zeros(S),
+                         want_probs=True)
+    assert st == 0
+    assert np.array_equal(n, o["n_acc"]) and np.array_equal(toks, o["tokens"])
+    assert np.array_equal(probs.astype(np.float64), o["probs"])  # one-hot rows
+    assert n.max() > 0 or k == 0
+
+
+@pytest.mark.parametrize("V", [1024, 8192, 129280])
+def test_mixed_temperatures_match_oracle(env, V):
+    S, k = 6, 4
+    v = synth.verify_inputs(synth.Streams(500 + V), S, k, V, 3.0, 1.0, 1.0)
+    temps = np.array([0.5, 1.0, 0.0, 2.0, 0.0, 1.3])
+    n, toks, probs, st = _gpu_ex(env, v, temps, want_probs=True)
+    o = env[2].pq_verify(v["target"], v["draft"], v["drafts"], v["u_acc"], v["u_fin"], 1.0, temps=temps,
+                         want_probs=True)
+    assert st == 0
+    assert np.abs(probs.astype(np.float64) - o["probs"]).max() <= PROB_ATOL
+    greedy = temps == 0.0
+    assert np.array_equal(n[greedy], o["n_acc"][greedy]) and np.array_equal(toks[greedy], o["tokens"][greedy])
+    samp = np.nonzero(~greedy)[0]
+    sub = {key: (o[key][samp] if o[key] is not None else None) for key in o if key not in ("bad_token", "bad_temperature")}
+    stats = compare_verify(n[samp], toks[samp], sub, v["u_acc"][samp], v["u_fin"][samp], k)
+    assert stats["exact"] + stats["mismatches_at_near_ties"] == len(samp)
+
+
+@pytest.mark.parametrize("V", [1024, 129280])
+def test_bad_temperature_marks_only_its_session(env, V):
+    S, k = 4, 3
+    v = synth.verify_inputs(synth.Streams(600 + V), S, k, V, 3.0, 1.0, 1.0)
+    temps = np.array([1.0, -0.5, np.nan, 0.0])
+    n, toks, _, st = _gpu_ex(env, v, temps)
+    assert st == 9  # Q2_ERR_BAD_TEMPERATURE
+    assert list(n[1:3]) == [-1, -1] and np.all(toks[1:3] == -1)
+    o = env[2].pq_verify(v["target"], v["draft"], v["drafts"], v["u_acc"], v["u_fin"], 1.0, temps=temps,
+                         want_probs=True)
+    assert n[3] == o["n_acc"][3] and np.array_equal(toks[3], o["tokens"][3])
+    sub = {key: (o[key][[0]] if o[key] is not None else None) for key in o if key not in ("bad_token", "bad_temperature")}
+    stats = compare_verify(n[[0]], toks[[0]], sub, v["u_acc"][[0]], v["u_fin"][[0]], k)
+    assert stats["exact"] + stats["mismatches_at_near_ties"] == 1
+
+
+@pytest.mark.parametrize("V", [1024, 129280])
+def test_equal_temperatures_equal_the_scalar_call(env, V):
+    S, k = 3, 4
+    v = synth.verify_inputs(synth.Streams(700 + V), S, k, V, 3.0, 1.0, 1.0)
+    v["T"] = 0.8
+    n0, t0, p0 = _gpu(env, v, want_probs=True)
+    n1, t1, p1, st = _gpu_ex(env, v, np.full(S, 0.8), want_probs=True)
+    assert st == 0 and np.array_equal(n0, n1) and np.array_equal(t0, t1) and np.array_equal(p0, p1)
