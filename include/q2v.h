@@ -213,6 +213,32 @@ q2_status pq_verify_noalloc(const float *target_logits, const float *draft_logit
                             int S, int k, int V, float temperature, int32_t *n_accepted,
                             int32_t *out_tokens, float *probs_out, q2_stream_t stream);
 
+/* ------------------------------------------------------------------ yield quench (host) */
+
+/* Per-session state of the terminal yield-quench controller ("ds4-on-spark" README, "The
+ * break-even law"; "1x Spark tuned DSpark ...", "The break-even law, and why speculation
+ * can't hurt you here"): the running regret in plain decode steps, the steps counted, and
+ * whether speculation has been switched off for the rest of the request. */
+typedef struct {
+    double regret;
+    int steps;
+    int quenched;
+} q2_quench_state;
+
+/* Host memory, S entries: zero regret, no steps, not quenched.  Q2_ERR_INVALID_ARG for a NULL
+ * state or S < 1. */
+q2_status q2_quench_init(q2_quench_state *state, int S);
+
+/* One verify step for S sessions (host code; n_accepted is the verify's output copied to the
+ * host).  A session that is not quenched and has n_accepted[s] >= 0 adds
+ * guard - (n_accepted[s] + 1) (one verify costs `guard` plain steps and commits
+ * n_accepted + 1 tokens; 2.16 is the pages' calibration) to its regret and is quenched,
+ * terminally, once the regret exceeds `threshold` (about 4 plain-step times).  Sessions with
+ * n_accepted < 0 (a device error) are skipped.  Returns the number of sessions quenched by
+ * this step, or -1 for invalid arguments (NULL pointers, S < 1, non-finite guard/threshold). */
+int q2_quench_update(q2_quench_state *state, int S, const int32_t *n_accepted, double guard,
+                     double threshold);
+
 /* ------------------------------------------------------------------ measurement hook */
 
 /* Kernels that q2_set_probe can bracket. */

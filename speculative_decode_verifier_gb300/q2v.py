@@ -23,7 +23,7 @@ STATUS_NAMES = {0: "Q2_OK", 1: "Q2_ERR_INVALID_ARG", 2: "Q2_ERR_ALIGNMENT", 3: "
 MOE_RENORMALIZE = 1
 EXPORTS = ("q2_tiny_gemm_workspace", "q2_tiny_gemm", "q2_moe_grouped_workspace", "q2_moe_grouped",
            "pq_verify_workspace", "pq_verify", "pq_verify_noalloc", "q2_get_device_status", "q2_status_string",
-           "q2_version", "q2_set_probe", "pq_verify_ex")
+           "q2_version", "q2_set_probe", "pq_verify_ex", "q2_quench_init", "q2_quench_update")
 
 # kernels that q2_set_probe can bracket (q2_probe_kernel)
 PROBE_NONE, PROBE_MOE_GATE_UP, PROBE_MOE_DOWN, PROBE_GEMM, PROBE_PQ_STATS, PROBE_PQ_VERIFY = range(6)
@@ -70,6 +70,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q2_status_string.argtypes = [I]
     lib.q2_status_string.restype = ctypes.c_char_p
     lib.q2_version.restype = I
+    lib.q2_quench_init.argtypes = [P, I]
+    lib.q2_quench_init.restype = I
+    lib.q2_quench_update.argtypes = [P, I, P, ctypes.c_double, ctypes.c_double]
+    lib.q2_quench_update.restype = I
     lib.q2_set_probe.argtypes = [I, P, P]
     lib.q2_set_probe.restype = I
     _lib = lib
@@ -90,6 +94,53 @@ def q2_status_string(status: int) -> str:
 
 def q2_version() -> int:
     return version()
+
+
+class QuenchState(ctypes.Structure):
+    """q2_quench_state: the running regret, the steps counted, quenched (0/1)."""
+    _fields_ = [("regret", ctypes.c_double), ("steps", ctypes.c_int), ("quenched", ctypes.c_int)]
+
+
+QUENCH_GUARD = 2.16      # plain steps per verify step (the pages' calibration)
+QUENCH_THRESHOLD = 4.0   # plain-step deficit that quenches a request
+
+
+def q2_quench_init(S: int):
+    """A fresh q2_quench_state array of S sessions (host memory)."""
+    state = (QuenchState * S)()
+    _raise(load().q2_quench_init(state, S), "q2_quench_init")
+    return state
+
+
+def q2_quench_update(state, n_accepted, guard: float = 2.16, threshold: float = 4.0) -> int:
+    """One verify step over len(state) sessions; returns the number newly quenched."""
+    import numpy as np
+    a = np.ascontiguousarray(np.asarray(n_accepted, dtype=np.int32))
+    if a.shape != (len(state),):
+        raise ValueError(f"n_accepted must have shape ({len(state)},)")
+    r = load().q2_quench_update(state, len(state), a.ctypes.data_as(ctypes.c_void_p), float(guard), float(threshold))
+    if r < 0:
+        raise Q2Error(1, "q2_quench_update")
+    return r
+
+
+class YieldQuench:
+    """Host-side yield-quench controller for S sessions (state kept in the library's C struct)."""
+
+    def __init__(self, S: int, guard: float = QUENCH_GUARD, threshold: float = QUENCH_THRESHOLD):
+        self.S, self.guard, self.threshold = S, float(guard), float(threshold)
+        self.state = q2_quench_init(S)
+
+    def update(self, n_accepted) -> int:
+        """One verify step; n_accepted: int32 host array [S] (a torch CPU tensor or numpy).
+        Returns the number of sessions this step quenched."""
+        return q2_quench_update(self.state, n_accepted, self.guard, self.threshold)
+
+    def quenched(self):
+        return [bool(self.state[s].quenched) for s in range(self.S)]
+
+    def regret(self):
+        return [self.state[s].regret for s in range(self.S)]
 
 
 def q2_set_probe(kernel: int, ev_begin=None, ev_end=None) -> None:

@@ -41,7 +41,7 @@ def test_binding_names_match_header():
 
 def test_version_and_status_strings(lib):
     assert lib.q2_version() == 100
-    for code in range(9):
+    for code in range(10):
         assert lib.q2_status_string(code)
     assert lib.q2_status_string(99) == b"unknown status"
 
