@@ -338,6 +338,7 @@ def run_device(args, rank: int, world: int):
     # weight stream of each starting before its activation prep is done), 4 rotating layer
     # sets (200 MB, larger than L2)
     chain = None
+    layer = None
     if not args.no_extras:
         layers = [[D(synth.q2b32_weights(synth.Streams(9000 + 8 * j + i), sh["N"], sh["K"]).reshape(-1))
                    for i in range(8)] for j in range(N_SETS)]
@@ -352,6 +353,22 @@ def run_device(args, rank: int, world: int):
         c_us = graph_us(chain_all, max(3, args.steps // 4)) / N_SETS
         chain = {"layers": 8, "us_per_8": c_us, "us_per_linear": c_us / 8,
                  "GB/s": 8 * lin_bytes / (c_us * 1e-6) / 1e9, "frac": 8 * lin_bytes / (c_us * 1e-6) / 1e9 / peak_x}
+
+        # one verifier layer: Q, K, V, O as 4096 x 4096 Q2B32 linears (the pages give no
+        # attention shapes; the model width is used) + the routed MoE FFN, all at M=5, one
+        # CUDA graph per step, PDL between the calls
+        Yq = torch.empty((sh["M"], sh["N"]), dtype=torch.float32, device=dev)
+
+        def layer_all():
+            for j in range(N_SETS):
+                for Wl in layers[j][:4]:
+                    q2v.q2_tiny_gemm(Wl, sh["N"], sh["K"], sets[j]["A"], Y=Yq, ws=wsc)
+                part_moe(sets[j])
+
+        l_us = graph_us(layer_all, max(3, args.steps // 4)) / N_SETS
+        l_bytes = 4 * lin_bytes + statistics.mean(active) * EXPERT_BYTES + sh["M"] * sh["H"] * 6
+        layer = {"workload": "Q,K,V,O 4096x4096 Q2B32 linears + routed MoE FFN (64 experts, top-6), M=5",
+                 "us": l_us, "GB/s": l_bytes / (l_us * 1e-6) / 1e9, "frac": l_bytes / (l_us * 1e-6) / 1e9 / peak_x}
         del layers
 
     # the cohort verify: 12 sessions x 5 rows = M=60 against a 129,280 x 4096 Q2B32 vocabulary
@@ -380,10 +397,18 @@ def run_device(args, rank: int, world: int):
             c_gemm()
             c_pq()
 
-        g_us, p_us, b_us = (graph_us(f, max(5, args.steps // 2)) for f in (c_gemm, c_pq, c_both))
+        Yc3 = Yco.view(12, 5, Nc)
+        wsf = q2v.workspace(q2v.q2_lm_head_verify_workspace(12, 4, Nc, Kc), dev)
+
+        def c_fused():
+            q2v.q2_lm_head_verify(Wc, Nc, Kc, Ac, Dc, xc, uac, ufc, 12, 4, temperature=1.0, target=Yc3,
+                                  n_acc=nc, tokens=tc, ws=wsf)
+
+        g_us, p_us, b_us, f_us = (graph_us(f, max(5, args.steps // 2)) for f in (c_gemm, c_pq, c_both, c_fused))
         wbytes = Nc * (Kc // 32) * 12
         cohort = {"workload": "M=60 x N=129280 x K=4096 Q2B32 GEMM (tcgen05) + pq_verify S=12 k=4 V=129280",
                   "gemm_us": g_us, "pq_verify_us": p_us, "gemm_plus_verify_us": b_us,
+                  "fused_lm_head_verify_us": f_us,
                   "gemm_GB/s": (wbytes + Mc * Kc * 2 + Mc * Nc * 4) / (g_us * 1e-6) / 1e9,
                   "gemm_TFLOP/s": 2.0 * Mc * Nc * Kc / (g_us * 1e-6) / 1e12,
                   "gemm_frac_hbm": (wbytes + Mc * Kc * 2 + Mc * Nc * 4) / (g_us * 1e-6) / 1e9 / peak_x}
@@ -487,6 +512,7 @@ def run_device(args, rank: int, world: int):
         "e2e": {"value": e2e_us, "unit": "µs", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
         "chained_linears_m5": chain,
+        "verifier_layer_m5": layer,
         "cohort_m60": cohort,
         "clocks": clocks,
     }

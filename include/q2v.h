@@ -213,6 +213,36 @@ q2_status pq_verify_noalloc(const float *target_logits, const float *draft_logit
                             int S, int k, int V, float temperature, int32_t *n_accepted,
                             int32_t *out_tokens, float *probs_out, q2_stream_t stream);
 
+/* ------------------------------------------------------------------ vocabulary head + verify */
+
+/* Workspace bytes for q2_lm_head_verify with these sizes. */
+size_t q2_lm_head_verify_workspace(int S, int k, int V, int K);
+
+/*
+ * The vocabulary head of the K+1-row verify followed by the p/q verify over its logits, with
+ * the GEMM's epilogue fused with the verify's softmax statistics ("Optimizing DeepSeek-V4-Flash
+ * ...", page 2, verifier-bottleneck reply: the verify runs "the vocabulary head" over the K+1
+ * rows; post #1 paragraph after the analyzer output: "fusing several operations ... reducing
+ * intermediate memory traffic").
+ *   target_logits[s][i][:] = A[s*(k+1) + i] W^T   (as q2_tiny_gemm, N = V), written to the
+ *                 caller's fp32 [S][k+1][V] buffer (16-byte aligned), then
+ *   the verify of pq_verify_ex (temperatures non-NULL: device fp32 [S], 0 = greedy) or of
+ *   pq_verify (temperatures NULL: one temperature > 0 for every session) over those logits.
+ *   W Q2B32 [V rows][K], A bf16 [S*(k+1)][lda]; 1 <= S*(k+1) <= 64; alignment, K and the
+ *   verify's other arguments as for q2_tiny_gemm and pq_verify.
+ * When 17 <= S*(k+1) <= 64, K % 128 == 0 and V > 4096, the tcgen05 GEMM's epilogue also writes
+ * each target row's (max, sum of exponentials) partial per 128-token tile, so the verify's
+ * statistics pass reads only the draft logits; otherwise the same kernels run unfused.  The
+ * results are those of q2_tiny_gemm followed by pq_verify(_ex) up to floating-point summation
+ * order.  Device errors: those of both calls, in one status word.
+ */
+q2_status q2_lm_head_verify(const void *W, int V, int K, const uint16_t *A, int lda,
+                            const float *draft_logits, const int32_t *draft_tokens,
+                            const float *u_acc, const float *u_fin, int S, int k,
+                            const float *temperatures, float temperature, float *target_logits,
+                            int32_t *n_accepted, int32_t *out_tokens, float *probs_out, void *ws,
+                            size_t ws_bytes, q2_stream_t stream);
+
 /* ------------------------------------------------------------------ yield quench (host) */
 
 /* Per-session state of the terminal yield-quench controller ("ds4-on-spark" README, "The

@@ -68,16 +68,21 @@ struct PqCarve {
     size_t bytes;
 };
 
-PqCarve pq_carve(void *ws, int S, int k, int V) {
-    Carver c(ws);
+PqCarve pq_carve_from(Carver &c, int S, int k, int V) {
+    const size_t off0 = c.off;
     PqCarve r{};
     const size_t R = 2 * (size_t)k + 1, C = pq_cmax(V);
     r.stats = static_cast<float *>(c.take((size_t)S * R * C * 2 * sizeof(float)));
     r.mass = static_cast<float *>(c.take((size_t)S * C * kSegsPerChunk * sizeof(float)));
     r.pmass = static_cast<float *>(c.take((size_t)S * C * kSegsPerChunk * sizeof(float)));
     r.tickets = static_cast<unsigned int *>(c.take((size_t)S * sizeof(unsigned int)));
-    r.bytes = c.off;
+    r.bytes = c.off - off0 + Q2_WORKSPACE_HEADER_BYTES;  // as a workspace of its own
     return r;
+}
+
+PqCarve pq_carve(void *ws, int S, int k, int V) {
+    Carver c(ws);
+    return pq_carve_from(c, S, k, V);
 }
 
 // ---------------------------------------------------------------- MoE sizes
@@ -134,6 +139,13 @@ q2_status pq_verify_impl(const float *target_logits, const float *draft_logits, 
                          const float *u_acc, const float *u_fin, int S, int k, int V, float temperature,
                          const float *temps, int32_t *n_accepted, int32_t *out_tokens, float *probs_out, void *ws,
                          size_t ws_bytes, q2_stream_t stream);
+q2_status pq_check_args(const float *target_logits, const float *draft_logits, const int32_t *draft_tokens,
+                        const float *u_acc, const float *u_fin, int S, int k, int V, int32_t *n_accepted,
+                        int32_t *out_tokens, float *probs_out);
+void pq_setup(PqArgs &a, PqSplit &sp, Carver &c, const float *target_logits, const float *draft_logits,
+              const int32_t *draft_tokens, const float *u_acc, const float *u_fin, int S, int k, int V,
+              float temperature, const float *temps, int32_t *n_accepted, int32_t *out_tokens, float *probs_out,
+              unsigned int *status, int sms);
 }  // namespace
 
 extern "C" {
@@ -201,7 +213,7 @@ q2_status q2_tiny_gemm(const void *W, int N, int K, const uint16_t *A, int M, in
         if (launch_prep_umma(A, lda, M, K, img, s) != cudaSuccess) return Q2_ERR_CUDA;
         const int sms = device_sms();
         return cuda_status(probed(kProbeGemm, s, [&] {
-            return launch_gemm_umma(W, N, K, M, img, Y, ldy, status_word(ws), sms, s);
+            return launch_gemm_umma(W, N, K, M, img, Y, ldy, status_word(ws), sms, s, UmFuse{});
         }));
     }
     const PrepLayout L(K);
@@ -267,6 +279,85 @@ q2_status pq_verify(const float *target_logits, const float *draft_logits, const
                           n_accepted, out_tokens, probs_out, ws, ws_bytes, stream);
 }
 
+// ---------------------------------------------------------------- fused vocabulary head + verify
+
+size_t q2_lm_head_verify_workspace(int S, int k, int V, int K) {
+    const long long M = (long long)S * (k + 1);
+    if (S < 1 || k < 0 || k > kMaxDrafts || V < 1 || V > (1 << 28) || M > 64 || !gemm_k_ok(K))
+        return Q2_WORKSPACE_HEADER_BYTES;
+    const bool umma = umma_gemm_supported((int)M, K);
+    const bool fused = umma && V > kWarpTierMaxV;
+    Carver c(nullptr);
+    c.take(umma ? umma_gemm_ws_bytes((int)M, K) : PrepLayout(K).bytes((int)M));
+    if (fused) c.take((size_t)M * cdiv(V, 128) * sizeof(float2));
+    if (V > kWarpTierMaxV) pq_carve_from(c, S, k, V);
+    return c.off;
+}
+
+q2_status q2_lm_head_verify(const void *W, int V, int K, const uint16_t *A, int lda, const float *draft_logits,
+                            const int32_t *draft_tokens, const float *u_acc, const float *u_fin, int S, int k,
+                            const float *temperatures, float temperature, float *target_logits,
+                            int32_t *n_accepted, int32_t *out_tokens, float *probs_out, void *ws, size_t ws_bytes,
+                            q2_stream_t stream) {
+    if (!W || !A || K < kBlockK || K % kBlockK != 0 || lda < K) return Q2_ERR_INVALID_ARG;
+    if (!temperatures && (!(temperature > 0.0f) || !isfinite(temperature))) return Q2_ERR_INVALID_ARG;
+    const q2_status ast = pq_check_args(target_logits, draft_logits, draft_tokens, u_acc, u_fin, S, k, V,
+                                        n_accepted, out_tokens, probs_out);
+    if (ast != Q2_OK) return ast;
+    const long long M = (long long)S * (k + 1);
+    if (M > 64 || !gemm_k_ok(K)) return Q2_ERR_UNSUPPORTED;
+    if (!aligned(W, 16) || !aligned(A, 16) || lda % 8 != 0 || (temperatures && !aligned(temperatures, 4)))
+        return Q2_ERR_ALIGNMENT;
+    const q2_status wst = check_ws(ws, ws_bytes, q2_lm_head_verify_workspace(S, k, V, K));
+    if (wst != Q2_OK) return wst;
+    cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
+    const int sms = device_sms();
+    unsigned int *status = status_word(ws);
+    const bool umma = umma_gemm_supported((int)M, K);
+    const bool fused = umma && V > kWarpTierMaxV;
+    Carver c(ws);
+    // 1. target logits = A W^T (rows s*(k+1) + i), with the target rows' softmax partials
+    //    taken in the tcgen05 epilogue when fused
+    cudaError_t e;
+    float *tstats = nullptr;
+    const int Ct = cdiv(V, 128);
+    if (umma) {
+        void *img = c.take(umma_gemm_ws_bytes((int)M, K));
+        if (fused) tstats = static_cast<float *>(c.take((size_t)M * Ct * sizeof(float2)));
+        e = launch_prep_umma(A, lda, (int)M, K, img, s);
+        if (e != cudaSuccess) return Q2_ERR_CUDA;
+        UmFuse fz{};
+        if (fused) {
+            fz.tstats = tstats;
+            fz.temps = temperatures;
+            fz.beta = temperatures ? 0.0f : (float)(1.4426950408889634 / (double)temperature);
+            fz.k1 = k + 1;
+        }
+        e = probed(kProbeGemm, s, [&] {
+            return launch_gemm_umma(W, V, K, (int)M, img, target_logits, V, status, sms, s, fz);
+        });
+    } else {
+        const PrepLayout L(K);
+        const PrepPtrs P = PrepPtrs::carve(c.take(L.bytes((int)M)), L, (int)M);
+        e = launch_prep_bf16(A, lda, nullptr, (int)M, K, P, L, s);
+        if (e != cudaSuccess) return Q2_ERR_CUDA;
+        e = probed(kProbeGemm, s, [&] {
+            return launch_gemm_small(W, V, K, P, L, (int)M, target_logits, V, status, s);
+        });
+    }
+    if (e != cudaSuccess) return Q2_ERR_CUDA;
+    // 2. the verify over those logits
+    PqArgs a;
+    PqSplit sp;
+    pq_setup(a, sp, c, target_logits, draft_logits, draft_tokens, u_acc, u_fin, S, k, V,
+             temperatures ? 1.0f : temperature, temperatures, n_accepted, out_tokens, probs_out, status, sms);
+    if (fused) {
+        sp.tstats = tstats;
+        sp.Ct = Ct;
+    }
+    return cuda_status(launch_pq_verify(a, sp, V <= kWarpTierMaxV, sms, s));
+}
+
 q2_status pq_verify_ex(const float *target_logits, const float *draft_logits, const int32_t *draft_tokens,
                        const float *u_acc, const float *u_fin, int S, int k, int V, const float *temperatures,
                        int32_t *n_accepted, int32_t *out_tokens, float *probs_out, void *ws, size_t ws_bytes,
@@ -280,10 +371,11 @@ q2_status pq_verify_ex(const float *target_logits, const float *draft_logits, co
 }  // extern "C"
 
 namespace {
-q2_status pq_verify_impl(const float *target_logits, const float *draft_logits, const int32_t *draft_tokens,
-                         const float *u_acc, const float *u_fin, int S, int k, int V, float temperature,
-                         const float *temps, int32_t *n_accepted, int32_t *out_tokens, float *probs_out, void *ws,
-                         size_t ws_bytes, q2_stream_t stream) {
+// Checks of the verify's own arguments (shared by pq_verify, pq_verify_ex and the fused
+// vocabulary-head verify).
+q2_status pq_check_args(const float *target_logits, const float *draft_logits, const int32_t *draft_tokens,
+                        const float *u_acc, const float *u_fin, int S, int k, int V, int32_t *n_accepted,
+                        int32_t *out_tokens, float *probs_out) {
     if (S < 1 || k < 0 || V < 1 || !target_logits || !u_fin || !n_accepted || !out_tokens)
         return Q2_ERR_INVALID_ARG;
     if (k > 0 && (!draft_logits || !draft_tokens || !u_acc)) return Q2_ERR_INVALID_ARG;
@@ -292,12 +384,15 @@ q2_status pq_verify_impl(const float *target_logits, const float *draft_logits, 
         !aligned(u_acc, 4) || !aligned(u_fin, 4) || !aligned(n_accepted, 4) || !aligned(out_tokens, 4) ||
         !aligned(probs_out, 4))
         return Q2_ERR_ALIGNMENT;
-    const bool warp_tier = V <= kWarpTierMaxV;
-    if (!warp_tier && S > 65535) return Q2_ERR_UNSUPPORTED;  // sessions map to grid.y
-    const size_t need = warp_tier ? (size_t)Q2_WORKSPACE_HEADER_BYTES : pq_carve(nullptr, S, k, V).bytes;
-    const q2_status wst = check_ws(ws, ws_bytes, need);
-    if (wst != Q2_OK) return wst;
-    PqArgs a;
+    if (V > kWarpTierMaxV && S > 65535) return Q2_ERR_UNSUPPORTED;  // sessions map to grid.y
+    return Q2_OK;
+}
+
+// Fill the verify's launch arguments; the split tier's scratch continues the carve c.
+void pq_setup(PqArgs &a, PqSplit &sp, Carver &c, const float *target_logits, const float *draft_logits,
+              const int32_t *draft_tokens, const float *u_acc, const float *u_fin, int S, int k, int V,
+              float temperature, const float *temps, int32_t *n_accepted, int32_t *out_tokens, float *probs_out,
+              unsigned int *status, int sms) {
     a.target = target_logits;
     a.draft = draft_logits;
     a.drafts = draft_tokens;
@@ -309,11 +404,10 @@ q2_status pq_verify_impl(const float *target_logits, const float *draft_logits, 
     a.n_acc = n_accepted;
     a.tokens = out_tokens;
     a.probs = probs_out;
-    a.status = status_word(ws);
-    PqSplit sp{};
-    const int sms = device_sms();
-    if (!warp_tier) {
-        const PqCarve pc = pq_carve(ws, S, k, V);
+    a.status = status;
+    sp = PqSplit{};
+    if (V > kWarpTierMaxV) {
+        const PqCarve pc = pq_carve_from(c, S, k, V);
         int C = std::max(1, std::min(cdiv(2 * sms, S), pq_cmax(V)));
         const int L = (int)align_up((size_t)cdiv(V, C), kChunkAlign);
         C = cdiv(V, L);
@@ -324,6 +418,25 @@ q2_status pq_verify_impl(const float *target_logits, const float *draft_logits, 
         sp.pmass = pc.pmass;
         sp.tickets = pc.tickets;
     }
+}
+
+q2_status pq_verify_impl(const float *target_logits, const float *draft_logits, const int32_t *draft_tokens,
+                         const float *u_acc, const float *u_fin, int S, int k, int V, float temperature,
+                         const float *temps, int32_t *n_accepted, int32_t *out_tokens, float *probs_out, void *ws,
+                         size_t ws_bytes, q2_stream_t stream) {
+    const q2_status ast = pq_check_args(target_logits, draft_logits, draft_tokens, u_acc, u_fin, S, k, V,
+                                        n_accepted, out_tokens, probs_out);
+    if (ast != Q2_OK) return ast;
+    const bool warp_tier = V <= kWarpTierMaxV;
+    const size_t need = warp_tier ? (size_t)Q2_WORKSPACE_HEADER_BYTES : pq_carve(nullptr, S, k, V).bytes;
+    const q2_status wst = check_ws(ws, ws_bytes, need);
+    if (wst != Q2_OK) return wst;
+    PqArgs a;
+    PqSplit sp;
+    const int sms = device_sms();
+    Carver c(ws);
+    pq_setup(a, sp, c, target_logits, draft_logits, draft_tokens, u_acc, u_fin, S, k, V, temperature, temps,
+             n_accepted, out_tokens, probs_out, status_word(ws), sms);
     return cuda_status(launch_pq_verify(a, sp, warp_tier, sms, reinterpret_cast<cudaStream_t>(stream)));
 }
 }  // namespace

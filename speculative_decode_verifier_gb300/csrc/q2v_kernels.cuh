@@ -44,6 +44,11 @@ struct PqSplit {
     float *mass;         // [S][C][8] draw mass of each warp segment of each chunk
     float *pmass;        // [S][C][8] p_j mass of each segment (zero-residual fallback)
     unsigned int *tickets;  // [S]
+    // Target rows' partials made elsewhere (the fused vocabulary-head GEMM), nullable:
+    // [S][k+1][Ct] float2, one per 128-token tile.  When set, the statistics kernel only
+    // streams the draft rows and the combine reads the target rows from here.
+    const float *tstats;
+    int Ct;
 };
 
 cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier, int num_sms, cudaStream_t st);
@@ -86,8 +91,19 @@ constexpr int kUmmaMinRowsExclusive = 16;
 bool umma_gemm_supported(int M, int K);
 size_t umma_gemm_ws_bytes(int M, int K);
 cudaError_t launch_prep_umma(const uint16_t *A, int lda, int M, int K, void *ws_region, cudaStream_t s);
+
+// Fusion of the vocabulary-head GEMM with the verify's softmax statistics: activation row m
+// is row m % k1 of session m / k1, and the epilogue writes, for every row and 128-token tile,
+// the (max, sum 2^((y - max) beta_s)) partial of the logits it stores (greedy sessions:
+// (max, first argmax as int bits)) to tstats [S][k1][Ct].  tstats null: a plain GEMM.
+struct UmFuse {
+    float *tstats;
+    const float *temps;  // [S] per-session temperatures (0 = greedy), nullable: beta for all
+    float beta;          // log2(e) / T when temps is null
+    int k1;              // rows per session (k + 1)
+};
 cudaError_t launch_gemm_umma(const void *W, int N, int K, int M, const void *ws_region, float *Y, int ldy,
-                             unsigned int *status, int num_sms, cudaStream_t s);
+                             unsigned int *status, int num_sms, cudaStream_t s, const UmFuse &fuse);
 
 // Measurement hook (q2_set_probe): records the caller's begin (end = 0) or end (end = 1)
 // event on s when `kernel` is the bracketed one; a no-op otherwise.

@@ -81,6 +81,11 @@ struct UmShared {
     uint32_t tmem_base;
     uint32_t abort_flag;
     int exps[64];
+    // fused verify statistics: per-column (activation row) beta and mode, and the epilogue
+    // warps' partials of the current tile
+    float col_beta[64];
+    int col_mode[64];
+    float2 part[kUmEpiWarps][64];
 };
 
 __host__ __device__ constexpr size_t um_smem_bytes(int npad) {
@@ -225,6 +230,15 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t *r) {
                  : "memory");
 }
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;\n" ::: "memory"); }
+__device__ __forceinline__ float um_ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ bool um_better_arg(float m2, int i2, float m1, int i1) {
+    return m2 > m1 || (m2 == m1 && i2 < i1);
+}
+
 __device__ __forceinline__ void tmem_wait_ld() { asm volatile("tcgen05.wait::ld.sync.aligned;\n" ::: "memory"); }
 
 // ---------------------------------------------------------------- activation prep
@@ -336,7 +350,7 @@ template <int NPAD>
 __global__ void __launch_bounds__(kUmThreads, 1)
     q2_gemm_umma_kernel(const __grid_constant__ CUtensorMap wmap, int N, int nst, const uint8_t *__restrict__ bimg,
                         const int *__restrict__ exps, int M, float *__restrict__ Y, int ldy,
-                        unsigned int *status) {
+                        unsigned int *status, UmFuse fz) {
     constexpr int kB = um_bstage(NPAD);
     extern __shared__ uint8_t um_smem_raw[];
     uint8_t *sm = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(um_smem_raw) + 1023) & ~uintptr_t(1023));
@@ -575,11 +589,27 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         }
         if (scale_mag_out_of_range(scale_max)) set_status(status, Q2_ERR_RANGE);
     } else {
-        // ---- epilogue: TMEM -> registers -> Y (warp w reads TMEM lanes 32w..32w+31)
+        // ---- epilogue: TMEM -> registers -> Y (warp w reads TMEM lanes 32w..32w+31), and when
+        // fused, each row's softmax (or argmax) partial over the tile's 128 tokens
         pdl_wait();
         pdl_trigger();
-        if (threadIdx.x < 64) sh->exps[threadIdx.x] = threadIdx.x < M ? exps[threadIdx.x] : 0;
+        if (threadIdx.x < 64) {
+            const int m = threadIdx.x;
+            sh->exps[m] = m < M ? exps[m] : 0;
+            if (fz.tstats && m < M) {
+                const float T = fz.temps ? fz.temps[m / fz.k1] : 0.0f;
+                int mode = 1;
+                float beta = fz.beta;
+                if (fz.temps) {
+                    mode = (T == 0.0f) ? 0 : ((T > 0.0f && T < INFINITY) ? 1 : -1);
+                    beta = mode == 1 ? (float)(1.4426950408889634 / (double)T) : 0.0f;
+                }
+                sh->col_mode[m] = mode;
+                sh->col_beta[m] = beta;
+            }
+        }
         asm volatile("bar.sync 1, %0;\n" ::"n"(kUmEpiWarps * 32) : "memory");
+        const int ntiles_all = cdiv(N, kUmRows);
         for (int q = 0; q < ngroups; ++q) {
             const int t0 = q * kUmGroup, tn = min(kUmGroup, my_tiles - t0);
             const uint32_t buf = (uint32_t)q & 1u;
@@ -592,11 +622,69 @@ __global__ void __launch_bounds__(kUmThreads, 1)
                 for (int c = 0; c < NPAD / 16; ++c)
                     tmem_ld16(tmem + ((uint32_t)(warp * 32) << 16) + col + (uint32_t)(c * 16), v + 16 * c);
                 tmem_wait_ld();
-                const int n = ((int)blockIdx.x + (t0 + t) * (int)gridDim.x) * kUmRows + warp * 32 + lane;
+                const int tile = (int)blockIdx.x + (t0 + t) * (int)gridDim.x;
+                const int n = tile * kUmRows + warp * 32 + lane;
+#pragma unroll
+                for (int m = 0; m < NPAD; ++m) v[m] = ldexpf(v[m], sh->exps[m]);
                 if (n < N) {
 #pragma unroll
                     for (int m = 0; m < NPAD; ++m)
-                        if (m < M) Y[(size_t)m * ldy + n] = ldexpf(v[m], sh->exps[m]);
+                        if (m < M) Y[(size_t)m * ldy + n] = v[m];
+                }
+                if (fz.tstats) {
+#pragma unroll
+                    for (int m = 0; m < NPAD; ++m) {
+                        if (m >= M) continue;
+                        const int mode = sh->col_mode[m];
+                        const float y = n < N ? v[m] : -INFINITY;
+                        if (mode == 1) {
+                            const float beta = sh->col_beta[m];
+                            float mx = y;
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+                            float z = (y > -INFINITY) ? um_ex2((y - mx) * beta) : 0.0f;
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+                            if (lane == 0) sh->part[warp][m] = make_float2(mx, z);
+                        } else if (mode == 0) {
+                            float mx = y;
+                            int ix = n < N ? n : 0x7FFFFFFF;
+#pragma unroll
+                            for (int o = 16; o > 0; o >>= 1) {
+                                const float m2 = __shfl_xor_sync(0xffffffffu, mx, o);
+                                const int i2 = __shfl_xor_sync(0xffffffffu, ix, o);
+                                if (um_better_arg(m2, i2, mx, ix)) {
+                                    mx = m2;
+                                    ix = i2;
+                                }
+                            }
+                            if (lane == 0) sh->part[warp][m] = make_float2(mx, __int_as_float(ix));
+                        }
+                    }
+                    asm volatile("bar.sync 1, %0;\n" ::"n"(kUmEpiWarps * 32) : "memory");
+                    if (threadIdx.x < M) {
+                        const int m = threadIdx.x, mode = sh->col_mode[m];
+                        float2 r = sh->part[0][m];
+                        if (mode == 1) {
+                            const float beta = sh->col_beta[m];
+                            float mx = r.x;
+                            for (int w = 1; w < kUmEpiWarps; ++w) mx = fmaxf(mx, sh->part[w][m].x);
+                            float z = 0.0f;
+                            for (int w = 0; w < kUmEpiWarps; ++w) {
+                                const float2 pw = sh->part[w][m];
+                                if (pw.x > -INFINITY) z += pw.y * um_ex2((pw.x - mx) * beta);
+                            }
+                            r = make_float2(mx, z);
+                        } else if (mode == 0) {
+                            for (int w = 1; w < kUmEpiWarps; ++w) {
+                                const float2 pw = sh->part[w][m];
+                                if (um_better_arg(pw.x, __float_as_int(pw.y), r.x, __float_as_int(r.y))) r = pw;
+                            }
+                        }
+                        if (mode >= 0)
+                            reinterpret_cast<float2 *>(fz.tstats)[(size_t)m * ntiles_all + tile] = r;
+                    }
+                    asm volatile("bar.sync 1, %0;\n" ::"n"(kUmEpiWarps * 32) : "memory");
                 }
             }
             tc_fence_before();
@@ -639,7 +727,8 @@ size_t g_umma_smem[4];  // dynamic shared memory each NPAD variant was configure
 
 template <int NPAD>
 cudaError_t launch_umma_variant(const CUtensorMap &map, int N, int nst, const uint8_t *img, const int *exps, int M,
-                                float *Y, int ldy, unsigned int *status, int num_sms, cudaStream_t s) {
+                                float *Y, int ldy, unsigned int *status, int num_sms, cudaStream_t s,
+                                const UmFuse &fz) {
     auto kern = q2_gemm_umma_kernel<NPAD>;
     const size_t smem = um_smem_bytes(NPAD);
     size_t &have = g_umma_smem[NPAD / 16 - 1];
@@ -658,7 +747,7 @@ cudaError_t launch_umma_variant(const CUtensorMap &map, int N, int nst, const ui
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, kern, map, N, nst, img, exps, M, Y, ldy, status);
+    return cudaLaunchKernelEx(&cfg, kern, map, N, nst, img, exps, M, Y, ldy, status, fz);
 }
 
 }  // namespace
@@ -682,7 +771,7 @@ cudaError_t launch_prep_umma(const uint16_t *A, int lda, int M, int K, void *ws_
 }
 
 cudaError_t launch_gemm_umma(const void *W, int N, int K, int M, const void *ws_region, float *Y, int ldy,
-                             unsigned int *status, int num_sms, cudaStream_t s) {
+                             unsigned int *status, int num_sms, cudaStream_t s, const UmFuse &fz) {
     const EncodeTiledFn encode = encode_tiled();
     if (!encode) return cudaErrorNotSupported;
     const int nb = K / kBlockK;
@@ -702,10 +791,10 @@ cudaError_t launch_gemm_umma(const void *W, int N, int K, int M, const void *ws_
                CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return cudaErrorInvalidValue;
     switch (npad) {
-        case 16: return launch_umma_variant<16>(map, N, nst, img, exps, M, Y, ldy, status, num_sms, s);
-        case 32: return launch_umma_variant<32>(map, N, nst, img, exps, M, Y, ldy, status, num_sms, s);
-        case 48: return launch_umma_variant<48>(map, N, nst, img, exps, M, Y, ldy, status, num_sms, s);
-        default: return launch_umma_variant<64>(map, N, nst, img, exps, M, Y, ldy, status, num_sms, s);
+        case 16: return launch_umma_variant<16>(map, N, nst, img, exps, M, Y, ldy, status, num_sms, s, fz);
+        case 32: return launch_umma_variant<32>(map, N, nst, img, exps, M, Y, ldy, status, num_sms, s, fz);
+        case 48: return launch_umma_variant<48>(map, N, nst, img, exps, M, Y, ldy, status, num_sms, s, fz);
+        default: return launch_umma_variant<64>(map, N, nst, img, exps, M, Y, ldy, status, num_sms, s, fz);
     }
 }
 

@@ -343,7 +343,7 @@ __global__ void __launch_bounds__(512) pqv_stats_kernel(PqArgs a, PqSplit sp) {
     if (smode == 0) {
         // greedy: (max, first index of it) of every row's chunk; the index travels as the
         // bits of the partial's second float
-        for (int r = warp; r < R; r += nwarps) {
+        for (int r = (sp.tstats ? a.k + 1 : 0) + warp; r < R; r += nwarps) {
             float m;
             int i;
             lane_argmax(row_ptr(a, s, r), c0, c1, lane, m, i);
@@ -353,7 +353,7 @@ __global__ void __launch_bounds__(512) pqv_stats_kernel(PqArgs a, PqSplit sp) {
         }
         return;
     }
-    for (int r = warp; r < R; r += nwarps) {
+    for (int r = (sp.tstats ? a.k + 1 : 0) + warp; r < R; r += nwarps) {
         const float *x = row_ptr(a, s, r);
         float m = -INFINITY, z = 0.0f;
         if (VEC) {
@@ -401,6 +401,17 @@ __global__ void __launch_bounds__(512) pqv_stats_kernel(PqArgs a, PqSplit sp) {
     }
 }
 
+// The chunk partials of row r of session s and their count: the target rows' from the fused
+// GEMM when it made them, else the statistics kernel's.
+__device__ __forceinline__ const float2 *row_partials(const PqArgs &a, const PqSplit &sp, int s, int r, int &n) {
+    if (sp.tstats && r <= a.k) {
+        n = sp.Ct;
+        return reinterpret_cast<const float2 *>(sp.tstats) + ((size_t)s * (a.k + 1) + r) * sp.Ct;
+    }
+    n = sp.C;
+    return reinterpret_cast<const float2 *>(sp.stats) + ((size_t)s * (2 * a.k + 1) + r) * sp.C;
+}
+
 // Kernel 2: combine, accept scan, per-warp chunk masses, last-arriver inverse-CDF search.
 //
 // Each chunk of L tokens is cut into 8 contiguous warp segments; warp w of the CTA owns
@@ -440,8 +451,9 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
             float m = -INFINITY;
             int i = 0x7FFFFFFF;
             if (r < R) {
-                const float2 *st = reinterpret_cast<const float2 *>(sp.stats) + ((size_t)s * R + r) * sp.C;
-                for (int cc = sub; cc < sp.C; cc += 16) {
+                int nc;
+                const float2 *st = row_partials(a, sp, s, r, nc);
+                for (int cc = sub; cc < nc; cc += 16) {
                     const float2 w = st[cc];
                     const int wi = __float_as_int(w.y);
                     if (better_arg(w.x, wi, m, i)) {
@@ -482,26 +494,27 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
         const int r = r0 + (tid >> 4), sub = tid & 15;
         float2 v[8];
         float m = -INFINITY;
-        const float2 *st = reinterpret_cast<const float2 *>(sp.stats) + ((size_t)s * R + min(r, R - 1)) * sp.C;
-        if (sp.C <= 16 * 8) {
+        int nc;
+        const float2 *st = row_partials(a, sp, s, min(r, R - 1), nc);
+        if (nc <= 16 * 8) {
 #pragma unroll
             for (int u = 0; u < 8; ++u) {
                 const int cc = sub + 16 * u;
-                v[u] = (r < R && cc < sp.C) ? st[cc] : make_float2(-INFINITY, 0.0f);
+                v[u] = (r < R && cc < nc) ? st[cc] : make_float2(-INFINITY, 0.0f);
                 m = fmaxf(m, v[u].x);
             }
         } else {
-            for (int cc = sub; r < R && cc < sp.C; cc += 16) m = fmaxf(m, st[cc].x);
+            for (int cc = sub; r < R && cc < nc; cc += 16) m = fmaxf(m, st[cc].x);
         }
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         float z = 0.0f;
-        if (sp.C <= 16 * 8) {
+        if (nc <= 16 * 8) {
 #pragma unroll
             for (int u = 0; u < 8; ++u)
                 if (v[u].x > -INFINITY) z += v[u].y * ex2((v[u].x - m) * beta);
         } else {
-            for (int cc = sub; r < R && cc < sp.C; cc += 16) {
+            for (int cc = sub; r < R && cc < nc; cc += 16) {
                 const float2 w = st[cc];
                 if (w.x > -INFINITY) z += w.y * ex2((w.x - m) * beta);
             }

@@ -23,7 +23,8 @@ STATUS_NAMES = {0: "Q2_OK", 1: "Q2_ERR_INVALID_ARG", 2: "Q2_ERR_ALIGNMENT", 3: "
 MOE_RENORMALIZE = 1
 EXPORTS = ("q2_tiny_gemm_workspace", "q2_tiny_gemm", "q2_moe_grouped_workspace", "q2_moe_grouped",
            "pq_verify_workspace", "pq_verify", "pq_verify_noalloc", "q2_get_device_status", "q2_status_string",
-           "q2_version", "q2_set_probe", "pq_verify_ex", "q2_quench_init", "q2_quench_update")
+           "q2_version", "q2_set_probe", "pq_verify_ex", "q2_quench_init", "q2_quench_update",
+           "q2_lm_head_verify_workspace", "q2_lm_head_verify")
 
 # kernels that q2_set_probe can bracket (q2_probe_kernel)
 PROBE_NONE, PROBE_MOE_GATE_UP, PROBE_MOE_DOWN, PROBE_GEMM, PROBE_PQ_STATS, PROBE_PQ_VERIFY = range(6)
@@ -70,6 +71,10 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q2_status_string.argtypes = [I]
     lib.q2_status_string.restype = ctypes.c_char_p
     lib.q2_version.restype = I
+    lib.q2_lm_head_verify_workspace.argtypes = [I, I, I, I]
+    lib.q2_lm_head_verify_workspace.restype = Z
+    lib.q2_lm_head_verify.argtypes = [P, I, I, P, I, P, P, P, P, I, I, P, F, P, P, P, P, P, Z, P]
+    lib.q2_lm_head_verify.restype = I
     lib.q2_quench_init.argtypes = [P, I]
     lib.q2_quench_init.restype = I
     lib.q2_quench_update.argtypes = [P, I, P, ctypes.c_double, ctypes.c_double]
@@ -312,6 +317,51 @@ def pq_verify_ex(target: torch.Tensor, draft: torch.Tensor | None, drafts: torch
                              ctypes.c_void_p(_stream(stream)))
     _raise(st, "pq_verify_ex")
     return n_acc, tokens
+
+
+def q2_lm_head_verify_workspace(S: int, k: int, V: int, K: int) -> int:
+    return load().q2_lm_head_verify_workspace(S, k, V, K)
+
+
+def q2_lm_head_verify(W: torch.Tensor, V: int, K: int, A: torch.Tensor, draft: torch.Tensor | None,
+                      drafts: torch.Tensor | None, u_acc: torch.Tensor | None, u_fin: torch.Tensor,
+                      S: int, k: int, temperatures: torch.Tensor | None = None, temperature: float = 1.0,
+                      target: torch.Tensor | None = None, n_acc: torch.Tensor | None = None,
+                      tokens: torch.Tensor | None = None, probs: torch.Tensor | None = None,
+                      ws: torch.Tensor | None = None, stream=None):
+    """Vocabulary head + verify: target = A W^T as [S, k+1, V] fp32, then the p/q verify over it
+    (temperatures: fp32 [S] on the device, 0 = greedy; else one temperature).  Returns
+    (target, n_acc, tokens)."""
+    _check(W, "W", torch.uint8)
+    if A.dtype == torch.bfloat16:
+        A = A.view(torch.int16)
+    _check(A, "A", torch.int16)
+    if k > 0:
+        _check(draft, "draft", torch.float32)
+        _check(drafts, "drafts", torch.int32)
+        _check(u_acc, "u_acc", torch.float32)
+    _check(u_fin, "u_fin", torch.float32)
+    _check(temperatures, "temperatures", torch.float32, nullable=True)
+    dev = A.device
+    if target is None:
+        target = torch.empty((S, k + 1, V), dtype=torch.float32, device=dev)
+    if n_acc is None:
+        n_acc = torch.empty(S, dtype=torch.int32, device=dev)
+    if tokens is None:
+        tokens = torch.empty((S, k + 1), dtype=torch.int32, device=dev)
+    for t, n in ((target, "target"),):
+        _check(t, n, torch.float32)
+    _check(n_acc, "n_acc", torch.int32)
+    _check(tokens, "tokens", torch.int32)
+    _check(probs, "probs", torch.float32, nullable=True)
+    if ws is None:
+        ws = workspace(q2_lm_head_verify_workspace(S, k, V, K), dev)
+    st = load().q2_lm_head_verify(_ptr(W), V, K, _ptr(A), A.shape[1], _ptr(draft) if k > 0 else None,
+                                  _ptr(drafts) if k > 0 else None, _ptr(u_acc) if k > 0 else None, _ptr(u_fin),
+                                  S, k, _ptr(temperatures), float(temperature), _ptr(target), _ptr(n_acc),
+                                  _ptr(tokens), _ptr(probs), _ptr(ws), ws.numel(), ctypes.c_void_p(_stream(stream)))
+    _raise(st, "q2_lm_head_verify")
+    return target, n_acc, tokens
 
 
 def pq_verify_noalloc(target: torch.Tensor, draft: torch.Tensor | None, drafts: torch.Tensor | None,
