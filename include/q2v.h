@@ -215,7 +215,7 @@ q2_status pq_verify_noalloc(const float *target_logits, const float *draft_logit
 
 /* ------------------------------------------------------------------ vocabulary head + verify */
 
-/* Workspace bytes for q2_lm_head_verify with these sizes. */
+/* Workspace bytes for q2_lm_head_verify with these sizes (either choice of flags). */
 size_t q2_lm_head_verify_workspace(int S, int k, int V, int K);
 
 /*
@@ -230,18 +230,22 @@ size_t q2_lm_head_verify_workspace(int S, int k, int V, int K);
  *   pq_verify (temperatures NULL: one temperature > 0 for every session) over those logits.
  *   W Q2B32 [V rows][K], A bf16 [S*(k+1)][lda]; 1 <= S*(k+1) <= 64; alignment, K and the
  *   verify's other arguments as for q2_tiny_gemm and pq_verify.
- * When 17 <= S*(k+1) <= 64, K % 128 == 0 and V > 4096, the tcgen05 GEMM's epilogue also writes
- * each target row's (max, sum of exponentials) partial per 128-token tile, so the verify's
- * statistics pass reads only the draft logits; otherwise the same kernels run unfused.  The
+ * flags: Q2_LM_HEAD_FUSE_STATS -- when 17 <= S*(k+1) <= 64, K % 128 == 0 and V > 4096, the
+ * tcgen05 GEMM's epilogue also reduces each target row's logits to (max, sum of exponentials)
+ * partials, one per CTA, and the verify's statistics pass then reads only the draft logits.
+ * Without the flag (the faster choice on GB300, where the statistics pass over the just-written,
+ * L2-resident logits costs less than the epilogue's cross-lane reductions) the same kernels run
+ * unfused.  The
  * results are those of q2_tiny_gemm followed by pq_verify(_ex) up to floating-point summation
  * order.  Device errors: those of both calls, in one status word.
  */
+#define Q2_LM_HEAD_FUSE_STATS 1u
 q2_status q2_lm_head_verify(const void *W, int V, int K, const uint16_t *A, int lda,
                             const float *draft_logits, const int32_t *draft_tokens,
                             const float *u_acc, const float *u_fin, int S, int k,
-                            const float *temperatures, float temperature, float *target_logits,
-                            int32_t *n_accepted, int32_t *out_tokens, float *probs_out, void *ws,
-                            size_t ws_bytes, q2_stream_t stream);
+                            const float *temperatures, float temperature, unsigned flags,
+                            float *target_logits, int32_t *n_accepted, int32_t *out_tokens,
+                            float *probs_out, void *ws, size_t ws_bytes, q2_stream_t stream);
 
 /* ------------------------------------------------------------------ yield quench (host) */
 

@@ -286,17 +286,16 @@ size_t q2_lm_head_verify_workspace(int S, int k, int V, int K) {
     if (S < 1 || k < 0 || k > kMaxDrafts || V < 1 || V > (1 << 28) || M > 64 || !gemm_k_ok(K))
         return Q2_WORKSPACE_HEADER_BYTES;
     const bool umma = umma_gemm_supported((int)M, K);
-    const bool fused = umma && V > kWarpTierMaxV;
     Carver c(nullptr);
     c.take(umma ? umma_gemm_ws_bytes((int)M, K) : PrepLayout(K).bytes((int)M));
-    if (fused) c.take((size_t)M * cdiv(V, 128) * sizeof(float2));
+    if (umma) c.take((size_t)M * umma_gemm_grid(V, device_sms()) * sizeof(float2));
     if (V > kWarpTierMaxV) pq_carve_from(c, S, k, V);
     return c.off;
 }
 
 q2_status q2_lm_head_verify(const void *W, int V, int K, const uint16_t *A, int lda, const float *draft_logits,
                             const int32_t *draft_tokens, const float *u_acc, const float *u_fin, int S, int k,
-                            const float *temperatures, float temperature, float *target_logits,
+                            const float *temperatures, float temperature, unsigned flags, float *target_logits,
                             int32_t *n_accepted, int32_t *out_tokens, float *probs_out, void *ws, size_t ws_bytes,
                             q2_stream_t stream) {
     if (!W || !A || K < kBlockK || K % kBlockK != 0 || lda < K) return Q2_ERR_INVALID_ARG;
@@ -313,17 +312,20 @@ q2_status q2_lm_head_verify(const void *W, int V, int K, const uint16_t *A, int 
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     const int sms = device_sms();
     unsigned int *status = status_word(ws);
+    if (flags & ~Q2_LM_HEAD_FUSE_STATS) return Q2_ERR_INVALID_ARG;
     const bool umma = umma_gemm_supported((int)M, K);
-    const bool fused = umma && V > kWarpTierMaxV;
+    const bool fused = (flags & Q2_LM_HEAD_FUSE_STATS) && umma && V > kWarpTierMaxV;
     Carver c(ws);
     // 1. target logits = A W^T (rows s*(k+1) + i), with the target rows' softmax partials
     //    taken in the tcgen05 epilogue when fused
     cudaError_t e;
     float *tstats = nullptr;
-    const int Ct = cdiv(V, 128);
+    const int Ct = umma_gemm_grid(V, sms);
     if (umma) {
         void *img = c.take(umma_gemm_ws_bytes((int)M, K));
-        if (fused) tstats = static_cast<float *>(c.take((size_t)M * Ct * sizeof(float2)));
+        // the partials region is carved either way, so the workspace size does not depend on flags
+        float *tregion = static_cast<float *>(c.take((size_t)M * Ct * sizeof(float2)));
+        if (fused) tstats = tregion;
         e = launch_prep_umma(A, lda, (int)M, K, img, s);
         if (e != cudaSuccess) return Q2_ERR_CUDA;
         UmFuse fz{};

@@ -93,9 +93,10 @@ size_t umma_gemm_ws_bytes(int M, int K);
 cudaError_t launch_prep_umma(const uint16_t *A, int lda, int M, int K, void *ws_region, cudaStream_t s);
 
 // Fusion of the vocabulary-head GEMM with the verify's softmax statistics: activation row m
-// is row m % k1 of session m / k1, and the epilogue writes, for every row and 128-token tile,
-// the (max, sum 2^((y - max) beta_s)) partial of the logits it stores (greedy sessions:
-// (max, first argmax as int bits)) to tstats [S][k1][Ct].  tstats null: a plain GEMM.
+// is row m % k1 of session m / k1; the epilogue merges, over the 128-token tiles its CTA
+// computes, each row's (max, sum 2^((y - max) beta_s)) partial of the logits it stores
+// (greedy sessions: (max, first argmax as int bits)) and writes one partial per row per CTA
+// to tstats [S][k1][grid].  tstats null: a plain GEMM.
 struct UmFuse {
     float *tstats;
     const float *temps;  // [S] per-session temperatures (0 = greedy), nullable: beta for all
@@ -104,6 +105,9 @@ struct UmFuse {
 };
 cudaError_t launch_gemm_umma(const void *W, int N, int K, int M, const void *ws_region, float *Y, int ldy,
                              unsigned int *status, int num_sms, cudaStream_t s, const UmFuse &fuse);
+// The tcgen05 GEMM's grid (one persistent CTA per SM, at most one per 128-row tile); the fused
+// statistics are one partial per CTA.
+inline int umma_gemm_grid(int N, int num_sms) { return N < 1 ? 1 : (cdiv(N, 128) < num_sms ? cdiv(N, 128) : num_sms); }
 
 // Measurement hook (q2_set_probe): records the caller's begin (end = 0) or end (end = 1)
 // event on s when `kernel` is the bracketed one; a no-op otherwise.

@@ -86,6 +86,7 @@ struct UmShared {
     float col_beta[64];
     int col_mode[64];
     float2 part[kUmEpiWarps][64];
+    float2 run[64];  // this CTA's running partial of each row over its tiles
 };
 
 __host__ __device__ constexpr size_t um_smem_bytes(int npad) {
@@ -606,10 +607,10 @@ __global__ void __launch_bounds__(kUmThreads, 1)
                 }
                 sh->col_mode[m] = mode;
                 sh->col_beta[m] = beta;
+                sh->run[m] = make_float2(-INFINITY, mode == 0 ? __int_as_float(0x7FFFFFFF) : 0.0f);
             }
         }
         asm volatile("bar.sync 1, %0;\n" ::"n"(kUmEpiWarps * 32) : "memory");
-        const int ntiles_all = cdiv(N, kUmRows);
         for (int q = 0; q < ngroups; ++q) {
             const int t0 = q * kUmGroup, tn = min(kUmGroup, my_tiles - t0);
             const uint32_t buf = (uint32_t)q & 1u;
@@ -632,57 +633,73 @@ __global__ void __launch_bounds__(kUmThreads, 1)
                         if (m < M) Y[(size_t)m * ldy + n] = v[m];
                 }
                 if (fz.tstats) {
+                    // per row (column m): this warp's (max, first argmax) over its 32 tokens, then
+                    // for sampling rows the sum of 2^((y - max) beta); 8 columns at a time, so
+                    // their shuffle chains overlap
 #pragma unroll
-                    for (int m = 0; m < NPAD; ++m) {
-                        if (m >= M) continue;
-                        const int mode = sh->col_mode[m];
-                        const float y = n < N ? v[m] : -INFINITY;
-                        if (mode == 1) {
-                            const float beta = sh->col_beta[m];
-                            float mx = y;
+                    for (int g0 = 0; g0 < NPAD; g0 += 8) {
+                        if (g0 >= M) break;
+                        float mx[8], zz[8];
+                        int ix[8];
 #pragma unroll
-                            for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-                            float z = (y > -INFINITY) ? um_ex2((y - mx) * beta) : 0.0f;
+                        for (int c = 0; c < 8; ++c) {
+                            mx[c] = (n < N && g0 + c < M) ? v[g0 + c] : -INFINITY;
+                            ix[c] = n < N ? n : 0x7FFFFFFF;
+                        }
 #pragma unroll
-                            for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-                            if (lane == 0) sh->part[warp][m] = make_float2(mx, z);
-                        } else if (mode == 0) {
-                            float mx = y;
-                            int ix = n < N ? n : 0x7FFFFFFF;
+                        for (int o = 16; o > 0; o >>= 1) {
 #pragma unroll
-                            for (int o = 16; o > 0; o >>= 1) {
-                                const float m2 = __shfl_xor_sync(0xffffffffu, mx, o);
-                                const int i2 = __shfl_xor_sync(0xffffffffu, ix, o);
-                                if (um_better_arg(m2, i2, mx, ix)) {
-                                    mx = m2;
-                                    ix = i2;
+                            for (int c = 0; c < 8; ++c) {
+                                const float m2 = __shfl_xor_sync(0xffffffffu, mx[c], o);
+                                const int i2 = __shfl_xor_sync(0xffffffffu, ix[c], o);
+                                if (um_better_arg(m2, i2, mx[c], ix[c])) {
+                                    mx[c] = m2;
+                                    ix[c] = i2;
                                 }
                             }
-                            if (lane == 0) sh->part[warp][m] = make_float2(mx, __int_as_float(ix));
+                        }
+#pragma unroll
+                        for (int c = 0; c < 8; ++c) {
+                            const float y = (n < N && g0 + c < M) ? v[g0 + c] : -INFINITY;
+                            zz[c] = (y > -INFINITY) ? um_ex2((y - mx[c]) * sh->col_beta[g0 + c < M ? g0 + c : 0]) : 0.0f;
+                        }
+#pragma unroll
+                        for (int o = 16; o > 0; o >>= 1) {
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) zz[c] += __shfl_xor_sync(0xffffffffu, zz[c], o);
+                        }
+                        if (lane == 0) {
+#pragma unroll
+                            for (int c = 0; c < 8; ++c) {
+                                const int m = g0 + c;
+                                if (m < M)
+                                    sh->part[warp][m] = sh->col_mode[m] == 0 ? make_float2(mx[c], __int_as_float(ix[c]))
+                                                                             : make_float2(mx[c], zz[c]);
+                            }
                         }
                     }
                     asm volatile("bar.sync 1, %0;\n" ::"n"(kUmEpiWarps * 32) : "memory");
                     if (threadIdx.x < M) {
+                        // merge the four warps' partials of this tile into the CTA's running one
                         const int m = threadIdx.x, mode = sh->col_mode[m];
-                        float2 r = sh->part[0][m];
+                        float2 r = sh->run[m];
                         if (mode == 1) {
                             const float beta = sh->col_beta[m];
                             float mx = r.x;
-                            for (int w = 1; w < kUmEpiWarps; ++w) mx = fmaxf(mx, sh->part[w][m].x);
-                            float z = 0.0f;
+                            for (int w = 0; w < kUmEpiWarps; ++w) mx = fmaxf(mx, sh->part[w][m].x);
+                            float z = (r.x > -INFINITY) ? r.y * um_ex2((r.x - mx) * beta) : 0.0f;
                             for (int w = 0; w < kUmEpiWarps; ++w) {
                                 const float2 pw = sh->part[w][m];
                                 if (pw.x > -INFINITY) z += pw.y * um_ex2((pw.x - mx) * beta);
                             }
                             r = make_float2(mx, z);
                         } else if (mode == 0) {
-                            for (int w = 1; w < kUmEpiWarps; ++w) {
+                            for (int w = 0; w < kUmEpiWarps; ++w) {
                                 const float2 pw = sh->part[w][m];
                                 if (um_better_arg(pw.x, __float_as_int(pw.y), r.x, __float_as_int(r.y))) r = pw;
                             }
                         }
-                        if (mode >= 0)
-                            reinterpret_cast<float2 *>(fz.tstats)[(size_t)m * ntiles_all + tile] = r;
+                        sh->run[m] = r;
                     }
                     asm volatile("bar.sync 1, %0;\n" ::"n"(kUmEpiWarps * 32) : "memory");
                 }
@@ -691,6 +708,9 @@ __global__ void __launch_bounds__(kUmThreads, 1)
             __syncwarp();
             if (lane == 0) mbar_arrive(&sh->acc_empty[buf]);
         }
+        // one partial per row per CTA: tstats [S][k1][gridDim.x]
+        if (fz.tstats && threadIdx.x < M && sh->col_mode[threadIdx.x] >= 0)
+            reinterpret_cast<float2 *>(fz.tstats)[(size_t)threadIdx.x * gridDim.x + blockIdx.x] = sh->run[threadIdx.x];
     }
 
     tc_fence_before();
@@ -738,7 +758,7 @@ cudaError_t launch_umma_variant(const CUtensorMap &map, int N, int nst, const ui
         have = smem;
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(min(cdiv(N, kUmRows), num_sms));
+    cfg.gridDim = dim3(umma_gemm_grid(N, num_sms));
     cfg.blockDim = dim3(kUmThreads);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

@@ -21,6 +21,7 @@ STATUS_NAMES = {0: "Q2_OK", 1: "Q2_ERR_INVALID_ARG", 2: "Q2_ERR_ALIGNMENT", 3: "
                 4: "Q2_ERR_WORKSPACE", 5: "Q2_ERR_CUDA", 6: "Q2_ERR_TIMEOUT", 7: "Q2_ERR_BAD_TOKEN",
                 8: "Q2_ERR_RANGE", 9: "Q2_ERR_BAD_TEMPERATURE"}
 MOE_RENORMALIZE = 1
+LM_HEAD_FUSE_STATS = 1
 EXPORTS = ("q2_tiny_gemm_workspace", "q2_tiny_gemm", "q2_moe_grouped_workspace", "q2_moe_grouped",
            "pq_verify_workspace", "pq_verify", "pq_verify_noalloc", "q2_get_device_status", "q2_status_string",
            "q2_version", "q2_set_probe", "pq_verify_ex", "q2_quench_init", "q2_quench_update",
@@ -73,7 +74,7 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q2_version.restype = I
     lib.q2_lm_head_verify_workspace.argtypes = [I, I, I, I]
     lib.q2_lm_head_verify_workspace.restype = Z
-    lib.q2_lm_head_verify.argtypes = [P, I, I, P, I, P, P, P, P, I, I, P, F, P, P, P, P, P, Z, P]
+    lib.q2_lm_head_verify.argtypes = [P, I, I, P, I, P, P, P, P, I, I, P, F, U, P, P, P, P, P, Z, P]
     lib.q2_lm_head_verify.restype = I
     lib.q2_quench_init.argtypes = [P, I]
     lib.q2_quench_init.restype = I
@@ -326,7 +327,7 @@ def q2_lm_head_verify_workspace(S: int, k: int, V: int, K: int) -> int:
 def q2_lm_head_verify(W: torch.Tensor, V: int, K: int, A: torch.Tensor, draft: torch.Tensor | None,
                       drafts: torch.Tensor | None, u_acc: torch.Tensor | None, u_fin: torch.Tensor,
                       S: int, k: int, temperatures: torch.Tensor | None = None, temperature: float = 1.0,
-                      target: torch.Tensor | None = None, n_acc: torch.Tensor | None = None,
+                      fuse_stats: bool = False, target: torch.Tensor | None = None, n_acc: torch.Tensor | None = None,
                       tokens: torch.Tensor | None = None, probs: torch.Tensor | None = None,
                       ws: torch.Tensor | None = None, stream=None):
     """Vocabulary head + verify: target = A W^T as [S, k+1, V] fp32, then the p/q verify over it
@@ -358,7 +359,8 @@ def q2_lm_head_verify(W: torch.Tensor, V: int, K: int, A: torch.Tensor, draft: t
         ws = workspace(q2_lm_head_verify_workspace(S, k, V, K), dev)
     st = load().q2_lm_head_verify(_ptr(W), V, K, _ptr(A), A.shape[1], _ptr(draft) if k > 0 else None,
                                   _ptr(drafts) if k > 0 else None, _ptr(u_acc) if k > 0 else None, _ptr(u_fin),
-                                  S, k, _ptr(temperatures), float(temperature), _ptr(target), _ptr(n_acc),
+                                  S, k, _ptr(temperatures), float(temperature), LM_HEAD_FUSE_STATS if fuse_stats else 0,
+                                  _ptr(target), _ptr(n_acc),
                                   _ptr(tokens), _ptr(probs), _ptr(ws), ws.numel(), ctypes.c_void_p(_stream(stream)))
     _raise(st, "q2_lm_head_verify")
     return target, n_acc, tokens

@@ -74,7 +74,7 @@ def test_chained_gemm_then_verify(cohort):
 
 # ---------------------------------------------------------------- fused vocabulary head + verify
 
-def _fused(c, temps=None, T=None, want_probs=True):
+def _fused(c, temps=None, T=None, want_probs=True, fuse=True):
     import torch
     q2v, dev, g, v = c["q2v"], c["dev"], c["g"], c["v"]
     S, k1, V = v["target"].shape
@@ -84,7 +84,7 @@ def _fused(c, temps=None, T=None, want_probs=True):
     tgt, n, toks = q2v.q2_lm_head_verify(to_dev(g["W"].reshape(-1), dev), V, g["K"], to_dev(g["A"], dev),
                                          to_dev(v["draft"], dev), to_dev(v["drafts"], dev), to_dev(v["u_acc"], dev),
                                          to_dev(v["u_fin"], dev), S, k1 - 1, temperatures=tt,
-                                         temperature=v["T"] if T is None else T, probs=probs, ws=ws)
+                                         temperature=v["T"] if T is None else T, fuse_stats=fuse, probs=probs, ws=ws)
     st = q2v.q2_get_device_status(ws)
     return (tgt.cpu().numpy(), n.cpu().numpy(), toks.cpu().numpy(),
             probs.cpu().numpy() if want_probs else None, st)
@@ -104,9 +104,10 @@ def _verify_against_oracle(c, tgt, n, toks, probs, temps=None, T=1.0):
     assert stats["exact"] + stats["mismatches_at_near_ties"] == len(samp)
 
 
-def test_fused_lm_head_verify(cohort):
+@pytest.mark.parametrize("fuse", [True, False])
+def test_fused_lm_head_verify(cohort, fuse):
     c = cohort
-    tgt, n, toks, probs, st = _fused(c)
+    tgt, n, toks, probs, st = _fused(c, fuse=fuse)
     assert st == 0
     S, k1, V = c["v"]["target"].shape
     check_gemm(tgt.reshape(S * k1, V), c["Yo"], c["absY"], "fused lm_head")
@@ -140,7 +141,7 @@ def test_lm_head_verify_shapes(orc, S, k, V, K):
     probs = torch.empty((S, 2 * k + 1, V), dtype=torch.float32, device=dev)
     tgt, n, toks = q2v.q2_lm_head_verify(to_dev(W.reshape(-1), dev), V, K, to_dev(A, dev), to_dev(v["draft"], dev),
                                          to_dev(v["drafts"], dev), to_dev(v["u_acc"], dev), to_dev(v["u_fin"], dev),
-                                         S, k, temperature=1.0, probs=probs)
+                                         S, k, temperature=1.0, fuse_stats=True, probs=probs)
     tgt = tgt.cpu().numpy()
     check_gemm(tgt.reshape(S * (k + 1), V), Yo, absY, f"lm_head S={S} V={V}")
     c = dict(v=v, orc=orc)
