@@ -65,6 +65,11 @@ constexpr uint64_t kUmWaitNs = 1000000000ull;                    // 1 s per wait
 
 static_assert(kUmAccBase + 2 * kUmGroup * kUmAccStride <= (int)kUmCols, "TMEM holds 512 columns");
 static_assert(kUmGroup == 2, "one MMA-issuing warp per tile of a group");
+// A stages are slotted by activation stage: slot (gb % 2) * kUmGroup + t holds tile t of
+// activation stage gb, and is free again once b_empty of stage gb completes (each MMA thread
+// commits that barrier after its MMAs of the stage), so one commit per stage and thread
+// releases both the activation stage and its A stages.
+static_assert(kUmAStages == 2 * kUmGroup, "two activation stages of A stages");
 
 __host__ __device__ constexpr int um_bstage(int npad) { return kUmKg * (npad / 8) * 128; }
 
@@ -72,7 +77,6 @@ struct UmShared {
     uint64_t raw_full[kUmRawStages];
     uint64_t raw_empty[kUmRawStages];
     uint64_t ab_full[kUmAStages];    // the dequant warps have written A (TMEM) and the m tile
-    uint64_t ab_empty[kUmAStages];   // the MMAs reading the A stage are done
     uint64_t b_full[kUmBStages];     // the activation stage has landed
     uint64_t b_empty[kUmBStages];    // the MMAs reading the B stage are done
     uint64_t acc_full[2];
@@ -372,7 +376,6 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         }
         for (int i = 0; i < kUmAStages; ++i) {
             mbar_init(&sh->ab_full[i], 4);
-            mbar_init(&sh->ab_empty[i], 1);
         }
         for (int i = 0; i < kUmBStages; ++i) {
             mbar_init(&sh->b_full[i], 1);  // the B warp, once its copies have landed
@@ -483,7 +486,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
             const uint64_t bdesc0 = umma_desc(smem_u32(sB), (NPAD / 8) * 128, 128);
             const uint64_t mdesc0 = umma_desc(smem_u32(sM), kUmKgBytes, 128);
             constexpr uint64_t kBStep = (2 * (NPAD / 8) * 128) >> 4;
-            uint32_t ga = 0, gb = 0;
+            uint32_t gb = 0;
             bool ok = true;
             for (int q = 0; ok && q < ngroups; ++q) {
                 const int tn = min(kUmGroup, my_tiles - q * kUmGroup);
@@ -491,7 +494,7 @@ __global__ void __launch_bounds__(kUmThreads, 1)
                 if (!um_wait(&sh->acc_empty[buf], (((uint32_t)q >> 1) & 1u) ^ 1u, abort_flag, status)) break;
                 tc_fence_after();
                 const uint32_t d = tmem + kUmAccBase + (buf * kUmGroup + (uint32_t)me) * kUmAccStride;
-                for (int s = 0; ok && s < nst; ++s, ++gb, ga += (uint32_t)tn) {
+                for (int s = 0; ok && s < nst; ++s, ++gb) {
                     // both threads wait for the B stage, a thread without a tile too: its
                     // release of the B slot must not run ahead of the stage (b_empty counts
                     // one arrival per thread per stage)
@@ -501,9 +504,8 @@ __global__ void __launch_bounds__(kUmThreads, 1)
                         break;
                     }
                     if (me < tn) {
-                        const uint32_t gm = ga + (uint32_t)me;  // this thread's A stage
-                        const uint32_t a = gm % kUmAStages;
-                        if (!um_wait(&sh->ab_full[a], (gm / kUmAStages) & 1u, abort_flag, status)) {
+                        const uint32_t a = (gb & 1u) * kUmGroup + (uint32_t)me;  // this thread's A stage
+                        if (!um_wait(&sh->ab_full[a], (gb >> 1) & 1u, abort_flag, status)) {
                             ok = false;
                             break;
                         }
@@ -516,7 +518,6 @@ __global__ void __launch_bounds__(kUmThreads, 1)
                         // the blocks' offsets: m (A, shared memory) x the blocks' activation sums
                         umma_f16(d, mdesc0 + (uint64_t)((a * (uint32_t)kUmMTile) >> 4), bd + kUmDataMmas * kBStep,
                                  idesc, 1u);
-                        umma_commit(&sh->ab_empty[a]);
                     }
                     umma_commit(&sh->b_empty[b]);
                 }
@@ -534,21 +535,24 @@ __global__ void __launch_bounds__(kUmThreads, 1)
         const int row = 32 * quarter + lane;
         uint32_t scale_max = 0u;  // running max of |d|, |m| (f16x2)
         const int nsup = cdiv(nst, kUmRawSpan);
-        uint32_t g = 0, rq = 0;  // A stages so far; raw copies of the groups before q
+        uint32_t g = 0, gb = 0, rq = 0;  // A stages and activation stages so far; raw copies before q
         bool ok = true;
         for (int q = 0; ok && q < ngroups; ++q) {
             const int tn = min(kUmGroup, my_tiles - q * kUmGroup);
-            for (int s = 0; ok && s < nst; ++s) {
+            for (int s = 0; ok && s < nst; ++s, ++gb) {
                 for (int t = 0; t < tn; ++t, ++g) {
                     if ((int)(g % kUmDeqGroups) != grp) continue;
                     // raw copy of (tile t, stages 4 (s/4) ..): released after its last use
                     const uint32_t gr = rq + (uint32_t)((s / kUmRawSpan) * tn + t);
-                    const uint32_t r = gr % kUmRawStages, a = g % kUmAStages;
+                    const uint32_t r = gr % kUmRawStages, a = (gb & 1u) * kUmGroup + (uint32_t)t;
                     const int first = s - s % kUmRawSpan;
                     const int uses = min(kUmRawSpan, nst - first);
                     const uint32_t release = (s == first + uses - 1) ? 1u + (uint32_t)(kUmRawSpan - uses) : 1u;
+                    // the slot's previous user, activation stage gb - 2, must be done (its b_empty)
+                    const uint32_t gp = gb - 2u;
                     if (!um_wait_warp(&sh->raw_full[r], (gr / kUmRawStages) & 1u, abort_flag, status) ||
-                        !um_wait_warp(&sh->ab_empty[a], ((g / kUmAStages) & 1u) ^ 1u, abort_flag, status)) {
+                        (gb >= 2u && !um_wait_warp(&sh->b_empty[gp % kUmBStages], (gp / kUmBStages) & 1u, abort_flag,
+                                                   status))) {
                         ok = false;
                         break;
                     }
