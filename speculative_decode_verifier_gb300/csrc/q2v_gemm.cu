@@ -10,45 +10,14 @@
 
 namespace q2v {
 
-// One CTA per activation row, one thread per Q2B32 block of 32 activations (K <= 8192,
-// so at most 256 blocks): per-row exponent, permuted f16x2 pair slots, hi/lo block sums.
-// Row r of the prep is source row rows[r] (or r when rows is NULL); rows[r] < 0 gives a
-// zero row.  Source rows are bf16 with leading dimension ld (ld % 8 == 0, 16-byte base).
+// One CTA per activation row (prep_row_bf16, q2v_mma_core.cuh).
 __global__ void __launch_bounds__(256) prep_bf16_kernel(const uint16_t *__restrict__ src, int ld,
                                                         const int *__restrict__ rows, int R, int K,
                                                         PrepPtrs P, PrepLayout L) {
     __shared__ float scratch[32];
     pdl_wait();
     pdl_trigger();
-    const int r = blockIdx.x;
-    const int b = threadIdx.x;
-    const int srow = rows ? rows[r] : r;
-    float v[32];
-    float mx = 0.0f;
-    if (b < L.nb && srow >= 0) {
-        const uint4 *p = reinterpret_cast<const uint4 *>(src + (size_t)srow * ld + (size_t)b * kBlockK);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint4 q = __ldg(p + j);
-            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                v[8 * j + 2 * i] = __uint_as_float(w[i] << 16);
-                v[8 * j + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fabsf(v[j]));
-    } else {
-#pragma unroll
-        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
-    }
-    const int e = act_exponent(block_max_nonneg(mx, scratch));
-    if (b == 0) P.exps[r] = e;
-    if (b < L.nbp)
-        prep_store_block(v, e, P.act + (size_t)r * L.act_words_per_row(),
-                         reinterpret_cast<__half *>(P.shi + (size_t)r * L.sum_words_per_row()),
-                         reinterpret_cast<__half *>(P.slo + (size_t)r * L.sum_words_per_row()), b);
+    prep_row_bf16(src, ld, rows ? rows[blockIdx.x] : (int)blockIdx.x, (int)blockIdx.x, P, L, scratch);
 }
 
 cudaError_t launch_prep_bf16(const uint16_t *src, int ld, const int *rows, int R, int K, const PrepPtrs &P,

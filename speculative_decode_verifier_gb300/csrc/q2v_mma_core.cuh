@@ -340,4 +340,39 @@ __device__ __forceinline__ float block_max_nonneg(float v, float *scratch32) {
     return m;
 }
 
+// Prepare one activation row (the whole block takes part; thread b handles Q2B32 block b of
+// 32 activations, K <= 8192 so at most 256 blocks): per-row exponent, permuted f16x2 pair
+// slots, hi/lo block sums.  Prepared row r is source row srow (srow < 0: a zero row); source
+// rows are bf16 with leading dimension ld (ld % 8 == 0, 16-byte base).
+__device__ __forceinline__ void prep_row_bf16(const uint16_t *__restrict__ src, int ld, int srow, int r,
+                                              const PrepPtrs &P, const PrepLayout &L, float *scratch32) {
+    const int b = threadIdx.x;
+    float v[32];
+    float mx = 0.0f;
+    if (b < L.nb && srow >= 0) {
+        const uint4 *p = reinterpret_cast<const uint4 *>(src + (size_t)srow * ld + (size_t)b * kBlockK);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const uint4 q = __ldg(p + j);
+            const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                v[8 * j + 2 * i] = __uint_as_float(w[i] << 16);
+                v[8 * j + 2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fabsf(v[j]));
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
+    }
+    const int e = act_exponent(block_max_nonneg(mx, scratch32));
+    if (b == 0) P.exps[r] = e;
+    if (b < L.nbp)
+        prep_store_block(v, e, P.act + (size_t)r * L.act_words_per_row(),
+                         reinterpret_cast<__half *>(P.shi + (size_t)r * L.sum_words_per_row()),
+                         reinterpret_cast<__half *>(P.slo + (size_t)r * L.sum_words_per_row()), b);
+}
+
 }  // namespace q2v

@@ -27,25 +27,31 @@
 
 namespace q2v {
 
-constexpr int kRouteThreads = 1024;
+constexpr int kRoutePrepThreads = 256;
 
-__global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(MoeArgs a, MoeWs w) {
-    __shared__ int s_ids[64 * 16];
-    __shared__ float s_g[64 * 16];
-    __shared__ int s_cnt[257];
-    pdl_wait();
-    pdl_trigger();
+// Routing of the M rows (one CTA): softmax over E, top-k by logit (ties to the lower index),
+// counting sort of the (row, slot) pairs by expert.  E <= 256: a lane keeps its 8 logits in
+// registers across the k arg-max rounds.
+__device__ __forceinline__ void route_rows(const MoeArgs &a, const MoeWs &w, int *s_ids, float *s_g, int *s_cnt) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
     const int E = a.E, K = a.topk, M = a.M;
     for (int e = tid; e <= E; e += blockDim.x) s_cnt[e] = 0;
     __syncthreads();
     for (int r = warp; r < M; r += nw) {
         const float *l = a.router + (size_t)r * E;
+        float lv[8];
         float mx = -INFINITY;
-        for (int e = lane; e < E; e += 32) mx = fmaxf(mx, l[e]);
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int e = lane + 32 * q;
+            lv[q] = e < E ? l[e] : -INFINITY;
+            mx = fmaxf(mx, lv[q]);
+        }
         for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         float z = 0.0f;
-        for (int e = lane; e < E; e += 32) z += expf(l[e] - mx);
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (lane + 32 * q < E) z += expf(lv[q] - mx);
         for (int o = 16; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
         // top-k by logit: repeated arg-max, ties to the lower index
         unsigned taken = 0u;  // bit q: expert lane + 32q already selected
@@ -53,11 +59,12 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(MoeArgs a, Moe
         for (int t = 0; t < K; ++t) {
             float best = -INFINITY;
             int bi = 0x7fffffff;
-            for (int e = lane, q = 0; e < E; e += 32, ++q) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const int e = lane + 32 * q;
                 const bool tk = (taken >> q) & 1u;
-                const float v = l[e];
-                if (!tk && (v > best || (v == best && e < bi) || bi == 0x7fffffff)) {
-                    best = v;
+                if (e < E && !tk && (lv[q] > best || (lv[q] == best && e < bi) || bi == 0x7fffffff)) {
+                    best = lv[q];
                     bi = e;
                 }
             }
@@ -108,6 +115,22 @@ __global__ void __launch_bounds__(kRouteThreads) moe_route_kernel(MoeArgs a, Moe
         if (a.ids_out) a.ids_out[p] = e;
         if (a.w_out) a.w_out[p] = s_g[p];
     }
+}
+
+// CTAs 0..M-1 prepare the activation rows of X (the B operand of gate and up); CTA M routes.
+// The two are independent, so one launch covers both.
+__global__ void __launch_bounds__(kRoutePrepThreads) moe_route_prep_kernel(MoeArgs a, MoeWs w, PrepLayout LX) {
+    __shared__ float scratch[32];
+    __shared__ int s_ids[64 * 16];
+    __shared__ float s_g[64 * 16];
+    __shared__ int s_cnt[257];
+    pdl_wait();
+    pdl_trigger();
+    if ((int)blockIdx.x < a.M) {
+        prep_row_bf16(a.X, a.H, (int)blockIdx.x, (int)blockIdx.x, w.prepX, LX, scratch);
+        return;
+    }
+    route_rows(a, w, s_ids, s_g, s_cnt);
 }
 
 
@@ -420,10 +443,8 @@ int choose_ks(int units_without_split, int ntk, int resident_warps) {
 }  // namespace
 
 cudaError_t launch_moe(const MoeArgs &a, const MoeWs &w, int num_sms, cudaStream_t s) {
-    cudaError_t err = launch_pdl(moe_route_kernel, dim3(1), dim3(kRouteThreads), s, a, w);
-    if (err != cudaSuccess) return err;
     const PrepLayout LX(a.H), LH(a.F);
-    err = launch_prep_bf16(a.X, a.H, nullptr, a.M, a.H, w.prepX, LX, s);
+    cudaError_t err = launch_pdl(moe_route_prep_kernel, dim3(a.M + 1), dim3(kRoutePrepThreads), s, a, w, LX);
     if (err != cudaSuccess) return err;
     const int P = a.M * a.topk;
     const int expect_active = min(a.E, P);
