@@ -437,7 +437,7 @@ cudaError_t launch_stream(const MoeArgs &a, const MoeWs &w, int KS, float *out, 
 // K splits so that the expected number of units is a few per resident warp.
 int choose_ks(int units_without_split, int ntk, int resident_warps) {
     int ks = 1;
-    while (ks < kMaxKSplits && ks < ntk && (long long)units_without_split * ks < 4LL * resident_warps) ks *= 2;
+    while (ks < kMaxKSplits && ks < ntk && (long long)units_without_split * ks < 2LL * resident_warps) ks *= 2;
     return ks;
 }
 }  // namespace
