@@ -65,6 +65,7 @@ struct PqCarve {
     float *stats;
     float *mass, *pmass;
     unsigned int *tickets;
+    float2 *xin;
     size_t bytes;
 };
 
@@ -76,6 +77,7 @@ PqCarve pq_carve_from(Carver &c, int S, int k, int V) {
     r.mass = static_cast<float *>(c.take((size_t)S * C * kSegsPerChunk * sizeof(float)));
     r.pmass = static_cast<float *>(c.take((size_t)S * C * kSegsPerChunk * sizeof(float)));
     r.tickets = static_cast<unsigned int *>(c.take((size_t)S * sizeof(unsigned int)));
+    r.xin = static_cast<float2 *>(c.take((size_t)S * std::max(k, 1) * sizeof(float2)));
     r.bytes = c.off - off0 + Q2_WORKSPACE_HEADER_BYTES;  // as a workspace of its own
     return r;
 }
@@ -415,6 +417,7 @@ void pq_setup(PqArgs &a, PqSplit &sp, Carver &c, const float *target_logits, con
         C = cdiv(V, L);
         sp.C = C;
         sp.L = L;
+        sp.xin = pc.xin;
         sp.stats = pc.stats;
         sp.mass = pc.mass;
         sp.pmass = pc.pmass;

@@ -44,6 +44,7 @@ struct PqSplit {
     float *mass;         // [S][C][8] draw mass of each warp segment of each chunk
     float *pmass;        // [S][C][8] p_j mass of each segment (zero-residual fallback)
     unsigned int *tickets;  // [S]
+    float2 *xin;         // [S][k] (target, draft) logit at each draft token, gathered by kernel 1
     // Target rows' partials made elsewhere (the fused vocabulary-head GEMM), nullable:
     // [S][k+1][Ct] float2, one per 128-token tile.  When set, the statistics kernel only
     // streams the draft rows and the combine reads the target rows from here.

@@ -14,10 +14,12 @@
 // Two tiers:
 //   * small V (<= kWarpTierMaxV): one warp per session does everything in one kernel;
 //   * large V: the vocabulary of each session is split into C chunks.  Kernel 1 streams
-//     every row's chunk once and writes (max, sum exp) partials.  Kernel 2 combines the
-//     partials, runs the accept scan, computes its chunk's residual (or bonus) mass from
-//     one or two rows, and the last CTA of the session to finish (an atomic ticket; no
-//     CTA ever waits on another) runs the inverse-CDF search inside the selected chunk.
+//     every row's chunk once (leaving the rows in L2) and writes (max, sum exp) partials;
+//     it also gathers both logits at each draft token.  Kernel 2 combines the partials,
+//     runs the accept scan, computes its chunk's residual (or bonus) mass from one or two
+//     rows, and the last CTA of the session to finish (an atomic ticket; no CTA ever waits
+//     on another) runs the inverse-CDF search with all of its threads: a block-wide scan
+//     over the session's segment masses, then one over the tokens of the chosen segment.
 //
 // Arithmetic is fp32 throughout (exponentials on the SFU via ex2.approx): reductions are
 // trees, and the running cumulative sums of the draws are compensated (a hi + lo pair
@@ -72,6 +74,48 @@ struct CSum {
     __device__ __forceinline__ bool exceeds(float x, float target) const { return hi + (lo + x) > target; }
     __device__ __forceinline__ float value() const { return hi + lo; }
 };
+
+// a + b for two compensated sums: two-sum of the high parts, low parts added.
+__device__ __forceinline__ CSum csum_plus(CSum a, const CSum &b) {
+    a.add(b.hi);
+    a.lo += b.lo;
+    return a;
+}
+
+// Block-wide scan of compensated values in thread order (blockDim.x a multiple of 32, at most
+// 1024): returns this thread's exclusive prefix and sets `total`.  `scratch` holds 64 floats;
+// the call synchronises the block once and leaves scratch free again only after the next
+// barrier.
+__device__ __forceinline__ CSum block_excl_scan(const CSum &v, float *scratch, CSum &total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
+    CSum inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        CSum n;
+        n.hi = __shfl_up_sync(0xffffffffu, inc.hi, o);
+        n.lo = __shfl_up_sync(0xffffffffu, inc.lo, o);
+        if (lane >= o) inc = csum_plus(n, inc);
+    }
+    CSum ex;
+    ex.hi = __shfl_up_sync(0xffffffffu, inc.hi, 1);
+    ex.lo = __shfl_up_sync(0xffffffffu, inc.lo, 1);
+    if (lane == 0) ex = CSum();
+    if (lane == 31) {
+        scratch[2 * warp] = inc.hi;
+        scratch[2 * warp + 1] = inc.lo;
+    }
+    __syncthreads();
+    CSum base, tot;
+    for (int w = 0; w < nw; ++w) {
+        CSum x;
+        x.hi = scratch[2 * w];
+        x.lo = scratch[2 * w + 1];
+        if (w < warp) base = csum_plus(base, x);
+        tot = csum_plus(tot, x);
+    }
+    total = tot;
+    return csum_plus(base, ex);
+}
 
 __device__ __forceinline__ const float *row_ptr(const PqArgs &a, int s, int r) {
     // rows 0..k: target rows; rows k+1..2k: draft rows 0..k-1
@@ -353,6 +397,11 @@ __global__ void __launch_bounds__(512) pqv_stats_kernel(PqArgs a, PqSplit sp) {
         }
         return;
     }
+    // the accept scan's inputs, gathered here so kernel 2 reads them in its first round of
+    // loads: the target and draft logits at each draft token (by a spare warp when the block
+    // has one, else by warp 0 after its rows)
+    const int gw = nwarps > R ? R : 0;
+    const bool gather = c == 0 && warp == gw && lane < a.k;
     for (int r = (sp.tstats ? a.k + 1 : 0) + warp; r < R; r += nwarps) {
         const float *x = row_ptr(a, s, r);
         float m = -INFINITY, z = 0.0f;
@@ -365,7 +414,7 @@ __global__ void __launch_bounds__(512) pqv_stats_kernel(PqArgs a, PqSplit sp) {
 #pragma unroll
                 for (int u = 0; u < U; ++u) {
                     const int i = base + u * 32 + lane;
-                    v[u] = i < n4 ? __ldcs(x4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                    v[u] = i < n4 ? __ldg(x4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
                 }
                 float bm = m;
 #pragma unroll
@@ -399,6 +448,12 @@ __global__ void __launch_bounds__(512) pqv_stats_kernel(PqArgs a, PqSplit sp) {
             *st = make_float2(M, zz);
         }
     }
+    if (gather) {
+        const int gx = a.drafts[(size_t)s * a.k + lane];
+        float2 v = make_float2(0.0f, 0.0f);  // an out-of-range token is caught by kernel 2
+        if (gx >= 0 && gx < a.V) v = make_float2(row_ptr(a, s, lane)[gx], row_ptr(a, s, a.k + 1 + lane)[gx]);
+        sp.xin[(size_t)s * a.k + lane] = v;
+    }
 }
 
 // The chunk partials of row r of session s and their count: the target rows' from the fused
@@ -416,15 +471,16 @@ __device__ __forceinline__ const float2 *row_partials(const PqArgs &a, const PqS
 //
 // Each chunk of L tokens is cut into 8 contiguous warp segments; warp w of the CTA owns
 // segment w and writes its draw mass (and its p_j mass, for the zero-residual fallback) to
-// the workspace.  The last CTA of the session to finish picks, with one warp, the segment
-// holding the crossing (a segmented scan over the session's C*8 masses) and then the token
-// inside it (a scan of that one segment): no block-wide barrier in the search.
+// the workspace.  The last CTA of the session to finish picks the segment holding the
+// crossing (a block-wide compensated scan over the session's C*8 masses) and then the token
+// inside it (the same over the segment's tokens).  Every load of the first phase (partials,
+// gathered draft logits) goes out in one round.
 template <bool VEC>
 __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
     __shared__ float rowM[kMaxRows];
     __shared__ float rowL2Z[kMaxRows];
-    __shared__ float s_wm[kMaxChunks * kSegsPerChunk];  // the last CTA's copy of the segment masses
     __shared__ int s_j, s_last;
+    extern __shared__ __align__(16) float pq_dyn[];  // the last CTA's copy of the segment masses
     pdl_wait();
     pdl_trigger();
     const int c = blockIdx.x, s = blockIdx.y;
@@ -488,6 +544,17 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
         return;
     }
 
+    // 0. the accept scan's inputs (gathered by kernel 1): these loads go out in one round with
+    //    the partials of step 1
+    int xv = 0;
+    float2 xl = make_float2(0.0f, 0.0f);
+    float uv = 0.0f;
+    if (warp == 0 && lane < a.k) {
+        xv = a.drafts[(size_t)s * a.k + lane];
+        xl = sp.xin[(size_t)s * a.k + lane];
+        uv = a.u_acc[(size_t)s * a.k + lane];
+    }
+
     // 1. row statistics from the chunk partials: 16 lanes per row, partials held in
     //    registers so the combine takes one round of loads
     for (int r0 = 0; r0 < R; r0 += 16) {
@@ -527,22 +594,17 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
         }
     }
     __syncthreads();
-    // 2. accept scan: lane i evaluates draft i (all loads in one round), a ballot finds
+    // 2. accept scan: lane i evaluates draft i from the prefetched logits, a ballot finds
     //    the first rejection
     if (warp == 0) {
         bool bad = false, rej = false;
         if (lane < a.k) {
-            const int x = a.drafts[(size_t)s * a.k + lane];
-            if (x < 0 || x >= a.V) {
+            if (xv < 0 || xv >= a.V) {
                 bad = true;
-            } else {
-                const float tx = row_ptr(a, s, lane)[x], dx = row_ptr(a, s, a.k + 1 + lane)[x];
-                const float u = a.u_acc[(size_t)s * a.k + lane];
-                if (dx != -INFINITY) {  // q(x) == 0 accepts
-                    const float lp = (tx - rowM[lane]) * beta - rowL2Z[lane];
-                    const float lq = (dx - rowM[a.k + 1 + lane]) * beta - rowL2Z[a.k + 1 + lane];
-                    rej = !(u < ex2(lp - lq));
-                }
+            } else if (xl.y != -INFINITY) {  // q(x) == 0 accepts
+                const float lp = (xl.x - rowM[lane]) * beta - rowL2Z[lane];
+                const float lq = (xl.y - rowM[a.k + 1 + lane]) * beta - rowL2Z[a.k + 1 + lane];
+                rej = !(uv < ex2(lp - lq));
             }
         }
         const unsigned badm = __ballot_sync(0xffffffffu, bad), rejm = __ballot_sync(0xffffffffu, rej);
@@ -601,52 +663,59 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
     }
     __syncthreads();
     if (tid == 0) {
-        __threadfence();
+        __threadfence();  // release this CTA's masses (the barrier above ordered them before it)
         const unsigned ticket = atomicAdd(sp.tickets + s, 1u);
-        s_last = (ticket == (unsigned)(sp.C - 1));
+        const int last = ticket == (unsigned)(sp.C - 1);
+        if (last) __threadfence();  // acquire: the other CTAs' masses, read below with ld.cg
+        s_last = last;
     }
     __syncthreads();
-    if (!s_last || warp != 0) return;
-    __threadfence();
+    if (!s_last) return;
 
-    // 4. last CTA, one warp: pick the segment holding the crossing, then the token in it.
-    //    The session's segment masses are first copied to shared memory in one round.
+    // 4. last CTA, all threads: the segment holding the crossing of u_fin * total, then the
+    //    token inside it.  Each level is a block-wide compensated scan: every thread sums a
+    //    contiguous run of entries, the scan gives its prefix, the first thread whose run
+    //    crosses walks that run.  If rounding puts the target past the end, the last entry
+    //    with mass is taken.
+    __shared__ float s_scan[64];
+    __shared__ int s_first, s_lastpos, s_ent;
+    __shared__ float s_pre[2];
     const int nseg = sp.C * kSegsPerChunk;
-    float *sm = s_wm;
-    const float *wsrc = sp.mass + (size_t)s * nseg;
-    for (int e = lane; e < nseg; e += 32) sm[e] = __ldcg(wsrc + e);
-    __syncwarp();
-    const int q = cdiv(nseg, 32);
-    const int e0 = min(nseg, lane * q), e1 = min(nseg, e0 + q);
+    const int nt = blockDim.x;
+    float *sm = pq_dyn;
     int mode = D.mode;
-    float seg = 0.0f;
-    for (int e = e0; e < e1; ++e) seg += sm[e];
-    float tot = warp_sum(seg);
-    if (mode == 0 && !(tot > 0.0f)) {  // zero residual mass: draw from p_j
-        mode = 1;
-        wsrc = sp.pmass + (size_t)s * nseg;
-        __syncwarp();
-        for (int e = lane; e < nseg; e += 32) sm[e] = __ldcg(wsrc + e);
-        __syncwarp();
-        seg = 0.0f;
-        for (int e = e0; e < e1; ++e) seg += sm[e];
-        tot = warp_sum(seg);
+    // level 1: segments
+    const int q = cdiv(nseg, nt);
+    const int e0 = min(nseg, tid * q), e1 = min(nseg, e0 + q);
+    CSum own, excl, tot;
+    for (int pass = 0; pass < 2; ++pass) {  // pass 1 only when the residual has no mass
+        const float *wsrc = (pass == 0 ? sp.mass : sp.pmass) + (size_t)s * nseg;
+        for (int e = tid; e < nseg; e += nt) sm[e] = __ldcg(wsrc + e);
+        __syncthreads();
+        own = CSum();
+        for (int e = e0; e < e1; ++e) own.add(sm[e]);
+        excl = block_excl_scan(own, s_scan, tot);
+        if (mode == 1 || tot.hi > 0.0f) break;
+        mode = 1;  // zero residual mass: draw from p_j
+        __syncthreads();
     }
     D.mode = mode;
-    const float target = a.u_fin[s] * tot;
-    const float incl = warp_incl_scan(seg, lane);
-    float excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) excl = 0.0f;
-    const unsigned hit = __ballot_sync(0xffffffffu, seg > 0.0f && excl + seg > target);
-    const unsigned pos = __ballot_sync(0xffffffffu, seg > 0.0f);
-    // the lane whose entries hold the crossing; if rounding put the target past the end,
-    // the last lane with mass (its last segment with mass is taken)
-    const int owner = hit ? (__ffs(hit) - 1) : (pos ? 31 - __clz(pos) : -1);
-    int ent = -1;
-    CSum prefix;
-    if (lane == owner) {
-        CSum pre, last_pre;
-        pre.add(excl);
+    const float target = a.u_fin[s] * (tot.hi + tot.lo);
+    if (tid == 0) {
+        s_first = nt;
+        s_lastpos = -1;
+    }
+    __syncthreads();
+    const float own_m = own.hi + own.lo;
+    if (own_m > 0.0f) {
+        atomicMax(&s_lastpos, tid);
+        if (excl.exceeds(own_m, target)) atomicMin(&s_first, tid);
+    }
+    __syncthreads();
+    const int owner1 = s_first < nt ? s_first : s_lastpos;
+    if (tid == owner1) {
+        // the first entry of this run whose end passes the target (else its last entry with mass)
+        CSum pre = excl, last_pre;
         int found = -1, last_nz = -1;
         CSum found_pre;
         for (int e = e0; e < e1; ++e) {
@@ -654,7 +723,7 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
             if (me > 0.0f) {
                 last_nz = e;
                 last_pre = pre;
-                if (hit && pre.exceeds(me, target)) {
+                if (s_first < nt && pre.exceeds(me, target)) {
                     found = e;
                     found_pre = pre;
                     break;
@@ -662,44 +731,72 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
             }
             pre.add(me);
         }
-        ent = found >= 0 ? found : last_nz;
-        prefix = found >= 0 ? found_pre : last_pre;
+        s_ent = found >= 0 ? found : last_nz;
+        const CSum pr = found >= 0 ? found_pre : last_pre;
+        s_pre[0] = pr.hi;
+        s_pre[1] = pr.lo;
     }
+    __syncthreads();
     int y_sel = -1;
-    if (owner >= 0) {
-        ent = __shfl_sync(0xffffffffu, ent, owner);
-        prefix.hi = __shfl_sync(0xffffffffu, prefix.hi, owner);
-        prefix.lo = __shfl_sync(0xffffffffu, prefix.lo, owner);
-        // the segment's tokens, 32 at a time in order; the loads of up to 8 rounds are
-        // issued together
+    if (owner1 >= 0) {
+        // level 2: the tokens of the selected segment, r per thread
+        const int ent = s_ent;
         const int sc = ent / kSegsPerChunk, sw = ent - sc * kSegsPerChunk;
-        const int y0 = sc * sp.L + sw * Lw, y1 = min(min(a.V, sc * sp.L + sp.L), y0 + Lw);
-        CSum carry = prefix;
-        int last_pos = -1;
-        for (int base0 = y0; base0 < y1 && y_sel < 0; base0 += 32 * 8) {
-            float wv[8];
+        const int ty0 = sc * sp.L + sw * Lw, ty1 = min(min(a.V, sc * sp.L + sp.L), ty0 + Lw);
+        const int r = cdiv(max(ty1 - ty0, 0), nt);
+        const int y0 = min(ty1, ty0 + tid * r), y1 = min(ty1, y0 + r);
+        CSum seg_pre;
+        seg_pre.hi = s_pre[0];
+        seg_pre.lo = s_pre[1];
+        // a thread's weights stay in registers for the walk when it has at most 4 tokens
+        float wv[4];
+        CSum own2, tot2;
+        if (r <= 4) {
 #pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int y = base0 + 32 * u + lane;
+            for (int u = 0; u < 4; ++u) {
+                const int y = y0 + u;
                 wv[u] = y < y1 ? draw_weight(D, beta, D.t[y], D.d[y]) : 0.0f;
+                if (y < y1) own2.add(wv[u]);
             }
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int base = base0 + 32 * u;
-                if (base < y1 && y_sel < 0) {
-                    const float w = wv[u];
-                    const float inc = warp_incl_scan(w, lane);
-                    const unsigned h = __ballot_sync(0xffffffffu, w > 0.0f && carry.exceeds(inc, target));
-                    const unsigned pz = __ballot_sync(0xffffffffu, w > 0.0f);
-                    if (pz) last_pos = base + 31 - __clz(pz);
-                    if (h) y_sel = base + __ffs(h) - 1;
-                    carry.add(__shfl_sync(0xffffffffu, inc, 31));
-                }
-            }
+        } else {
+            for (int y = y0; y < y1; ++y) own2.add(draw_weight(D, beta, D.t[y], D.d[y]));
         }
-        if (y_sel < 0) y_sel = last_pos;
+        __syncthreads();  // s_scan is reused
+        const CSum excl2 = csum_plus(seg_pre, block_excl_scan(own2, s_scan, tot2));
+        if (tid == 0) {
+            s_first = nt;
+            s_lastpos = -1;
+        }
+        __syncthreads();
+        const float own2_m = own2.hi + own2.lo;
+        if (own2_m > 0.0f) {
+            atomicMax(&s_lastpos, tid);
+            if (excl2.exceeds(own2_m, target)) atomicMin(&s_first, tid);
+        }
+        __syncthreads();
+        const int owner2 = s_first < nt ? s_first : s_lastpos;
+        if (tid == owner2) {
+            CSum pre = excl2;
+            int found = -1, last_nz = -1;
+            for (int y = y0; y < y1; ++y) {
+                const int u = y - y0;
+                const float w = r > 4 ? draw_weight(D, beta, D.t[y], D.d[y])
+                                      : (u == 0 ? wv[0] : u == 1 ? wv[1] : u == 2 ? wv[2] : wv[3]);
+                if (w > 0.0f) {
+                    last_nz = y;
+                    if (s_first < nt && pre.exceeds(w, target)) {
+                        found = y;
+                        break;
+                    }
+                }
+                pre.add(w);
+            }
+            s_ent = found >= 0 ? found : last_nz;
+        }
+        __syncthreads();
+        y_sel = owner2 >= 0 ? s_ent : -1;
     }
-    if (lane == 0) write_tokens(a, s, j, y_sel);
+    if (tid == 0) write_tokens(a, s, j, y_sel);
 }
 
 cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier, int num_sms, cudaStream_t st) {
@@ -712,15 +809,18 @@ cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier,
     const bool vec = (a.V % 4) == 0 && (sp.L % 4) == 0;
     const int R = 2 * a.k + 1;
     const dim3 grid(sp.C, a.S);
-    const int warps1 = min(R, 16);
+    const int warps1 = min(R + 1, 16);  // a spare warp gathers the accept-scan inputs
     cudaError_t e = probed(kProbePqStats, st, [&] {
         return vec ? launch_pdl(pqv_stats_kernel<true>, grid, dim3(warps1 * 32), st, a, sp)
                    : launch_pdl(pqv_stats_kernel<false>, grid, dim3(warps1 * 32), st, a, sp);
     });
     if (e != cudaSuccess) return e;
+    // dynamic shared memory: the last CTA's copy of the segment masses (at most
+    // kMaxChunks * kSegsPerChunk floats)
+    const size_t smem2 = (size_t)sp.C * kSegsPerChunk * sizeof(float);
     return probed(kProbePqVerify, st, [&] {
-        return vec ? launch_pdl(pqv_verify_kernel<true>, grid, dim3(256), st, a, sp)
-                   : launch_pdl(pqv_verify_kernel<false>, grid, dim3(256), st, a, sp);
+        return vec ? launch_pdl_smem(pqv_verify_kernel<true>, grid, dim3(256), smem2, st, a, sp)
+                   : launch_pdl_smem(pqv_verify_kernel<false>, grid, dim3(256), smem2, st, a, sp);
     });
 }
 

@@ -67,6 +67,7 @@ def test_batched_config_full_size(env):
     (5, 4, 4097, 1.0),       # smallest split-tier V, V % 4 != 0 (scalar loads)
     (7, 3, 10000, 1.5),      # ragged last chunk
     (40, 4, 32768, 1.0),     # many sessions: few chunks each
+    (320, 2, 20000, 1.0),    # one chunk per session: segments of 2,512 tokens, 10 per thread in the draw
     (2, 16, 8192, 1.0),      # the largest k
     (3, 0, 5000, 1.0),       # k = 0: plain sampling from p_0
     (9, 0, 300, 0.9),        # k = 0 in the warp tier
