@@ -799,6 +799,25 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
     if (tid == 0) write_tokens(a, s, j, y_sel);
 }
 
+namespace {
+// launch_pdl with dynamic shared memory
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl_smem(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t stream,
+                            Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+}  // namespace
+
 cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier, int num_sms, cudaStream_t st) {
     if (warp_tier) {
         const int blocks = max(1, min(cdiv(a.S, kWarpTierWarps), num_sms * 8));
