@@ -11,7 +11,8 @@ are random, not trained.  Device timing replays one CUDA graph per input set, ro
 
 Prints one JSON line.  `value` is the device-timed step time in microseconds (inputs resident
 in HBM); `e2e` is the same step through the Python binding with pinned host buffers copied
-in and results copied out inside the timed region.  `--impl reference` times the fp64 CPU
+in and results copied out inside the timed region, every step; the input copies run on a
+second stream, so step i+1's copies overlap step i's kernels.  `--impl reference` times the fp64 CPU
 oracle on the host cores instead (the only place this file runs the oracle besides the
 cpu_baseline leg).
 """
@@ -88,6 +89,25 @@ def make_inputs(set_id: int):
     m = synth.config_moe(2, salt=set_id)
     v = synth.config_verify(3, salt=set_id)
     return g, m, v
+
+
+def _packed(layout, device, pin=False):
+    """One uint8 buffer holding the tensors of `layout` [(name, shape, dtype)] at 256-byte
+    aligned offsets; returns (buffer, {name: typed view})."""
+    import torch
+    offs, off = [], 0
+    for _, shape, dt in layout:
+        offs.append(off)
+        nbytes = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+        off = (off + nbytes + 255) // 256 * 256
+    buf = torch.empty(max(off, 256), dtype=torch.uint8, device=device)
+    if pin:
+        buf = buf.pin_memory()
+    views = {}
+    for (name, shape, dt), o in zip(layout, offs):
+        nbytes = int(np.prod(shape)) * torch.empty((), dtype=dt).element_size()
+        views[name] = buf[o:o + nbytes].view(dt).view(shape)
+    return buf, views
 
 
 class ClockSampler:
@@ -177,30 +197,32 @@ def run_device(args, rank: int, world: int):
             shapes = dict(N=g["N"], K=g["K"], M=g["M"], E=m["E"], H=m["H"], F=m["F"], topk=m["topk"],
                           S=v["target"].shape[0], k=v["target"].shape[1] - 1, V=v["target"].shape[2])
     sh = shapes
-    Y1 = torch.empty((sh["M"], sh["N"]), dtype=torch.float32, device=dev)
-    Y2 = torch.empty((sh["M"], sh["H"]), dtype=torch.float32, device=dev)
+    # the step's results (the linear's Y, the MoE's Y, accepted counts, tokens) live in one
+    # device buffer, so the end-to-end loop reads them back with one copy
+    res_layout = [("Y1", (sh["M"], sh["N"]), torch.float32), ("Y2", (sh["M"], sh["H"]), torch.float32),
+                  ("n", (sh["S"],), torch.int32), ("t", (sh["S"], sh["k"] + 1), torch.int32)]
+    res_dev, res = _packed(res_layout, dev)
+    Y1, Y2, n_acc, toks = res["Y1"], res["Y2"], res["n"], res["t"]
     ids = torch.empty((sh["M"], sh["topk"]), dtype=torch.int32, device=dev)
     gw = torch.empty((sh["M"], sh["topk"]), dtype=torch.float32, device=dev)
-    n_acc = torch.empty(sh["S"], dtype=torch.int32, device=dev)
-    toks = torch.empty((sh["S"], sh["k"] + 1), dtype=torch.int32, device=dev)
     ws1 = q2v.workspace(q2v.q2_tiny_gemm_workspace(sh["M"], sh["N"], sh["K"]), dev)
     ws2 = q2v.workspace(q2v.q2_moe_grouped_workspace(sh["M"], sh["E"], sh["topk"], sh["H"], sh["F"]), dev)
     ws3 = q2v.workspace(q2v.pq_verify_workspace(sh["S"], sh["k"], sh["V"]), dev)
 
-    def part_gemm(s):
-        q2v.q2_tiny_gemm(s["W"], sh["N"], sh["K"], s["A"], Y=Y1, ws=ws1)
+    def part_gemm(s, o=res):
+        q2v.q2_tiny_gemm(s["W"], sh["N"], sh["K"], s["A"], Y=o["Y1"], ws=ws1)
 
-    def part_moe(s):
+    def part_moe(s, o=res):
         q2v.q2_moe_grouped(moe_w["Wg"], moe_w["Wu"], moe_w["Wd"], sh["E"], sh["H"], sh["F"], sh["topk"], s["X"],
-                           s["R"], Y=Y2, ids_out=ids, w_out=gw, ws=ws2)
+                           s["R"], Y=o["Y2"], ids_out=ids, w_out=gw, ws=ws2)
 
-    def part_pq(s):
-        q2v.pq_verify(s["T"], s["Dl"], s["x"], s["ua"], s["uf"], 1.0, n_acc=n_acc, tokens=toks, ws=ws3)
+    def part_pq(s, o=res):
+        q2v.pq_verify(s["T"], s["Dl"], s["x"], s["ua"], s["uf"], 1.0, n_acc=o["n"], tokens=o["t"], ws=ws3)
 
-    def step(s):
-        part_gemm(s)
-        part_moe(s)
-        part_pq(s)
+    def step(s, o=res):
+        part_gemm(s, o)
+        part_moe(s, o)
+        part_pq(s, o)
 
     if args.profile:
         # eager steps on one input set, for an ncu launch list (no graphs, no e2e, no oracle)
@@ -415,40 +437,72 @@ def run_device(args, rank: int, world: int):
                   "gemm_frac_hbm": (wbytes + Mc * Kc * 2 + Mc * Nc * 4) / (g_us * 1e-6) / 1e9 / peak_x}
         del Wc
 
-    # e2e: through the binding, pinned host inputs in, results out, every step
-    pin = []
+    # e2e: through the binding, pinned host inputs in, results out, every step.  Each input
+    # set is one pinned host buffer and one device buffer (the tensors are views at 256-byte
+    # aligned offsets), so a step's inputs go in with one copy and its results come back
+    # with one.
+    in_keys = ("A", "X", "R", "T", "Dl", "x", "ua", "uf")
+    in_layout = [(k, tuple(sets[0][k].shape), sets[0][k].dtype) for k in in_keys]
+    pin, dev_in = [], []
     for s in sets:
-        h = {k: torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)).pin_memory()
-             for k, a in s["host"].items()}
-        pin.append(h)
-    out_host = dict(Y1=torch.empty_like(Y1, device="cpu").pin_memory(), Y2=torch.empty_like(Y2, device="cpu").pin_memory(),
-                    n=torch.empty_like(n_acc, device="cpu").pin_memory(),
-                    t=torch.empty_like(toks, device="cpu").pin_memory())
-    h2d = sum(t.numel() * t.element_size() for t in pin[0].values())
-    d2h = sum(t.numel() * t.element_size() for t in out_host.values())
-    dev_in = [dict(A=torch.empty_like(s["A"]), X=torch.empty_like(s["X"]), R=torch.empty_like(s["R"]),
-                   T=torch.empty_like(s["T"]), Dl=torch.empty_like(s["Dl"]), x=torch.empty_like(s["x"]),
-                   ua=torch.empty_like(s["ua"]), uf=torch.empty_like(s["uf"]), W=s["W"]) for s in sets]
+        hb, hv = _packed(in_layout, "cpu", pin=True)
+        for k in in_keys:
+            a = s["host"][k]
+            hv[k].copy_(torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)))
+        db, dv = _packed(in_layout, dev)
+        dv["W"] = s["W"]
+        pin.append(hb)
+        dev_in.append((db, dv))
+    # each slot has its own result buffer, read back on the copy stream once its step is done,
+    # so no copy sits between two steps' kernels on the compute stream
+    res_slots = [_packed(res_layout, dev) for _ in range(N_SETS)]
+    res_host = [torch.empty_like(res_dev, device="cpu").pin_memory() for _ in range(N_SETS)]
+    h2d = pin[0].numel()
+    d2h = res_host[0].numel()
 
-    def e2e_step(i):
-        s = dev_in[i % N_SETS]
-        h = pin[i % N_SETS]
-        for key in ("A", "X", "R", "T", "Dl", "x", "ua", "uf"):
-            s[key].copy_(h[key], non_blocking=True)
-        step(s)
-        out_host["Y1"].copy_(Y1, non_blocking=True)
-        out_host["Y2"].copy_(Y2, non_blocking=True)
-        out_host["n"].copy_(n_acc, non_blocking=True)
-        out_host["t"].copy_(toks, non_blocking=True)
+    # Steps are pipelined across two streams: step i's inputs are copied on a copy stream into
+    # device slot i % N_SETS while earlier steps compute; a step waits for its own inputs, and
+    # a slot is refilled only after the step that read it has finished.  Every step still
+    # copies its own inputs in and its results out inside the timed region.
+    comp = torch.cuda.current_stream()
+    cstream = torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(N_SETS)]
+    ev_done = [torch.cuda.Event() for _ in range(N_SETS)]
+    AHEAD = N_SETS - 1
 
-    for i in range(args.warmup):
-        e2e_step(i)
+    def copy_in(i):
+        j = i % N_SETS
+        with torch.cuda.stream(cstream):
+            cstream.wait_event(ev_done[j])
+            dev_in[j][0].copy_(pin[j], non_blocking=True)
+            ev_in[j].record(cstream)
+
+    def copy_out(i):
+        j = i % N_SETS
+        with torch.cuda.stream(cstream):
+            cstream.wait_event(ev_done[j])
+            res_host[j].copy_(res_slots[j][0], non_blocking=True)
+
+    def run_steps(n):
+        for i in range(min(AHEAD, n)):
+            copy_in(i)
+        for i in range(n):
+            if i + AHEAD < n:
+                copy_in(i + AHEAD)
+            j = i % N_SETS
+            comp.wait_event(ev_in[j])
+            step(dev_in[j][1], res_slots[j][1])
+            ev_done[j].record(comp)
+            copy_out(i)
+
+    run_steps(args.warmup)
     torch.cuda.synchronize()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    e0.record()
-    for i in range(args.steps):
-        e2e_step(i)
-    e1.record()
+    e0.record(comp)
+    cstream.wait_event(e0)
+    run_steps(args.steps)
+    comp.wait_stream(cstream)  # the last results are home before the clock stops
+    e1.record(comp)
     torch.cuda.synchronize()
     e2e_us = e0.elapsed_time(e1) / args.steps * 1000.0
 
