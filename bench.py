@@ -91,6 +91,18 @@ def make_inputs(set_id: int):
     return g, m, v
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest of every rank's x (the job is as slow as its slowest replica); x itself when
+    no process group is running."""
+    import torch
+    import torch.distributed as dist
+    if not dist.is_available() or not dist.is_initialized() or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def _packed(layout, device, pin=False):
     """One uint8 buffer holding the tensors of `layout` [(name, shape, dtype)] at 256-byte
     aligned offsets; returns (buffer, {name: typed view})."""
@@ -290,10 +302,7 @@ def run_device(args, rank: int, world: int):
 
     g_step = capture(step)
     step_us, clocks = timed(g_step, args.steps, args.warmup, clocks=True)
-    if world > 1:
-        t = torch.tensor([step_us], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        step_us = float(t.item())
+    step_us = max_over_ranks(step_us, dev)
     # per-kernel device time inside the step: each timed step is its own graph whose launch of
     # the kernel is bracketed by its own event pair (q2_set_probe); these steps replay back to
     # back after warm-up, like the timed region above
