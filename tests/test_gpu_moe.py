@@ -52,6 +52,7 @@ def test_moe_config_full_size(env):
     dict(E=8, H=256, F=128, M=64, topk=2),     # many rows per expert: several slices
     dict(E=256, H=128, F=64, M=4, topk=16),    # the largest E and top-k
     dict(E=16, H=8192, F=256, M=2, topk=4),    # the largest H
+    dict(E=64, H=4096, F=2048, M=1, topk=6),   # one row: every active expert has a single column
 ])
 def test_shapes(env, over):
     m = synth.config_moe(2, salt=sum(over.values()), **over)
