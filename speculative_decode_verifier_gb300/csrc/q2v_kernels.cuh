@@ -76,9 +76,10 @@ struct MoeWs {
     int *active;      // [E] expert ids with count > 0, ascending; active_n at active[E]
     int *pair_row;    // [M*topk] activation row of each expert-grouped pair
     int *pair_of;     // [M*topk] grouped position of (row, slot)
+    int *slot_of;     // [M*topk] (row, slot) index r*topk + t of each grouped position
     float *gate_w;    // [M*topk] gate weight of (row, slot)
     float *h;         // [KS][2][M*topk][F] fp32 gate and up partial sums per K split
-    float *out;       // [KS][M*topk][H] fp32 down projection partial sums per K split
+    float *out;       // [KS][M*topk][H] fp32 down projection partial sums per K split, by (row, slot)
     PrepPtrs prepX;   // prepared X rows (K = H)
     PrepPtrs prepH;   // prepared h rows (K = F)
 };

@@ -32,7 +32,8 @@ constexpr int kRoutePrepThreads = 256;
 // Routing of the M rows (one CTA): softmax over E, top-k by logit (ties to the lower index),
 // counting sort of the (row, slot) pairs by expert.  E <= 256: a lane keeps its 8 logits in
 // registers across the k arg-max rounds.
-__device__ __forceinline__ void route_rows(const MoeArgs &a, const MoeWs &w, int *s_ids, float *s_g, int *s_cnt) {
+__device__ __forceinline__ void route_rows(const MoeArgs &a, const MoeWs &w, int *s_ids, float *s_g, int *s_cnt,
+                                           int *s_off) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
     const int E = a.E, K = a.topk, M = a.M;
     for (int e = tid; e <= E; e += blockDim.x) s_cnt[e] = 0;
@@ -92,25 +93,53 @@ __device__ __forceinline__ void route_rows(const MoeArgs &a, const MoeWs &w, int
     const int P = M * K;
     for (int p = tid; p < P; p += blockDim.x) atomicAdd(&s_cnt[s_ids[p]], 1);
     __syncthreads();
-    if (tid == 0) {
-        int off = 0, na = 0;
-        for (int e = 0; e < E; ++e) {
-            w.offsets[e] = off;
-            w.counts[e] = s_cnt[e];
-            if (s_cnt[e] > 0) w.active[na++] = e;
-            off += s_cnt[e];
+    if (warp == 0) {
+        // expert offsets and the ascending list of active experts: lane l holds experts
+        // 8l .. 8l+7 (E <= 256), one warp scan of the counts and of the active flags
+        int c[8], sum = 0, nz = 0;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int e = 8 * lane + q;
+            c[q] = e < E ? s_cnt[e] : 0;
+            sum += c[q];
+            nz += c[q] > 0;
         }
-        w.offsets[E] = off;
-        w.active[E] = na;
+        int isum = sum, inz = nz;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int ts = __shfl_up_sync(0xffffffffu, isum, o), tz = __shfl_up_sync(0xffffffffu, inz, o);
+            if (lane >= o) {
+                isum += ts;
+                inz += tz;
+            }
+        }
+        int off = isum - sum, na = inz - nz;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int e = 8 * lane + q;
+            if (e < E) {
+                s_off[e] = off;
+                w.offsets[e] = off;
+                w.counts[e] = c[q];
+                if (c[q] > 0) w.active[na++] = e;
+            }
+            off += c[q];
+        }
+        if (lane == 31) {
+            s_off[E] = isum;
+            w.offsets[E] = isum;
+            w.active[E] = inz;
+        }
     }
     __syncthreads();
     for (int p = tid; p < P; p += blockDim.x) {
         const int r = p / K, e = s_ids[p];
         int before = 0;  // rows < r routed to e (a row picks an expert at most once)
         for (int q = 0; q < r * K; ++q) before += (s_ids[q] == e);
-        const int pos = w.offsets[e] + before;
+        const int pos = s_off[e] + before;
         w.pair_row[pos] = r;
         w.pair_of[p] = pos;
+        w.slot_of[pos] = p;
         w.gate_w[p] = s_g[p];
         if (a.ids_out) a.ids_out[p] = e;
         if (a.w_out) a.w_out[p] = s_g[p];
@@ -124,13 +153,14 @@ __global__ void __launch_bounds__(kRoutePrepThreads) moe_route_prep_kernel(MoeAr
     __shared__ int s_ids[64 * 16];
     __shared__ float s_g[64 * 16];
     __shared__ int s_cnt[257];
+    __shared__ int s_off[257];
     pdl_wait();
     pdl_trigger();
     if ((int)blockIdx.x < a.M) {
         prep_row_bf16(a.X, a.H, (int)blockIdx.x, (int)blockIdx.x, w.prepX, LX, scratch);
         return;
     }
-    route_rows(a, w, s_ids, s_g, s_cnt);
+    route_rows(a, w, s_ids, s_g, s_cnt, s_off);
 }
 
 
@@ -228,7 +258,7 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
     __shared__ int s_off[256];
     __shared__ int s_cnt[256];
     __shared__ int s_prow[64 * 16];
-    __shared__ int s_rows[8], s_exps[8];
+    __shared__ int s_rows[8], s_exps[8], s_orow[8];
     pdl_wait();
     pdl_trigger();
     const int P = a.M * a.topk;
@@ -285,6 +315,9 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
                 const int r = c < mc ? (GATEUP ? s_prow[off + m0 + c] : off + m0 + c) : -1;
                 s_rows[c] = r;
                 s_exps[c] = r >= 0 ? Pp0.exps[r] : 0;
+                // output row: the grouped position (gate/up, read by the h prep in that order)
+                // or the (row, slot) index (down, read by the combine)
+                s_orow[c] = c < mc ? (GATEUP ? off + m0 + c : w.slot_of[off + m0 + c]) : 0;
             }
             __syncthreads();
             stage_act_issue(sm_act, SA, Pp0, L, s_rows, mc);  // the oldest async group
@@ -294,8 +327,7 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
                 for (int qq = 0; qq < 4; ++qq) {
                     const int c = 2 * t + (qq & 1), rr = g + 8 * (qq >> 1);
                     if (c < mc && rr < ui.rows_valid) {
-                        const int pos = off + m0 + c;
-                        dst[(size_t)pos * um.Nrows + ui.n0 + rr] = ldexpf(acc[0][qq] + acc[1][qq], s_exps[c]);
+                        dst[(size_t)s_orow[c] * um.Nrows + ui.n0 + rr] = ldexpf(acc[0][qq] + acc[1][qq], s_exps[c]);
                     }
                     acc[0][qq] = 0.0f;
                     acc[1][qq] = 0.0f;
@@ -381,17 +413,13 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(MoeArgs a, MoeWs w, in
     for (size_t i = (size_t)blockIdx.x * blockDim.x + threadIdx.x; i < (size_t)a.M * H;
          i += (size_t)gridDim.x * blockDim.x) {
         const int r = (int)(i / H), n = (int)(i - (size_t)r * H);
-        int pos[16];
-        float gw[16];
-        for (int t = 0; t < K; ++t) {  // all indices first: one dependent round trip, not K
-            pos[t] = w.pair_of[r * K + t];
-            gw[t] = w.gate_w[r * K + t];
-        }
+        // the down outputs are stored by (row, slot), so the gate weights and the outputs are
+        // independent loads: one round trip
         float y = 0.0f;
         for (int t = 0; t < K; ++t) {
             float o = 0.0f;
-            for (int ks = 0; ks < KS; ++ks) o += w.out[((size_t)ks * P + pos[t]) * H + n];
-            y = fmaf(gw[t], o, y);
+            for (int ks = 0; ks < KS; ++ks) o += w.out[((size_t)ks * P + (size_t)r * K + t) * H + n];
+            y = fmaf(w.gate_w[r * K + t], o, y);
         }
         a.Y[i] = y;
     }

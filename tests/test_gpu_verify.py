@@ -105,14 +105,15 @@ def test_masked_vocabulary(env):
 
 def test_bad_token_sets_status(env):
     dev, q2v, _ = env
-    for V in (1024, 8192):
+    for V, bad in ((1024, None), (8192, None), (1024, -1), (8192, -1)):
         v = synth.config_verify(0, V=V, S=3)
         v["drafts"] = v["drafts"].copy()
-        v["drafts"][1, 2] = V
+        v["drafts"][1, 2] = V if bad is None else bad
         ws = q2v.workspace(q2v.pq_verify_workspace(3, 4, V), dev)
         n, toks, _ = _gpu(env, v, ws=ws)
         assert q2v.q2_get_device_status(ws) == 7  # Q2_ERR_BAD_TOKEN
         assert n[1] == -1 and np.all(toks[1] == -1)
+        assert n[0] >= 0 and n[2] >= 0  # the other sessions are verified as usual
         assert q2v.q2_get_device_status(ws) == 0
 
 
