@@ -51,9 +51,12 @@ q2_status cuda_status(cudaError_t e) { return e == cudaSuccess ? Q2_OK : Q2_ERR_
 
 bool gemm_k_ok(int K) { return K >= kBlockK && K % kBlockK == 0 && K <= kMaxTileWarps * kTileBlocks * kBlockK; }
 
+// Either path's needs (which path runs depends on N and the device), so a workspace sized
+// once fits every call with these M and K.
 size_t gemm_ws_bytes(int M, int K) {
     Carver c(nullptr);
-    c.take(umma_gemm_supported(M, K) ? umma_gemm_ws_bytes(M, K) : PrepLayout(K).bytes(M));
+    const size_t prep = PrepLayout(K).bytes(M);
+    c.take(umma_gemm_usable(M, K) ? std::max(umma_gemm_ws_bytes(M, K), prep) : prep);
     return c.off;
 }
 
@@ -211,10 +214,10 @@ q2_status q2_tiny_gemm(const void *W, int N, int K, const uint16_t *A, int M, in
     if (wst != Q2_OK) return wst;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     Carver c(ws);
-    if (umma_gemm_supported(M, K)) {
+    const int sms = device_sms();
+    if (umma_gemm_preferred(M, N, K, sms)) {
         void *img = c.take(umma_gemm_ws_bytes(M, K));
         if (launch_prep_umma(A, lda, M, K, img, s) != cudaSuccess) return Q2_ERR_CUDA;
-        const int sms = device_sms();
         return cuda_status(probed(kProbeGemm, s, [&] {
             return launch_gemm_umma(W, N, K, M, img, Y, ldy, status_word(ws), sms, s, UmFuse{});
         }));
@@ -288,12 +291,16 @@ size_t q2_lm_head_verify_workspace(int S, int k, int V, int K) {
     const long long M = (long long)S * (k + 1);
     if (S < 1 || k < 0 || k > kMaxDrafts || V < 1 || V > (1 << 28) || M > 64 || !gemm_k_ok(K))
         return Q2_WORKSPACE_HEADER_BYTES;
-    const bool umma = umma_gemm_supported((int)M, K);
-    Carver c(nullptr);
-    c.take(umma ? umma_gemm_ws_bytes((int)M, K) : PrepLayout(K).bytes((int)M));
-    if (umma) c.take((size_t)M * umma_gemm_grid(V, device_sms()) * sizeof(float2));
-    if (V > kWarpTierMaxV) pq_carve_from(c, S, k, V);
-    return c.off;
+    // either GEMM path's regions (the path depends on the shape and the device), then the verify's
+    Carver a(nullptr), b(nullptr);
+    if (umma_gemm_usable((int)M, K)) {
+        a.take(umma_gemm_ws_bytes((int)M, K));
+        a.take((size_t)M * umma_gemm_grid(V, device_sms()) * sizeof(float2));
+        if (V > kWarpTierMaxV) pq_carve_from(a, S, k, V);
+    }
+    b.take(PrepLayout(K).bytes((int)M));
+    if (V > kWarpTierMaxV) pq_carve_from(b, S, k, V);
+    return std::max(a.off, b.off);
 }
 
 q2_status q2_lm_head_verify(const void *W, int V, int K, const uint16_t *A, int lda, const float *draft_logits,
@@ -316,7 +323,7 @@ q2_status q2_lm_head_verify(const void *W, int V, int K, const uint16_t *A, int 
     const int sms = device_sms();
     unsigned int *status = status_word(ws);
     if (flags & ~Q2_LM_HEAD_FUSE_STATS) return Q2_ERR_INVALID_ARG;
-    const bool umma = umma_gemm_supported((int)M, K);
+    const bool umma = umma_gemm_preferred((int)M, V, K, sms);
     const bool fused = (flags & Q2_LM_HEAD_FUSE_STATS) && umma && V > kWarpTierMaxV;
     Carver c(ws);
     // 1. target logits = A W^T (rows s*(k+1) + i), with the target rows' softmax partials

@@ -86,11 +86,16 @@ struct MoeWs {
 
 cudaError_t launch_moe(const MoeArgs &a, const MoeWs &w, int num_sms, cudaStream_t s);
 
-// q2_tiny_gemm on the tcgen05 tensor cores (q2v_umma.cu): kUmmaMinRowsExclusive < M <= 64
-// and K % 128 == 0 (the weight rows then start on 16-byte boundaries, as TMA needs).  The
-// prep writes the activation operand image into a workspace region of umma_gemm_ws_bytes.
-constexpr int kUmmaMinRowsExclusive = 16;
-bool umma_gemm_supported(int M, int K);
+// q2_tiny_gemm on the tcgen05 tensor cores (q2v_umma.cu), for 1 <= M <= 64 and K % 128 == 0
+// (the weight rows then start on 16-byte boundaries, as TMA needs).  umma_gemm_usable says
+// whether a shape can take that path; umma_gemm_preferred picks the faster path for a shape on
+// `sms` SMs: tcgen05 above 16 rows, and at 5..16 rows once there are enough 128-row tiles per
+// SM.  The crossovers, measured on GB300 at K = 4096, are about 108 weight rows per SM at 9..16
+// activation rows (where the mma.sync kernel needs two 8-row slices) and 216 at 5..8 rows; at
+// fewer rows, or fewer weight rows, the mma.sync kernel is the faster one.
+bool umma_gemm_usable(int M, int K);
+bool umma_gemm_preferred(int M, int N, int K, int sms);
+// The prep writes the activation operand image into a workspace region of umma_gemm_ws_bytes.
 size_t umma_gemm_ws_bytes(int M, int K);
 cudaError_t launch_prep_umma(const uint16_t *A, int lda, int M, int K, void *ws_region, cudaStream_t s);
 

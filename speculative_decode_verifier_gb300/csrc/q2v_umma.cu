@@ -776,7 +776,16 @@ cudaError_t launch_umma_variant(const CUtensorMap &map, int N, int nst, const ui
 
 }  // namespace
 
-bool umma_gemm_supported(int M, int K) { return M > kUmmaMinRowsExclusive && M <= 64 && K % 128 == 0; }
+bool umma_gemm_usable(int M, int K) { return M >= 1 && M <= 64 && K % 128 == 0; }
+
+bool umma_gemm_preferred(int M, int N, int K, int sms) {
+    if (!umma_gemm_usable(M, K)) return false;
+    if (M > 16) return true;
+    const long long rows_per_sm = (long long)N / (sms > 0 ? sms : 1);
+    if (M >= 9) return rows_per_sm >= 108;
+    if (M >= 5) return rows_per_sm >= 216;
+    return false;
+}
 
 size_t umma_gemm_ws_bytes(int M, int K) {
     const int npad = cdiv(M, 16) * 16;

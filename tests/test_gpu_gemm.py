@@ -151,7 +151,9 @@ def test_probe_brackets_the_gemm_kernel(env):
         q2v.q2_set_probe(q2v.PROBE_GEMM, None, None)
 
 
-# ---- the tcgen05 path (17 <= M <= 64 with K % 128 == 0); other K fall back to mma.sync
+# ---- the tcgen05 path: K % 128 == 0 and 17 <= M <= 64, or 5 <= M <= 16 with enough 128-row
+# tiles per SM (on a 152-SM GB300: N >= 32,832 at 5..8 rows, N >= 16,416 at 9..16 rows);
+# other shapes take mma.sync
 
 @pytest.mark.parametrize("M,N,K", [
     (17, 129, 128),     # one stage, ragged N just past one 128-row tile, 32-row padding
@@ -166,6 +168,11 @@ def test_probe_brackets_the_gemm_kernel(env):
     (24, 100000, 256),  # 782 tiles: 5-6 per CTA, a full group of 4 then a partial one
     (48, 160000, 128),  # 1250 tiles: 8-9 per CTA, two full groups and a one-tile group
     (33, 50, 160),      # K % 128 != 0: the mma.sync path
+    (5, 33000, 256),    # 5 rows, enough tiles per SM: tcgen05 with 16-column padding, ragged tail
+    (8, 40000, 128),    # 8 rows, one stage
+    (9, 16500, 512),    # 9 rows
+    (16, 20000, 384),   # 16 rows, three stages
+    (4, 50000, 256),    # 4 rows: stays on mma.sync however many weight rows
 ])
 def test_umma_shapes(env, M, N, K):
     st = synth.Streams(5000 + M * 7 + N + K)
