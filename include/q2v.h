@@ -86,8 +86,9 @@ size_t q2_tiny_gemm_workspace(int M, int N, int K);
  *   A    bf16 activations [M][lda] (row-major), 16-byte aligned, lda >= K, lda % 8 == 0.
  *   M    activation rows, 1 <= M <= 64.
  *   Y    fp32 output [M][ldy], ldy >= N, 4-byte aligned.  Fully overwritten for n < N.
- *   ws   workspace of q2_tiny_gemm_workspace(M,N,K) bytes.
- * Accumulation is fp32; each product uses q*d rounded once to fp16 and the offset m
+ *   ws   workspace of q2_tiny_gemm_workspace(M,N,K) bytes (the size depends on M and K only).
+ * The kernel (mma.sync, or tcgen05 for K % 128 == 0 with more rows) is chosen from the shape
+ * and the device; both give the same bound below.  Accumulation is fp32; each product uses q*d rounded once to fp16 and the offset m
  * exactly, and activations converted to fp16 under an exact per-row power-of-two scale, so
  * |Y - exact| stays far below 2e-3 * sum_k |a_k w_k|.  Scales must satisfy |d| < 64 (real
  * 2-bit block scales are orders of magnitude smaller).
