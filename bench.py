@@ -444,6 +444,21 @@ def run_device(args, rank: int, world: int):
                   "gemm_GB/s": (wbytes + Mc * Kc * 2 + Mc * Nc * 4) / (g_us * 1e-6) / 1e9,
                   "gemm_TFLOP/s": 2.0 * Mc * Nc * Kc / (g_us * 1e-6) / 1e12,
                   "gemm_frac_hbm": (wbytes + Mc * Kc * 2 + Mc * Nc * 4) / (g_us * 1e-6) / 1e9 / peak_x}
+        # one session (S=1, k=4: M=5 rows) against the same vocabulary head: the head GEMM and
+        # the verify in one call
+        v1 = synth.verify_inputs(synth.streams(4, salt=2), 1, 4, Nc, 0.0, 1.0, 1.0,
+                                 target=np.zeros((1, 5, Nc), np.float32))
+        D1, x1, ua1, uf1 = D(v1["draft"]), D(v1["drafts"]), D(v1["u_acc"]), D(v1["u_fin"])
+        A1 = Ac[:5].contiguous()
+        Y1h = torch.empty((1, 5, Nc), dtype=torch.float32, device=dev)
+        n1 = torch.empty(1, dtype=torch.int32, device=dev)
+        t1 = torch.empty((1, 5), dtype=torch.int32, device=dev)
+        ws1h = q2v.workspace(q2v.q2_lm_head_verify_workspace(1, 4, Nc, Kc), dev)
+        s_us = graph_us(lambda: q2v.q2_lm_head_verify(Wc, Nc, Kc, A1, D1, x1, ua1, uf1, 1, 4, temperature=1.0,
+                                                      target=Y1h, n_acc=n1, tokens=t1, ws=ws1h),
+                        max(5, args.steps // 2))
+        cohort["session_m5_lm_head_verify_us"] = s_us
+        cohort["session_m5_GB/s"] = (wbytes + 5 * Kc * 2 + 5 * Nc * 4 + 4 * 4 * Nc) / (s_us * 1e-6) / 1e9
         del Wc
 
     # e2e: through the binding, pinned host inputs in, results out, every step.  Each input
