@@ -462,11 +462,14 @@ cudaError_t launch_stream(const MoeArgs &a, const MoeWs &w, int KS, float *out, 
     return launch_stream_variant<GU, false>(GU ? 1 : 3, a, w, KS, out, num_sms, smem, s);
 }
 
-// K splits so that the expected number of units is a few per resident warp.
+// K splits so that the expected number of units is a few per resident warp.  Split ks takes
+// tiles [ks * tps, min(ntk, (ks + 1) * tps)) with tps = cdiv(ntk, KS); the count is then
+// reduced to cdiv(ntk, tps) so that no split is empty (the weight ring would otherwise fetch
+// and multiply a tile past the end of the row for an empty split).
 int choose_ks(int units_without_split, int ntk, int resident_warps) {
     int ks = 1;
     while (ks < kMaxKSplits && ks < ntk && (long long)units_without_split * ks < 2LL * resident_warps) ks *= 2;
-    return ks;
+    return cdiv(ntk, cdiv(ntk, ks));
 }
 }  // namespace
 

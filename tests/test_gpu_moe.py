@@ -53,6 +53,9 @@ def test_moe_config_full_size(env):
     dict(E=256, H=128, F=64, M=4, topk=16),    # the largest E and top-k
     dict(E=16, H=8192, F=256, M=2, topk=4),    # the largest H
     dict(E=64, H=4096, F=2048, M=1, topk=6),   # one row: every active expert has a single column
+    dict(E=32, H=1024, F=96, M=8, topk=4),     # all 8 X rows in one MMA column set
+    dict(E=256, H=2816, F=160, M=7, topk=16),  # 11 K tiles, the largest E and top-k
+    dict(E=8, H=4352, F=64, M=3, topk=2),      # 17 K tiles: 8 splits of 3 would leave 2 empty, so 6 are used
 ])
 def test_shapes(env, over):
     m = synth.config_moe(2, salt=sum(over.values()), **over)
@@ -77,4 +80,12 @@ def test_workspace_reuse(env):
     ws = q2v.workspace(q2v.q2_moe_grouped_workspace(5, 8, 2, 256, 128), dev)
     a, _ = _run(env, m, ws=ws)
     b, _ = _run(env, m, ws=ws)
+    assert np.array_equal(a, b)
+
+
+def test_verifier_shape_is_deterministic(env):
+    # every sum (K tiles, K splits, slots) runs in a fixed order
+    m = synth.config_moe(2, salt=6, E=64, H=4096, F=2048, M=5, topk=6)
+    a, _ = _run(env, m)
+    b, _ = _run(env, m)
     assert np.array_equal(a, b)
