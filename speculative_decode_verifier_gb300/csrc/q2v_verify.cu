@@ -636,14 +636,25 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
         if (VEC) {
             const float4 *t4 = reinterpret_cast<const float4 *>(D.t);
             const float4 *d4 = reinterpret_cast<const float4 *>(D.d);
-            for (int i = (y0 >> 2) + lane; i < (y1 >> 2); i += 32) {
-                const float4 xt = t4[i];
-                const float4 xd = (D.mode == 0) ? d4[i] : xt;
-                wsum += draw_weight(D, beta, xt.x, xd.x) + draw_weight(D, beta, xt.y, xd.y) +
-                        draw_weight(D, beta, xt.z, xd.z) + draw_weight(D, beta, xt.w, xd.w);
-                if (D.mode == 0)
-                    psum += ex2((xt.x - D.mt) * beta - D.lt) + ex2((xt.y - D.mt) * beta - D.lt) +
-                            ex2((xt.z - D.mt) * beta - D.lt) + ex2((xt.w - D.mt) * beta - D.lt);
+            // four float4 of each row per lane in flight before any is used
+            const int i1 = y1 >> 2;
+            for (int i0 = (y0 >> 2) + lane; i0 < i1; i0 += 4 * 32) {
+                float4 xt[4], xd[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + 32 * u;
+                    xt[u] = i < i1 ? t4[i] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                    xd[u] = (i < i1 && D.mode == 0) ? d4[i] : xt[u];
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    if (i0 + 32 * u >= i1) break;
+                    wsum += draw_weight(D, beta, xt[u].x, xd[u].x) + draw_weight(D, beta, xt[u].y, xd[u].y) +
+                            draw_weight(D, beta, xt[u].z, xd[u].z) + draw_weight(D, beta, xt[u].w, xd[u].w);
+                    if (D.mode == 0)
+                        psum += ex2((xt[u].x - D.mt) * beta - D.lt) + ex2((xt[u].y - D.mt) * beta - D.lt) +
+                                ex2((xt[u].z - D.mt) * beta - D.lt) + ex2((xt[u].w - D.mt) * beta - D.lt);
+                }
             }
         } else {
             for (int y = y0 + lane; y < y1; y += 32) {
@@ -690,7 +701,15 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
     CSum own, excl, tot;
     for (int pass = 0; pass < 2; ++pass) {  // pass 1 only when the residual has no mass
         const float *wsrc = (pass == 0 ? sp.mass : sp.pmass) + (size_t)s * nseg;
-        for (int e = tid; e < nseg; e += nt) sm[e] = __ldcg(wsrc + e);
+        // up to 8 loads per thread in flight before any is stored
+        for (int e = tid; e < nseg; e += 8 * nt) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = e + u * nt < nseg ? __ldcg(wsrc + e + u * nt) : 0.0f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (e + u * nt < nseg) sm[e + u * nt] = v[u];
+        }
         __syncthreads();
         own = CSum();
         for (int e = e0; e < e1; ++e) own.add(sm[e]);

@@ -52,6 +52,8 @@ def test_verifier_linear_config(env):
     (64, 32, 4096),    # the largest M
     (5, 64, 8192),     # the largest K (32 warp tiles)
     (1, 1, 32),        # the smallest problem
+    (6, 4100, 4064),   # a ragged last 16-row group at the verifier width; 127 blocks (odd), a partial 16th tile
+    (8, 4864, 1024),   # 8 rows in one activation slice, 304 row groups
 ])
 def test_shapes(env, M, N, K):
     st = synth.Streams(1000 + M * 7 + N + K)
