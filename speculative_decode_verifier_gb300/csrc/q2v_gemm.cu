@@ -88,7 +88,7 @@ __global__ void __launch_bounds__(kGemmWarps * 32) q2_gemm_mma_kernel(const uint
 }
 
 namespace {
-size_t g_gemm_smem[2];  // dynamic shared memory each variant was configured for
+size_t g_gemm_smem[kCacheDevices][2];  // dynamic shared memory each variant was configured for, per device
 
 template <bool A8>
 cudaError_t launch_gemm_variant(const uint8_t *w, int N, int K, const PrepPtrs &P, const PrepLayout &L, int M,
@@ -96,10 +96,11 @@ cudaError_t launch_gemm_variant(const uint8_t *w, int N, int K, const PrepPtrs &
     auto kern = q2_gemm_mma_kernel<A8>;
     const int ncols = min(8, M);
     const size_t smem = SmemAct(L, ncols).bytes();
-    if (g_gemm_smem[A8] < smem) {
+    const int dv = cache_device();
+    if (dv < 0 || g_gemm_smem[dv][A8] < smem) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        g_gemm_smem[A8] = smem;
+        if (dv >= 0) g_gemm_smem[dv][A8] = smem;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(cdiv(N, kRowsPerCta));

@@ -6,6 +6,16 @@
 
 namespace q2v {
 
+// Host-side caches of per-device launch state (a kernel's dynamic shared-memory opt-in and its
+// occupancy are properties of a device) are indexed by the current device's ordinal; an
+// ordinal beyond the cache (-1 here) is served without caching.
+constexpr int kCacheDevices = 64;
+inline int cache_device() {
+    int d = 0;
+    if (cudaGetDevice(&d) != cudaSuccess || d < 0 || d >= kCacheDevices) return -1;
+    return d;
+}
+
 // ------------------------------------------------------------------ GEMM
 
 cudaError_t launch_prep_bf16(const uint16_t *src, int ld, const int *rows, int R, int K, const PrepPtrs &P,

@@ -426,23 +426,29 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(MoeArgs a, MoeWs w, in
 }
 
 namespace {
-int g_stream_blocks[4];  // resident CTAs per SM of the four stream-kernel variants (0 = unknown)
-size_t g_stream_smem[4];  // dynamic shared memory each variant was configured for
+// per device: resident CTAs per SM of the four stream-kernel variants (0 = unknown) and the
+// dynamic shared memory each was configured for
+int g_stream_blocks[kCacheDevices][4];
+size_t g_stream_smem[kCacheDevices][4];
 
 template <bool GU, bool A8>
 cudaError_t launch_stream_variant(int idx, const MoeArgs &a, const MoeWs &w, int KS, float *out, int num_sms,
                                   size_t smem, cudaStream_t s) {
     auto kern = moe_stream_kernel<GU, A8>;
-    if (g_stream_smem[idx] < smem) {
+    const int dv = cache_device();
+    int blocks = dv >= 0 ? g_stream_blocks[dv][idx] : 0;
+    if (dv < 0 || g_stream_smem[dv][idx] < smem) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, 256, smem) != cudaSuccess || n <= 0) n = 1;
-        g_stream_blocks[idx] = n;
-        g_stream_smem[idx] = smem;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, 256, smem) != cudaSuccess || blocks <= 0)
+            blocks = 1;
+        if (dv >= 0) {
+            g_stream_blocks[dv][idx] = blocks;
+            g_stream_smem[dv][idx] = smem;
+        }
     }
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(num_sms * g_stream_blocks[idx]);
+    cfg.gridDim = dim3(num_sms * blocks);
     cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

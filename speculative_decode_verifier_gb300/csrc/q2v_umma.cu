@@ -748,7 +748,7 @@ EncodeTiledFn encode_tiled() {
     return fn;
 }
 
-size_t g_umma_smem[4];  // dynamic shared memory each NPAD variant was configured for
+size_t g_umma_smem[kCacheDevices][4];  // dynamic shared memory each NPAD variant was configured for, per device
 
 template <int NPAD>
 cudaError_t launch_umma_variant(const CUtensorMap &map, int N, int nst, const uint8_t *img, const int *exps, int M,
@@ -756,11 +756,11 @@ cudaError_t launch_umma_variant(const CUtensorMap &map, int N, int nst, const ui
                                 const UmFuse &fz) {
     auto kern = q2_gemm_umma_kernel<NPAD>;
     const size_t smem = um_smem_bytes(NPAD);
-    size_t &have = g_umma_smem[NPAD / 16 - 1];
-    if (have < smem) {
+    const int dv = cache_device();
+    if (dv < 0 || g_umma_smem[dv][NPAD / 16 - 1] < smem) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        have = smem;
+        if (dv >= 0) g_umma_smem[dv][NPAD / 16 - 1] = smem;
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(umma_gemm_grid(N, num_sms));
