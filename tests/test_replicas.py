@@ -60,5 +60,10 @@ def test_reference_arm_prints_on_rank_zero_only(rank, expect_output):
     if expect_output:
         d = json.loads(lines[-1])
         assert d["impl"] == "reference" and d["higher_is_better"] is False and d["value"] > 0
+        # the line reports exactly the steps it ran, and the contract's e2e and baseline blocks
+        assert d["steps"] == 1 and d["warmup"] == 3
+        assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
+        cb = d["cpu_baseline"]
+        assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
     else:
         assert lines == []
