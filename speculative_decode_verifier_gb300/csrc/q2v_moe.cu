@@ -13,9 +13,9 @@
 //                (pairs of one expert ordered by row), the list of active experts;
 //   2. prep X:   the activation rows in the small-M GEMM's B-operand layout;
 //   3. gate/up:  one grouped GEMM over units (active expert, gate|up, 16-row group, K split);
-//                each warp streams whole units with a one-tile register lookahead, with no
-//                shared memory and no barriers; every active expert's weights are read
-//                once for all rows routed to it;
+//                a CTA stages the prepared rows of each expert run in shared memory once, and
+//                each warp streams its units' weight tiles through its own cp.async ring;
+//                every active expert's weights are read once for all rows routed to it;
 //   4. prep h:   h = silu(sum of gate splits) * (sum of up splits), fused into the B-operand
 //                prep of the down GEMM;
 //   5. down:     the same grouped GEMM over (active expert, 16-row group, K split) units;
