@@ -72,6 +72,7 @@ def test_batched_config_full_size(env):
     (3, 0, 5000, 1.0),       # k = 0: plain sampling from p_0
     (9, 0, 300, 0.9),        # k = 0 in the warp tier
     (4, 2, 1, 1.0),          # V = 1
+    (4, 4, 129280, 50.0),    # near-uniform p and q: CDF cells ~7.7e-6 wide, residuals of nearly equal probabilities
 ])
 def test_shapes(env, S, k, V, T):
     st = synth.Streams(5000 + S + 31 * k + V)
