@@ -388,7 +388,16 @@ def test_chi_square_detects_a_planted_mistake(orc):
 # ----------------------------------------------------------------- MoE
 
 def _silu(z):
-    return z / (1 + np.exp(-z))
+    # z * sigmoid(z) through scipy's logistic function, not the oracle's own expression
+    return z * scipy.special.expit(z)
+
+
+def test_silu_reference_identities():
+    # silu(z) - silu(-z) = z (sigmoid(z) + sigmoid(-z) = 1), silu(0) = 0, silu(z) -> z for large z
+    z = np.linspace(-30.0, 30.0, 601)
+    np.testing.assert_allclose(_silu(z) - _silu(-z), z, rtol=0, atol=1e-12)
+    assert _silu(np.array([0.0]))[0] == 0.0
+    np.testing.assert_allclose(_silu(np.array([40.0])), [40.0], rtol=1e-15)
 
 
 def test_moe_single_expert_reduces_to_three_gemms(orc):
