@@ -304,6 +304,21 @@ q2_status q2_set_probe(int kernel, void *ev_begin, void *ev_end);
  * return it (Q2_OK if no device error was recorded since the last read). */
 q2_status q2_get_device_status(const void *ws, q2_stream_t stream);
 
+/* ------------------------------------------------------------------ failure detection */
+
+/* Self-test of device-side failure detection; the verifier method has no counterpart.  Every
+ * wait inside the library's kernels is bounded: the tcgen05 GEMM's roles wait on mbarriers for
+ * at most 1 s, then record Q2_ERR_TIMEOUT and wind down.  This call exercises that give-up
+ * path without a GPU fault.  It launches one CTA on `stream` in which one thread performs the
+ * same bounded mbarrier wait on a barrier that nothing completes.  After 1 s the wait gives
+ * up, Q2_ERR_TIMEOUT goes into the status word of `ws`, the kernel returns, and the context
+ * stays usable, so the next q2_get_device_status(ws) returns Q2_ERR_TIMEOUT.
+ *   ws  device workspace of at least Q2_WORKSPACE_HEADER_BYTES, 16-byte aligned; only its
+ *       status word is written.
+ * Errors: Q2_ERR_WORKSPACE for a NULL, misaligned or too small workspace; Q2_ERR_CUDA if the
+ * launch fails. */
+q2_status q2_selftest_wait_timeout(void *ws, size_t ws_bytes, q2_stream_t stream);
+
 /* Static description of a status code. */
 const char *q2_status_string(q2_status status);
 

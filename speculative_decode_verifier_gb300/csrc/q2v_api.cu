@@ -183,6 +183,12 @@ const char *q2_status_string(q2_status s) {
     return "unknown status";
 }
 
+q2_status q2_selftest_wait_timeout(void *ws, size_t ws_bytes, q2_stream_t stream) {
+    const q2_status wst = check_ws(ws, ws_bytes, Q2_WORKSPACE_HEADER_BYTES);
+    if (wst != Q2_OK) return wst;
+    return cuda_status(launch_wait_selftest(status_word(ws), reinterpret_cast<cudaStream_t>(stream)));
+}
+
 q2_status q2_get_device_status(const void *ws, q2_stream_t stream) {
     if (!ws || !aligned(ws, 16)) return Q2_ERR_WORKSPACE;
     unsigned int st = 0;

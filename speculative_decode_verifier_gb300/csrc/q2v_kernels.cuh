@@ -126,6 +126,10 @@ cudaError_t launch_gemm_umma(const void *W, int N, int K, int M, const void *ws_
 // statistics are one partial per CTA.
 inline int umma_gemm_grid(int N, int num_sms) { return N < 1 ? 1 : (cdiv(N, 128) < num_sms ? cdiv(N, 128) : num_sms); }
 
+// One CTA whose bounded mbarrier wait runs out and records Q2_ERR_TIMEOUT in *status
+// (q2_selftest_wait_timeout, q2v_umma.cu).
+cudaError_t launch_wait_selftest(unsigned int *status, cudaStream_t s);
+
 // Measurement hook (q2_set_probe): records the caller's begin (end = 0) or end (end = 1)
 // event on s when `kernel` is the bracketed one; a no-op otherwise.
 enum ProbeKernel : int { kProbeMoeGateUp = 1, kProbeMoeDown = 2, kProbeGemm = 3, kProbePqStats = 4, kProbePqVerify = 5 };

@@ -794,6 +794,29 @@ size_t umma_gemm_ws_bytes(int M, int K) {
     return align_up((size_t)nst * um_bstage(npad), 256) + 256;
 }
 
+// The bounded wait's give-up path (q2_selftest_wait_timeout): one thread waits, through the
+// same um_wait the GEMM's roles use, on an mbarrier that nothing arrives on.  It holds no
+// copies and no tensor memory, so after the wait runs out the kernel simply returns.
+__global__ void __launch_bounds__(32) q2_wait_selftest_kernel(unsigned int *status) {
+    __shared__ __align__(8) uint64_t bar;
+    __shared__ uint32_t abort_flag;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        abort_flag = 0u;
+        fence_mbar_init();
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) (void)um_wait(&bar, 0u, &abort_flag, status);
+}
+
+cudaError_t launch_wait_selftest(unsigned int *status, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1);
+    cfg.blockDim = dim3(32);
+    cfg.stream = s;
+    return cudaLaunchKernelEx(&cfg, q2_wait_selftest_kernel, status);
+}
+
 cudaError_t launch_prep_umma(const uint16_t *A, int lda, int M, int K, void *ws_region, cudaStream_t s) {
     const int nb = K / kBlockK;
     const int nst = cdiv(nb, kUmBlocks);

@@ -25,7 +25,7 @@ LM_HEAD_FUSE_STATS = 1
 EXPORTS = ("q2_tiny_gemm_workspace", "q2_tiny_gemm", "q2_moe_grouped_workspace", "q2_moe_grouped",
            "pq_verify_workspace", "pq_verify", "pq_verify_noalloc", "q2_get_device_status", "q2_status_string",
            "q2_version", "q2_set_probe", "pq_verify_ex", "q2_quench_init", "q2_quench_update",
-           "q2_lm_head_verify_workspace", "q2_lm_head_verify")
+           "q2_lm_head_verify_workspace", "q2_lm_head_verify", "q2_selftest_wait_timeout")
 
 # kernels that q2_set_probe can bracket (q2_probe_kernel)
 PROBE_NONE, PROBE_MOE_GATE_UP, PROBE_MOE_DOWN, PROBE_GEMM, PROBE_PQ_STATS, PROBE_PQ_VERIFY = range(6)
@@ -82,6 +82,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q2_quench_update.restype = I
     lib.q2_set_probe.argtypes = [I, P, P]
     lib.q2_set_probe.restype = I
+    lib.q2_selftest_wait_timeout.argtypes = [P, Z, P]
+    lib.q2_selftest_wait_timeout.restype = I
     _lib = lib
     return lib
 
@@ -205,6 +207,14 @@ def workspace(nbytes: int, device=None) -> torch.Tensor:
 
 def q2_get_device_status(ws: torch.Tensor, stream=None) -> int:
     return load().q2_get_device_status(_ptr(ws), ctypes.c_void_p(_stream(stream)))
+
+
+def q2_selftest_wait_timeout(ws: torch.Tensor, stream=None) -> None:
+    """Launch the failure-detection self-test: a bounded device wait that nothing completes
+    records Q2_ERR_TIMEOUT in ws's status word after 1 s (read it with q2_get_device_status)."""
+    _check(ws, "ws", torch.uint8)
+    _raise(load().q2_selftest_wait_timeout(_ptr(ws), ws.numel(), ctypes.c_void_p(_stream(stream))),
+           "q2_selftest_wait_timeout")
 
 
 # ------------------------------------------------------------------ entry points

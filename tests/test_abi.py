@@ -135,6 +135,13 @@ def test_moe_host_errors(lib):
     assert _moe(lib, wsb=1000) == 4
 
 
+def test_selftest_wait_timeout_host_errors(lib):
+    # workspace checks come before any launch
+    assert lib.q2_selftest_wait_timeout(None, 1 << 20, None) == 4
+    assert lib.q2_selftest_wait_timeout(FAKE_MIS, 1 << 20, None) == 4
+    assert lib.q2_selftest_wait_timeout(FAKE, 100, None) == 4
+
+
 def test_python_binding_refuses_cpu_tensors():
     import torch
 
