@@ -76,8 +76,8 @@ size_t q2_tiny_gemm_workspace(int M, int N, int K);
 /*
  * Y[m][n] = sum_k A[m][k] * w[n][k]  for m < M, n < N   (Y = A W^T, fp32 out).
  *
- * The "projections and the vocabulary head" of the K+1-row verify (page 2 of the
- * thread above, verifier-bottleneck reply) with the tiny-batch matmul shapes of
+ * The projection matmuls and the vocabulary head that the K+1-row verify runs (page 2 of
+ * the thread above, verifier-bottleneck reply) with the tiny-batch matmul shapes of
  * post #1 (K+1 = 1..5 rows per session; up to 12 sessions batched in the cohort
  * post #20 describes).
  *
@@ -141,8 +141,8 @@ size_t pq_verify_workspace(int S, int k, int V);
  * Exact p/q rejection-sampling verify for S independent sessions of k drafts each
  * ("Optimizing DeepSeek-V4-Flash ...", page 1, opening post: drafts are sampled from
  * q, the target defines p, accepted tokens follow min(1, p(x)/q(x)), rejected drafts
- * are replaced from the positive residual distribution; posts #12 and #20: "exact
- * residual correction"; "1x Spark tuned DSpark ...", deep-dive, "On losslessness":
+ * are replaced from the positive residual distribution; posts #12 and #20 describe the
+ * correction as exact; "1x Spark tuned DSpark ...", deep-dive, "On losslessness":
  * the verify rows are the only token source, drawn with the request's own sampler).
  *
  * For session s:  p_i = softmax(target[s][i] / T) (i = 0..k),  q_i = softmax(draft[s][i] / T)
@@ -201,11 +201,13 @@ q2_status pq_verify_ex(const float *target_logits, const float *draft_logits,
  *
  * Arguments and results are those of pq_verify, minus ws/ws_bytes.  The scratch is a fixed
  * 2 MiB array in device memory that the library holds on every device that loads it, until
- * the process exits; nothing is allocated.  Sizes whose pq_verify_workspace(S, k, V) exceeds
- * 2 MiB are refused with Q2_ERR_UNSUPPORTED before anything is enqueued (S = 24 sessions of
- * k = 4 drafts at V = 129,280 fit).  The first call on a device looks up the array's device
- * address once (make that first call before any stream capture).  Every call shares the one
- * array and clears its status word; calls that may overlap on the GPU (other streams,
+ * the process exits; nothing is allocated.  Host-detectable errors return before anything is
+ * enqueued: the argument errors of pq_verify, and Q2_ERR_UNSUPPORTED for sizes whose
+ * pq_verify_workspace(S, k, V) exceeds 2 MiB (at k = 4 drafts and V = 129,280, up to S = 15
+ * sessions fit; S = 16 does not).  Each call looks up the array's address on the current
+ * device (a host-side query; the first lookup on a device may load the library's device code
+ * there, so make the first call on each device before any stream capture).  Every call shares
+ * the one array and clears its status word; calls that may overlap on the GPU (other streams,
  * other host threads) race on it and must be ordered by the caller.  Device-detected errors
  * show in the outputs: a session with a draft token outside [0, V) gets n_accepted = -1.
  */
@@ -222,9 +224,9 @@ size_t q2_lm_head_verify_workspace(int S, int k, int V, int K);
 /*
  * The vocabulary head of the K+1-row verify followed by the p/q verify over its logits, with
  * the GEMM's epilogue fused with the verify's softmax statistics ("Optimizing DeepSeek-V4-Flash
- * ...", page 2, verifier-bottleneck reply: the verify runs "the vocabulary head" over the K+1
- * rows; post #1 paragraph after the analyzer output: "fusing several operations ... reducing
- * intermediate memory traffic").
+ * ...", page 2, verifier-bottleneck reply: the vocabulary head is part of the K+1-row verify;
+ * post #1, paragraph after the analyzer output: fused operations cut the memory traffic
+ * between steps).
  *   target_logits[s][i][:] = A[s*(k+1) + i] W^T   (as q2_tiny_gemm, N = V), written to the
  *                 caller's fp32 [S][k+1][V] buffer (16-byte aligned), then
  *   the verify of pq_verify_ex (temperatures non-NULL: device fp32 [S], 0 = greedy) or of

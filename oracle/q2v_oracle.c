@@ -22,8 +22,8 @@
  *    page 1, opening post, paragraph after the analyzer output: drafts are drawn
  *    from q, the target defines p, a draft is accepted with probability
  *    min(1, p(x)/q(x)), and a rejected draft is replaced from the positive
- *    residual distribution; the same thread's posts #12 and #20 call this
- *    "exact residual correction").  When every draft is accepted the one extra
+ *    residual distribution; the same thread's posts #12 and #20 describe the
+ *    correction as exact).  When every draft is accepted the one extra
  *    token is drawn from the last target row ("1x Spark tuned DSpark for
  *    DeepSeek-V4-Flash ...", deep-dive, "On losslessness": the verify forward is
  *    the only token source and the accept loop samples from the verify-row

@@ -376,6 +376,21 @@ q2_status q2_lm_head_verify(const void *W, int V, int K, const uint16_t *A, int 
     return cuda_status(launch_pq_verify(a, sp, V <= kWarpTierMaxV, sms, s));
 }
 
+}  // extern "C"
+
+// The host-side checks pq_verify makes before it enqueues anything (temperature, pointers,
+// sizes, alignment), for callers that must reject bad arguments before touching the stream.
+q2_status q2v::pq_verify_precheck(const float *target_logits, const float *draft_logits,
+                                  const int32_t *draft_tokens, const float *u_acc, const float *u_fin, int S,
+                                  int k, int V, float temperature, int32_t *n_accepted, int32_t *out_tokens,
+                                  float *probs_out) {
+    if (!(temperature > 0.0f) || !isfinite(temperature)) return Q2_ERR_INVALID_ARG;
+    return pq_check_args(target_logits, draft_logits, draft_tokens, u_acc, u_fin, S, k, V, n_accepted,
+                         out_tokens, probs_out);
+}
+
+extern "C" {
+
 q2_status pq_verify_ex(const float *target_logits, const float *draft_logits, const int32_t *draft_tokens,
                        const float *u_acc, const float *u_fin, int S, int k, int V, const float *temperatures,
                        int32_t *n_accepted, int32_t *out_tokens, float *probs_out, void *ws, size_t ws_bytes,

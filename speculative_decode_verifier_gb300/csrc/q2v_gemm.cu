@@ -1,6 +1,6 @@
 // q2v_gemm.cu -- activation prep and the small-M Q2B32 dequant GEMM (Y = A W^T).
 //
-// The "projections and the vocabulary head" of the K+1-row verify ("Optimizing
+// The projection matmuls and the vocabulary head of the K+1-row verify ("Optimizing
 // DeepSeek-V4-Flash on a single NVIDIA GB10/GX10 with DSpark speculative decoding",
 // page 2, verifier-bottleneck reply) at the tiny-batch shapes of the opening post
 // (about 5 target rows per verify).  The pages' own kernels were tiny-batch HMMA

@@ -63,6 +63,11 @@ struct PqSplit {
 };
 
 cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier, int num_sms, cudaStream_t st);
+// pq_verify's host-side argument checks alone (q2v_api.cu): Q2_OK or the status pq_verify would
+// return for these arguments before enqueueing anything.
+q2_status pq_verify_precheck(const float *target_logits, const float *draft_logits, const int32_t *draft_tokens,
+                             const float *u_acc, const float *u_fin, int S, int k, int V, float temperature,
+                             int32_t *n_accepted, int32_t *out_tokens, float *probs_out);
 
 // ------------------------------------------------------------------ routed MoE
 

@@ -1,7 +1,7 @@
 // q2v_moe.cu -- routed-expert FFN of the verify forward on sm_103a.
 //
-// The verifier "repeatedly executes attention, routed MoE, projections and the
-// vocabulary head" over the K+1 rows ("Optimizing DeepSeek-V4-Flash on a single NVIDIA
+// Each verify runs the routed-expert FFN (with attention, the projections and the vocabulary
+// head) over the K+1 rows ("Optimizing DeepSeek-V4-Flash on a single NVIDIA
 // GB10/GX10 with DSpark speculative decoding", page 2, verifier-bottleneck reply); the
 // engines fused the router, fused gate+up+SwiGLU for decode ("1x Spark tuned DSpark for
 // DeepSeek-V4-Flash ...", reply on the decode arc) and deduplicated expert reads across

@@ -11,14 +11,11 @@
 namespace {
 
 // The fixed scratch.  Every device that loads the library holds these bytes until the
-// process exits.  In host code `g_pq_scratch` only names the symbol: its device address is
-// obtained with cudaGetSymbolAddress (once per device) and that address is what the kernels
-// receive.
+// process exits.  In host code `g_pq_scratch` only names the symbol: its device address on
+// the current device is obtained with cudaGetSymbolAddress, and that address is what the
+// kernels receive.
 constexpr size_t kNoAllocScratchBytes = (size_t)2 << 20;  // 2 MiB
 static __device__ __align__(256) unsigned char g_pq_scratch[kNoAllocScratchBytes];
-
-constexpr int kMaxNoAllocDevices = 64;
-void *g_scratch_addr[kMaxNoAllocDevices];  // device address of g_pq_scratch, per device
 
 }  // namespace
 
@@ -26,18 +23,17 @@ extern "C" q2_status pq_verify_noalloc(const float *target_logits, const float *
                                        const int32_t *draft_tokens, const float *u_acc, const float *u_fin,
                                        int S, int k, int V, float temperature, int32_t *n_accepted,
                                        int32_t *out_tokens, float *probs_out, q2_stream_t stream) {
-    // the same scratch layout pq_verify uses; sizes it cannot hold are refused up front
-    const size_t need = pq_verify_workspace(S, k, V);
-    if (need > kNoAllocScratchBytes) return Q2_ERR_UNSUPPORTED;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxNoAllocDevices) return Q2_ERR_CUDA;
-    if (g_scratch_addr[dev] == nullptr) {
-        // one-time set-up on this device (with this device current)
-        void *p = nullptr;
-        if (cudaGetSymbolAddress(&p, g_pq_scratch) != cudaSuccess || p == nullptr) return Q2_ERR_CUDA;
-        g_scratch_addr[dev] = p;
-    }
-    void *ws = g_scratch_addr[dev];
+    // everything the host can reject is rejected before any work is enqueued: the arguments
+    // as pq_verify checks them, then sizes whose scratch (the layout pq_verify uses) would not
+    // fit the fixed array
+    const q2_status ast = q2v::pq_verify_precheck(target_logits, draft_logits, draft_tokens, u_acc, u_fin, S, k,
+                                                  V, temperature, n_accepted, out_tokens, probs_out);
+    if (ast != Q2_OK) return ast;
+    if (pq_verify_workspace(S, k, V) > kNoAllocScratchBytes) return Q2_ERR_UNSUPPORTED;
+    // the array's address on the current device, looked up on every call (a host-side query),
+    // so no cached address is shared between host threads or outlives a device reset
+    void *ws = nullptr;
+    if (cudaGetSymbolAddress(&ws, g_pq_scratch) != cudaSuccess || ws == nullptr) return Q2_ERR_CUDA;
     // the array keeps the previous call's contents: the status word must start at zero (the
     // kernels reset their own counters and overwrite every partial they read)
     if (cudaMemsetAsync(ws, 0, Q2_WORKSPACE_HEADER_BYTES, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)

@@ -1,7 +1,7 @@
 // q2v_umma.cu -- the Q2B32 dequant GEMM on the fifth-generation tensor cores (tcgen05), for
 // the wider verify batches: more than 16 activation rows, such as 12 sessions x (k+1) = 60
 // rows against the vocabulary head, and 5..16 rows against many weight rows, such as one
-// session's vocabulary head ("projections and the vocabulary head" of the K+1-row verify,
+// session's vocabulary head (the vocabulary head is one of the matmuls of the K+1-row verify,
 // "Optimizing DeepSeek-V4-Flash on a single NVIDIA GB10/GX10 with DSpark speculative
 // decoding", page 2, verifier-bottleneck reply).  At 60 rows the contraction is as heavy as
 // the weight stream (about 250 flop per weight byte), so both the tensor cores and HBM have to

@@ -148,3 +148,23 @@ def test_python_binding_refuses_cpu_tensors():
     from speculative_decode_verifier_gb300 import q2v
     with pytest.raises(ValueError):
         q2v.q2_tiny_gemm(torch.zeros(16, dtype=torch.uint8), 1, 32, torch.zeros((1, 32), dtype=torch.int16))
+
+
+def _noalloc(lib, S=2, k=4, V=129280, T=1.0, t=FAKE):
+    return lib.pq_verify_noalloc(t, FAKE, FAKE, FAKE, FAKE, S, k, V, T, FAKE, FAKE, None, None)
+
+
+def test_noalloc_size_limit_and_host_errors(lib):
+    """The no-workspace verify holds a 2 MiB scratch: at k = 4, V = 129,280 the largest S whose
+    pq_verify workspace fits is 15; S = 16 is refused with Q2_ERR_UNSUPPORTED.  Argument errors come
+    back as pq_verify's, and every refusal happens before anything is enqueued (no device is
+    touched here)."""
+    assert lib.pq_verify_workspace(15, 4, 129280) <= 2 << 20
+    assert lib.pq_verify_workspace(16, 4, 129280) > 2 << 20
+    assert _noalloc(lib, S=16) == 3
+    assert _noalloc(lib, S=4096, k=16) == 3
+    assert _noalloc(lib, T=-1.0) == 1
+    assert _noalloc(lib, T=float("nan")) == 1
+    assert _noalloc(lib, S=0) == 1
+    assert _noalloc(lib, k=17) == 3
+    assert _noalloc(lib, t=FAKE_MIS) == 2

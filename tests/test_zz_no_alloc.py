@@ -74,3 +74,35 @@ def test_noalloc_refuses_sizes_beyond_its_scratch(env):
     assert q2v.pq_verify_workspace(S, k, V) > (2 << 20)
     st = lib.pq_verify_noalloc(fake, fake, fake, fake, fake, S, k, V, 1.0, fake, fake, None, None)
     assert st == 3  # Q2_ERR_UNSUPPORTED
+
+
+def _driver():
+    """libcuda (the driver API) through ctypes: stream capture and graph node counts."""
+    drv = ctypes.CDLL("libcuda.so.1")
+    begin = getattr(drv, "cuStreamBeginCapture_v2", None) or drv.cuStreamBeginCapture
+    begin.argtypes = [ctypes.c_void_p, ctypes.c_int]
+    drv.cuStreamEndCapture.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_void_p)]
+    drv.cuGraphGetNodes.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.POINTER(ctypes.c_size_t)]
+    drv.cuGraphDestroy.argtypes = [ctypes.c_void_p]
+    return drv, begin
+
+
+def test_noalloc_rejected_call_enqueues_nothing(env):
+    """A call refused on the host (bad temperature, oversized S) adds no work to the stream: a
+    capture around it yields a graph with no nodes."""
+    import torch
+    dev, q2v, lib = env
+    drv, begin = _driver()
+    s = torch.cuda.Stream(device=dev)
+    fake = ctypes.c_void_p(1 << 20)  # never dereferenced: both calls are refused on the host
+    for S, T, want in ((2, -1.0, 1), (16, 1.0, 3)):
+        assert begin(ctypes.c_void_p(s.cuda_stream), 2) == 0  # relaxed capture mode
+        st = lib.pq_verify_noalloc(fake, fake, fake, fake, fake, S, 4, 129280, T, fake, fake, None,
+                                   ctypes.c_void_p(s.cuda_stream))
+        graph = ctypes.c_void_p()
+        assert drv.cuStreamEndCapture(ctypes.c_void_p(s.cuda_stream), ctypes.byref(graph)) == 0
+        n = ctypes.c_size_t(0)
+        assert drv.cuGraphGetNodes(graph, None, ctypes.byref(n)) == 0
+        drv.cuGraphDestroy(graph)
+        assert st == want
+        assert n.value == 0
