@@ -442,6 +442,90 @@ def test_moe_routing_and_combine_brute_force(orc, renorm):
         assert np.all(out["tol"][r] > 0)
 
 
+def _silu_derivative():
+    """d silu / dz, differentiated symbolically by sympy from z / (1 + exp(-z)) (not the
+    oracle's closed form), as a numpy function."""
+    sympy = pytest.importorskip("sympy")
+    z = sympy.Symbol("z", real=True)
+    return sympy.lambdify(z, sympy.diff(z / (1 + sympy.exp(-z)), z), "numpy")
+
+
+def _moe_tol_numpy(gq, uq, dq, ids, w, x, rel=2e-3):
+    """The MoE parity bound from its definition, with numpy matrix products: per output n,
+    sum over the row's slots of g * (rel * sum_f |h_f wd_nf| + sum_f |wd_nf| dh_f), where
+    dh_f = |d silu(gate_f)/d gate * up_f| * tol_gate_f + |silu(gate_f)| * tol_up_f and tol_gate,
+    tol_up are the GEMM bounds rel * sum_k |x_k w_fk| of the gate and up projections."""
+    dsilu = _silu_derivative()
+    tol = np.zeros(dq.shape[1])
+    for t, e in enumerate(ids):
+        gate, up = gq[e] @ x, uq[e] @ x
+        tg, tu = rel * (np.abs(gq[e]) @ np.abs(x)), rel * (np.abs(uq[e]) @ np.abs(x))
+        h = _silu(gate) * up
+        dh = np.abs(dsilu(gate) * up) * tg + np.abs(_silu(gate)) * tu
+        tol += w[t] * (rel * (np.abs(dq[e]) @ np.abs(h)) + np.abs(dq[e]) @ dh)
+    return tol
+
+
+def test_silu_derivative_reference_matches_finite_differences():
+    dsilu = _silu_derivative()
+    z = np.linspace(-12.0, 12.0, 97)
+    eps = 1e-6
+    fd = (_silu(z + eps) - _silu(z - eps)) / (2 * eps)
+    np.testing.assert_allclose(dsilu(z), fd, rtol=0, atol=1e-8)
+
+
+@pytest.mark.parametrize("renorm", [False, True])
+def test_moe_tolerance_matches_its_definition(orc, renorm):
+    """The oracle's MoE bound `tol` equals the bound recomputed from its definition (the GEMM
+    rule 2e-3 * sum |a w| carried through silu(gate) * up to first order, then through the down
+    projection and the gate weights) on the brute-force routing case; a dropped gate weight,
+    a wrong derivative or a 10x relative factor would each change it far beyond 1e-12."""
+    st = synth.Streams(22)
+    E, H, F, M, topk = 4, 32, 64, 3, 2
+    Wg = synth.q2b32_weights(st, F, H, batch=E)
+    Wu = synth.q2b32_weights(st, F, H, batch=E)
+    Wd = synth.q2b32_weights(st, H, F, batch=E)
+    X = synth.activations_bf16(st, M, H)
+    router = st["router"].normal(0, 1, size=(M, E)).astype(np.float32)
+    out = orc.moe(Wg, Wu, Wd, E, H, F, topk, X, router, renorm=renorm)
+    x = synth.bf16_bits_to_f32(X).astype(np.float64)
+    gq = orc.dequant(Wg, E * F, H).reshape(E, F, H)
+    uq = orc.dequant(Wu, E * F, H).reshape(E, F, H)
+    dq = orc.dequant(Wd, E * H, F).reshape(E, H, F)
+    for r in range(M):
+        prob = scipy.special.softmax(router[r].astype(np.float64))
+        ids = np.argsort(-prob, kind="stable")[:topk]
+        w = prob[ids] / (prob[ids].sum() if renorm else 1.0)
+        want = _moe_tol_numpy(gq, uq, dq, ids, w, x[r])
+        np.testing.assert_allclose(out["tol"][r], want, rtol=1e-12, atol=0)
+
+
+def _q2b32_constant_rows(n_rows, K, code, d_bits, m_bits=0):
+    """Q2B32 bytes of n_rows x K weights, every code equal to `code`, scale and offset given as
+    fp16 bit patterns (little-endian in the block)."""
+    byte = code | code << 2 | code << 4 | code << 6
+    blk = bytes([byte] * 8) + bytes([d_bits & 0xFF, d_bits >> 8, m_bits & 0xFF, m_bits >> 8])
+    return np.frombuffer(blk * (n_rows * K // 32), np.uint8).copy()
+
+
+def test_moe_tolerance_hand_worked_element(orc):
+    """One expert, H = F = 32, every weight 1 (code 1, d = 1, m = 0), x = e_0, zero router
+    logits (g = 1).  Then gate_f = up_f = 1, h_f = silu(1) = sigma(1), the gate and up bounds are
+    2e-3 * 1, and for every output n:
+      tol = 2e-3 * 32 * sigma(1) + 32 * 2e-3 * (silu'(1) * 1 + silu(1) * 1)
+          = 0.064 * (2 sigma(1) + silu'(1)),
+    with sigma(1) = 0.7310585786300049 and silu'(1) = sigma(1) + sigma(1)(1 - sigma(1))
+    = 0.9276705118714868, i.e. tol = 0.064 * 2.3897876691314966 = 0.1529464108244158.
+    Y_n = 32 * sigma(1) = 23.393874516160157."""
+    H = F = 32
+    one = _q2b32_constant_rows(F, H, 1, 0x3C00)
+    X = np.zeros((1, H), np.uint16)
+    X[0, 0] = 0x3F80  # bf16 1.0
+    out = orc.moe(one, one, one, 1, H, F, 1, X, np.zeros((1, 1), np.float32))
+    np.testing.assert_allclose(out["Y"][0], np.full(H, 23.393874516160157), rtol=1e-14)
+    np.testing.assert_allclose(out["tol"][0], np.full(H, 0.1529464108244158), rtol=1e-13)
+
+
 def test_pq_verify_accept_threshold_is_p_over_q(orc):
     """Accept iff u < p(x)/q(x): the largest fp32 below the ratio accepts, the smallest fp32
     at or above it rejects (the ratio taken from scipy's softmax, not the oracle)."""
