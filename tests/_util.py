@@ -2,6 +2,7 @@
 CUDA path with the oracle under the stated acceptance rules."""
 from __future__ import annotations
 
+import os
 import re
 from pathlib import Path
 
@@ -16,6 +17,10 @@ PROB_ATOL = 1e-5
 # a uniform within this of a decision boundary (p/q, or a normalised CDF cell edge) is a
 # near-tie: the token may differ there, and such draws are counted and reported.
 NEAR_TIE = 1e-5
+
+# every compare_verify result of this test session, as (test id, counts); conftest.py prints
+# the per-test totals at the end of the run and writes them to $Q2V_NEAR_TIE_REPORT when set
+NEAR_TIE_LOG: list[tuple[str, dict]] = []
 
 
 def header_functions() -> list[str]:
@@ -90,4 +95,5 @@ def compare_verify(gpu_n, gpu_tok, orc: dict, u_acc, u_fin, k: int) -> dict:
                 w = probs[s, k]
             lo, hi = _cells(w)
             assert w[y] > 0 and lo[y] - NEAR_TIE <= u <= hi[y] + NEAR_TIE, (s, y, lo[y], hi[y], u)
+    NEAR_TIE_LOG.append((os.environ.get("PYTEST_CURRENT_TEST", "?").split(" ")[0], dict(stats)))
     return stats
