@@ -7,14 +7,18 @@ One step = one pass of the whole hot path at the M=5 verifier shapes:
   (3) the p/q verify of 3 sessions x 4 drafts over V=129280 (pq_verify).
 Inputs are seeded synthetic tensors (see speculative_decode_verifier_gb300.synth); weights
 are random, not trained.  Device timing replays one CUDA graph per input set, rotating over
-4 sets, so every step touches > 250 MB (more than the 126 MB L2).
+4 sets, each with its own weights (the linear's and all 64 experts'), so every step touches
+> 250 MB that the previous step did not (more than the 126 MB L2).
 
 Prints one JSON line.  `value` is the device-timed step time in microseconds (inputs resident
 in HBM); `e2e` is the same step through the Python binding with pinned host buffers copied
 in and results copied out inside the timed region, every step; the input copies run on a
-second stream, so step i+1's copies overlap step i's kernels.  `--impl reference` times the fp64 CPU
-oracle on the host cores instead (the only place this file runs the oracle besides the
-cpu_baseline leg).
+second stream, so step i+1's copies overlap step i's kernels.  `cpu_baseline` is the fp64 CPU
+oracle timed on the host cores over the full step of input set 0 (all cores, and one core);
+the same oracle outputs check the GPU's results of that set's graph-replayed step (`parity`:
+GEMM and MoE bounds, accepted counts and tokens with the near-ties counted), and of the M=60
+cohort.  `--impl reference` times the oracle alone.  These two legs are the only places this
+file runs the oracle.
 """
 from __future__ import annotations
 
@@ -44,8 +48,8 @@ EXPERT_BYTES = 3 * 2048 * (4096 // 32) * 12   # gate + up + down of one expert
 
 def _kernel_source_digest() -> str:
     """sha256 (first 16 hex digits) of the source the gate+up stream kernel is built from: the
-    shared device headers and the kernel's own definition.  A traffic figure recorded under
-    profiles/ is only reported while this digest still matches the one recorded with it."""
+    shared device headers and the kernel's own definition.  The traffic figure recorded with the
+    ncu summaries is only reported while this digest still matches the one recorded with it."""
     import hashlib
     import re
     csrc = os.path.join(ROOT, "speculative_decode_verifier_gb300", "csrc")
@@ -61,7 +65,7 @@ def _kernel_source_digest() -> str:
 
 
 def _traffic_record():
-    """The `traffic-record:` line of profiles/verifier_step_m5_launch_list.md, as a dict."""
+    """The `traffic-record:` line of the step's launch-list summary under profiles/, as a dict."""
     path = os.path.join(ROOT, "profiles", "verifier_step_m5_launch_list.md")
     try:
         with open(path) as f:
@@ -195,19 +199,23 @@ def run_device(args, rank: int, world: int):
         assert q2v.q2_get_device_status(wsc) == 0
         return None
 
-    # resident inputs, N_SETS rotating sets
+    # resident inputs, N_SETS rotating sets, each with its own weights (the linear's and the 64
+    # experts'), so no step finds the previous step's weights in L2
     sets = []
+    host0 = None
     for i in range(N_SETS):
         g, m, v = make_inputs(i)
         sets.append(dict(
             W=D(g["W"].reshape(-1)), A=D(g["A"]), X=D(m["X"]), R=D(m["router"]),
+            Wg=D(m["Wg"].reshape(-1)), Wu=D(m["Wu"].reshape(-1)), Wd=D(m["Wd"].reshape(-1)),
             T=D(v["target"]), Dl=D(v["draft"]), x=D(v["drafts"]), ua=D(v["u_acc"]), uf=D(v["u_fin"]),
             host=dict(A=g["A"], X=m["X"], R=m["router"], T=v["target"], Dl=v["draft"], x=v["drafts"],
                       ua=v["u_acc"], uf=v["u_fin"])))
         if i == 0:
-            moe_w = {k: D(m[k].reshape(-1)) for k in ("Wg", "Wu", "Wd")}
+            host0 = (g, m, v)   # the oracle leg checks this set's step
             shapes = dict(N=g["N"], K=g["K"], M=g["M"], E=m["E"], H=m["H"], F=m["F"], topk=m["topk"],
                           S=v["target"].shape[0], k=v["target"].shape[1] - 1, V=v["target"].shape[2])
+        del g, m, v
     sh = shapes
     # the step's results (the linear's Y, the MoE's Y, accepted counts, tokens) live in one
     # device buffer, so the end-to-end loop reads them back with one copy
@@ -225,7 +233,7 @@ def run_device(args, rank: int, world: int):
         q2v.q2_tiny_gemm(s["W"], sh["N"], sh["K"], s["A"], Y=o["Y1"], ws=ws1)
 
     def part_moe(s, o=res):
-        q2v.q2_moe_grouped(moe_w["Wg"], moe_w["Wu"], moe_w["Wd"], sh["E"], sh["H"], sh["F"], sh["topk"], s["X"],
+        q2v.q2_moe_grouped(s["Wg"], s["Wu"], s["Wd"], sh["E"], sh["H"], sh["F"], sh["topk"], s["X"],
                            s["R"], Y=o["Y2"], ids_out=ids, w_out=gw, ws=ws2)
 
     def part_pq(s, o=res):
@@ -303,6 +311,13 @@ def run_device(args, rank: int, world: int):
     g_step = capture(step)
     step_us, clocks = timed(g_step, args.steps, args.warmup, clocks=True)
     step_us = max_over_ranks(step_us, dev)
+    # the results of set 0's graph-replayed step, for the oracle leg's parity check
+    res_dev.zero_()
+    g_step[0].replay()
+    torch.cuda.synchronize()
+    gpu0 = {k: res[k].cpu().numpy() for k in ("Y1", "Y2", "n", "t")}
+    st0 = [q2v.q2_get_device_status(w) for w in (ws1, ws2, ws3)]
+    assert st0 == [0, 0, 0], f"device status {st0} after the timed steps"
     # per-kernel device time inside the step: each timed step is its own graph whose launch of
     # the kernel is bracketed by its own event pair (q2_set_probe); these steps replay back to
     # back after warm-up, like the timed region above
@@ -365,6 +380,25 @@ def run_device(args, rank: int, world: int):
     peak_x, _ = _peaks()
     lin_bytes = sh["N"] * (sh["K"] // 32) * 12 + sh["M"] * sh["K"] * 2 + sh["M"] * sh["N"] * 4
 
+    # read-only HBM bandwidth on this GPU: q2_hbm_read_probe streams a 4 GiB buffer once per call
+    # (every kernel of the step is a read stream, so this is the bound next to the copy peak)
+    rbuf = torch.empty(4 << 30, dtype=torch.uint8, device=dev).random_(0, 256)
+    sink = torch.zeros(1, dtype=torch.int32, device=dev)
+    for _ in range(3):
+        q2v.q2_hbm_read_probe(rbuf, sink)
+    torch.cuda.synchronize()
+    ea, eb = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps_r = 10
+    ea.record()
+    for _ in range(reps_r):
+        q2v.q2_hbm_read_probe(rbuf, sink)
+    eb.record()
+    torch.cuda.synchronize()
+    read_gbs = rbuf.numel() / (ea.elapsed_time(eb) / reps_r * 1e-3) / 1e9
+    read_probe = {"GB/s": read_gbs, "bytes": rbuf.numel(), "calls": reps_r,
+                  "kernel": "q2_hbm_read_probe (16-byte evict-first loads, 8 in flight per thread, 4x512 threads per SM)"}
+    del rbuf
+
     # the verifier-layer shape: 8 distinct 4096 x 4096 Q2B32 linears back to back (PDL, the
     # weight stream of each starting before its activation prep is done), 4 rotating layer
     # sets (200 MB, larger than L2)
@@ -405,6 +439,7 @@ def run_device(args, rank: int, world: int):
     # the cohort verify: 12 sessions x 5 rows = M=60 against a 129,280 x 4096 Q2B32 vocabulary
     # head on the tcgen05 path, then pq_verify (S=12, k=4) over those logits
     cohort = None
+    cohort_host = None
     if not args.no_extras:
         gc = synth.config_gemm(4)
         Wc, Ac = D(gc["W"].reshape(-1)), D(gc["A"])
@@ -459,6 +494,11 @@ def run_device(args, rank: int, world: int):
                         max(5, args.steps // 2))
         cohort["session_m5_lm_head_verify_us"] = s_us
         cohort["session_m5_GB/s"] = (wbytes + 5 * Kc * 2 + 5 * Nc * 4 + 4 * 4 * Nc) / (s_us * 1e-6) / 1e9
+        # the cohort's results (the head GEMM then pq_verify over its logits, one eager pass),
+        # for the oracle leg's parity check
+        c_both()
+        torch.cuda.synchronize()
+        cohort_host = dict(g=gc, v=vc, Y=Yco.cpu().numpy(), n=nc.cpu().numpy(), t=tc.cpu().numpy())
         del Wc
 
     # e2e: through the binding, pinned host inputs in, results out, every step.  Each input
@@ -474,7 +514,8 @@ def run_device(args, rank: int, world: int):
             a = s["host"][k]
             hv[k].copy_(torch.from_numpy(np.ascontiguousarray(a.view(np.int16) if a.dtype == np.uint16 else a)))
         db, dv = _packed(in_layout, dev)
-        dv["W"] = s["W"]
+        for k in ("W", "Wg", "Wu", "Wd"):
+            dv[k] = s[k]
         pin.append(hb)
         dev_in.append((db, dv))
     # each slot has its own result buffer, read back on the copy stream once its step is done,
@@ -563,6 +604,7 @@ def run_device(args, rank: int, world: int):
             d["bytes"] = tot_b / len(set_ids)
             d["GB/s"] = tot_b / (sum(us) * 1e-6) / 1e9
             d["frac"] = d["GB/s"] / peak
+            d["frac_of_read_probe"] = d["GB/s"] / read_gbs
         kernels[name] = d
     dom = kernels["moe_gate_up"]
     # DRAM traffic of one launch from the recorded ncu capture, scaled to the mean launch by
@@ -587,37 +629,105 @@ def run_device(args, rank: int, world: int):
         "roofline": {"bound": "hbm", "kernel": "moe_stream_kernel<gate+up> (MoE gate+up grouped dequant GEMM)",
                      "achieved": dom["GB/s"], "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": dom["frac"], "traffic": traffic,
+                     "read_probe_GB/s": read_gbs, "frac_of_read_probe": dom["GB/s"] / read_gbs,
                      "algorithmic_bytes_per_launch": dom["bytes"], "us_per_launch": dom["us"]},
         "e2e": {"value": e2e_us, "unit": "µs", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "gpu_launches": LAUNCHES_PER_STEP * args.steps,
+        "read_probe": read_probe,
         "chained_linears_m5": chain,
         "verifier_layer_m5": layer,
         "cohort_m60": cohort,
         "clocks": clocks,
     }
-    return line
+    return line, dict(host0=host0, gpu0=gpu0, cohort=cohort_host)
 
 
 # ----------------------------------------------------------------------------- oracle arm
 
-def _oracle_step(g, m, v, frac: float, threads: int):
-    """One oracle pass over a `frac` sample of the step (leading output rows of the linear and
-    of each expert projection are not separable in the oracle, so the sample is: the linear on
-    frac*N rows, the MoE on ceil(frac*M) rows, pq_verify on all sessions)."""
+def _oracle_step(g, m, v, threads: int):
+    """One full verifier step on the fp64 oracle: the linear (all 4096 output rows), the MoE FFN
+    (all 5 rows), pq_verify (all 3 sessions).  Returns (seconds, outputs)."""
     from oracle import oracle
-    n = max(16, int(g["N"] * frac))
-    rows = g["W"][:n]
     t0 = time.perf_counter()
-    oracle.gemm(rows, n, g["K"], g["A"], threads=threads)
-    t1 = time.perf_counter()
-    mrows = 1
-    oracle.moe(m["Wg"], m["Wu"], m["Wd"], m["E"], m["H"], m["F"], m["topk"], m["X"][:mrows], m["router"][:mrows],
-               threads=threads)
-    t2 = time.perf_counter()
-    oracle.pq_verify(v["target"], v["draft"], v["drafts"], v["u_acc"], v["u_fin"], v["T"], threads=threads)
-    t3 = time.perf_counter()
-    # scale each part to the full workload
-    return (t1 - t0) * g["N"] / n + (t2 - t1) * m["M"] / mrows + (t3 - t2)
+    lin = oracle.gemm(g["W"], g["N"], g["K"], g["A"], threads=threads)
+    moe = oracle.moe(m["Wg"], m["Wu"], m["Wd"], m["E"], m["H"], m["F"], m["topk"], m["X"], m["router"],
+                     threads=threads)
+    pq = oracle.pq_verify(v["target"], v["draft"], v["drafts"], v["u_acc"], v["u_fin"], v["T"], threads=threads)
+    return time.perf_counter() - t0, dict(lin=lin, moe=moe, pq=pq)
+
+
+NEAR_TIE = 1e-5   # a uniform this close to a decision boundary makes a near-tie
+
+
+def _near_ties(n_gpu, t_gpu, o, u_acc, u_fin, k):
+    """Per-session comparison of the GPU's accepted counts and tokens with the oracle's: how many
+    match exactly, how many had a uniform within 1e-5 of an evaluated accept ratio p/q or of the
+    oracle's chosen CDF cell edge (near-ties), how many differ at a near-tie, and how many differ
+    without one (a parity failure)."""
+    st = dict(sessions=int(len(n_gpu)), exact=0, accept_near_ties=0, draw_near_ties=0,
+              mismatches_at_near_ties=0, mismatches_without_near_tie=0)
+    for s in range(len(n_gpu)):
+        jo = int(o["n_acc"][s])
+        same = int(n_gpu[s]) == jo and np.array_equal(t_gpu[s], o["tokens"][s])
+        acc_tie = any(np.isfinite(o["ratio"][s, i]) and abs(float(u_acc[s, i]) - o["ratio"][s, i]) < NEAR_TIE
+                      for i in range(min(jo + 1, k)))
+        u = float(u_fin[s])
+        draw_tie = abs(u - o["cell_lo"][s]) < NEAR_TIE or abs(u - o["cell_hi"][s]) < NEAR_TIE
+        st["accept_near_ties"] += int(acc_tie)
+        st["draw_near_ties"] += int(draw_tie)
+        if same:
+            st["exact"] += 1
+        elif acc_tie or draw_tie:
+            st["mismatches_at_near_ties"] += 1
+        else:
+            st["mismatches_without_near_tie"] += 1
+    return st
+
+
+def _gemm_check(Y_gpu, Y_orc, absY):
+    r = np.abs(np.asarray(Y_gpu, np.float64) - Y_orc) / np.maximum(2e-3 * absY, 1e-300)
+    return {"elements": int(r.size), "max_err_over_bound": float(r.max()), "pass": bool(np.all(r <= 1.0))}
+
+
+def oracle_leg(extras, core_runs: int = 3):
+    """cpu_baseline and parity: the oracle's full step on input set 0, timed on all host cores
+    (`core_runs` runs) and on one core; its outputs against the GPU's graph-replayed step of the
+    same set; the M=60 cohort's head GEMM (timed once) and the verify of the GPU's logits."""
+    from oracle import oracle
+    oracle.build()
+    threads = oracle.default_threads()
+    g, m, v = extras["host0"]
+    runs = [_oracle_step(g, m, v, threads) for _ in range(core_runs)]
+    t_all = statistics.mean(r[0] for r in runs)
+    t_one, _ = _oracle_step(g, m, v, 1)
+    out = runs[0][1]
+    gpu = extras["gpu0"]
+    k = v["target"].shape[1] - 1
+    moe_r = np.abs(gpu["Y2"].astype(np.float64) - out["moe"]["Y"]) / out["moe"]["tol"]
+    parity = {
+        "input_set": 0,
+        "q2_tiny_gemm": _gemm_check(gpu["Y1"], *out["lin"]),
+        "q2_moe_grouped": {"elements": int(moe_r.size), "max_err_over_bound": float(moe_r.max()),
+                           "pass": bool(np.all(moe_r <= 1.0))},
+        "pq_verify": _near_ties(gpu["n"], gpu["t"], out["pq"], v["u_acc"], v["u_fin"], k),
+    }
+    cpu = {"value": t_all * 1e6, "unit": "µs", "cores": threads, "kind": "oracle",
+           "sample": (f"the full step of input set 0 (linear 4096x4096 M=5, MoE FFN on all 5 rows, pq_verify "
+                      f"S=3 k=4 V=129280), fp64, {threads} OpenMP threads, mean of {core_runs} runs"),
+           "one_core_us": t_one * 1e6}
+    c = extras.get("cohort")
+    if c is not None:
+        gc, vc = c["g"], c["v"]
+        t0 = time.perf_counter()
+        Yo, absYo = oracle.gemm(gc["W"], gc["N"], gc["K"], gc["A"], threads=threads)
+        cpu["cohort_m60_gemm_us"] = (time.perf_counter() - t0) * 1e6
+        S, k1 = vc["draft"].shape[0], vc["draft"].shape[1] + 1
+        logits = c["Y"].reshape(S, k1, -1)
+        po = oracle.pq_verify(logits, vc["draft"], vc["drafts"], vc["u_acc"], vc["u_fin"], 1.0, threads=threads)
+        parity["cohort_m60"] = {"lm_head_gemm": _gemm_check(c["Y"], Yo, absYo),
+                                "pq_verify_on_gpu_logits": _near_ties(c["n"], c["t"], po, vc["u_acc"],
+                                                                      vc["u_fin"], k1 - 1)}
+    return cpu, parity
 
 
 def run_oracle(steps: int, warmup: int):
@@ -625,14 +735,12 @@ def run_oracle(steps: int, warmup: int):
     oracle.build()
     threads = oracle.default_threads()
     g, m, v = make_inputs(0)
-    frac = 0.25
     for _ in range(max(0, warmup)):
-        _oracle_step(g, m, v, frac, threads)
-    times = [_oracle_step(g, m, v, frac, threads) for _ in range(steps)]
+        _oracle_step(g, m, v, threads)
+    times = [_oracle_step(g, m, v, threads)[0] for _ in range(steps)]
     us = statistics.mean(times) * 1e6
-    return us, threads, (f"per step: the linear on 25% of its 4096 output rows, the MoE FFN on 1 of 5 rows "
-                         f"(all 6 experts of that row), pq_verify on all 3 sessions; times scaled to the "
-                         f"full step; fp64; {threads} OpenMP threads")
+    return us, threads, (f"the full step of input set 0 (linear 4096x4096 M=5, MoE FFN on all 5 rows, pq_verify "
+                         f"S=3 k=4 V=129280), fp64, {threads} OpenMP threads")
 
 
 def main():
@@ -656,8 +764,8 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return
-        # exactly W untimed and K timed steps, each a bounded sample of the step (about half a
-        # second of fp64 work on 16 host cores)
+        # exactly W untimed and K timed full steps (about half a second of fp64 work each on
+        # 16 host cores)
         us, cores, sample = run_oracle(max(1, args.steps), args.warmup)
         print(json.dumps({
             "impl": "reference", "metric": METRIC, "value": us, "unit": "µs", "n_gpus": 0,
@@ -672,13 +780,13 @@ def main():
     if world > 1:
         import torch
         torch.distributed.init_process_group("nccl")
-    line = run_device(args, rank, world)
-    if line is None:
+    got = run_device(args, rank, world)
+    if got is None:
         return
+    line, extras = got
     if rank == 0:
         if not args.no_cpu_baseline and world == 1:
-            us, cores, sample = run_oracle(1, 0)
-            line["cpu_baseline"] = {"value": us, "unit": "µs", "cores": cores, "kind": "oracle", "sample": sample}
+            line["cpu_baseline"], line["parity"] = oracle_leg(extras)
         print(json.dumps(line))
     if world > 1:
         import torch

@@ -300,6 +300,17 @@ typedef enum {
  * not thread-safe; a recording failure makes the bracketed call return Q2_ERR_CUDA. */
 q2_status q2_set_probe(int kernel, void *ev_begin, void *ev_end);
 
+/* Read-only HBM bandwidth probe for measurement harnesses; the verifier method has no
+ * counterpart (the "ds4-on-spark" README, section "Roofline", measures copy and read-only
+ * bandwidth the same way on GB10).  Enqueues on `stream` one kernel that reads every byte of
+ * `buf` once (16-byte loads, L1 bypassed, evict-first in L2) and writes nothing, except *sink
+ * when the folded value of the data happens to equal a fixed constant; time it with events
+ * around the call.  The caller owns both buffers.
+ *   buf   device memory, 16-byte aligned, `bytes` > 0 and a multiple of 16.
+ *   sink  device memory, 4 bytes, 4-byte aligned.
+ * Errors: Q2_ERR_INVALID_ARG, Q2_ERR_ALIGNMENT, Q2_ERR_CUDA (launch failure). */
+q2_status q2_hbm_read_probe(const void *buf, size_t bytes, unsigned int *sink, q2_stream_t stream);
+
 /* ------------------------------------------------------------------ status */
 
 /* Synchronise `stream`, read the device status word of workspace `ws`, clear it, and

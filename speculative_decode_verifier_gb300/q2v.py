@@ -25,7 +25,8 @@ LM_HEAD_FUSE_STATS = 1
 EXPORTS = ("q2_tiny_gemm_workspace", "q2_tiny_gemm", "q2_moe_grouped_workspace", "q2_moe_grouped",
            "pq_verify_workspace", "pq_verify", "pq_verify_noalloc", "q2_get_device_status", "q2_status_string",
            "q2_version", "q2_set_probe", "pq_verify_ex", "q2_quench_init", "q2_quench_update",
-           "q2_lm_head_verify_workspace", "q2_lm_head_verify", "q2_selftest_wait_timeout")
+           "q2_lm_head_verify_workspace", "q2_lm_head_verify", "q2_selftest_wait_timeout",
+           "q2_hbm_read_probe")
 
 # kernels that q2_set_probe can bracket (q2_probe_kernel)
 PROBE_NONE, PROBE_MOE_GATE_UP, PROBE_MOE_DOWN, PROBE_GEMM, PROBE_PQ_STATS, PROBE_PQ_VERIFY = range(6)
@@ -84,6 +85,8 @@ def load(path: str | None = None) -> ctypes.CDLL:
     lib.q2_set_probe.restype = I
     lib.q2_selftest_wait_timeout.argtypes = [P, Z, P]
     lib.q2_selftest_wait_timeout.restype = I
+    lib.q2_hbm_read_probe.argtypes = [P, Z, P, P]
+    lib.q2_hbm_read_probe.restype = I
     _lib = lib
     return lib
 
@@ -218,6 +221,15 @@ def q2_selftest_wait_timeout(ws: torch.Tensor, stream=None) -> None:
 
 
 # ------------------------------------------------------------------ entry points
+
+def q2_hbm_read_probe(buf: torch.Tensor, sink: torch.Tensor, stream=None) -> None:
+    """Enqueue one read of every byte of `buf` (a contiguous CUDA tensor whose byte size is a
+    multiple of 16) on the current stream; `sink` is a CUDA int32/uint32 tensor of >= 1 element."""
+    _check(buf, "buf", buf.dtype if isinstance(buf, torch.Tensor) else None)
+    _check(sink, "sink", torch.int32)
+    nbytes = buf.numel() * buf.element_size()
+    _raise(load().q2_hbm_read_probe(_ptr(buf), nbytes, _ptr(sink), _stream(stream)), "q2_hbm_read_probe")
+
 
 def q2_tiny_gemm(W: torch.Tensor, N: int, K: int, A: torch.Tensor, Y: torch.Tensor | None = None,
                  ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
