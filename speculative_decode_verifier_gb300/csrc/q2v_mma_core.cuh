@@ -305,8 +305,10 @@ __device__ __forceinline__ int act_exponent(float maxabs) {
 // (the row scale and the code-position factor of dequant_pos, both exact), and the sum of
 // the block's f16 activations under the row scale alone, split into hi + lo f16.  The
 // padding blocks (v all zero) store zeros.
-__device__ __forceinline__ void prep_store_block(const float (&v)[32], int e, uint32_t *act_row, __half *sh,
-                                                 __half *sl, int b) {
+// The prepared form of one block: its 16 pair slots and its hi + lo block sum (see
+// prep_store_block).
+__device__ __forceinline__ void prep_block_values(const float (&v)[32], int e, uint32_t (&w)[16], __half &hi,
+                                                  __half &lo) {
     __half h[32];
     float s = 0.0f;
 #pragma unroll
@@ -314,18 +316,43 @@ __device__ __forceinline__ void prep_store_block(const float (&v)[32], int e, ui
         h[j] = __float2half_rn(ldexpf(v[j], -e - 2 * (j & 3)));
         s += __half2float(__float2half_rn(ldexpf(v[j], -e)));
     }
-    uint32_t w[16];
 #pragma unroll
     for (int p = 0; p < 16; ++p) {
         const int k0 = 16 * (p >> 3) + (p & 7);
         w[p] = pack_half2(h[k0], h[k0 + 8]);
     }
+    hi = __float2half_rn(s);
+    lo = __float2half_rn(s - __half2float(hi));
+}
+
+__device__ __forceinline__ void prep_store_block(const float (&v)[32], int e, uint32_t *act_row, __half *sh,
+                                                 __half *sl, int b) {
+    uint32_t w[16];
+    __half hi, lo;
+    prep_block_values(v, e, w, hi, lo);
     uint4 *dst = reinterpret_cast<uint4 *>(act_row + (size_t)b * 16);
 #pragma unroll
     for (int j = 0; j < 4; ++j) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
-    const __half hi = __float2half_rn(s);
     sh[b] = hi;
-    sl[b] = __float2half_rn(s - __half2float(hi));
+    sl[b] = lo;
+}
+
+// The same prepared block written straight into a staged operand (the SmemAct layout that
+// stage_act_issue produces): slot p of block b of column c lands at pair (b / 2), fragment
+// group p / 4, block half b % 2, and word (p & 2 ? 4 : 0) + (p & 1) inside the group.
+__device__ __forceinline__ void prep_store_block_smem(const float (&v)[32], int e, uint32_t *sm, const SmemAct &SA,
+                                                      int c, int b) {
+    uint32_t w[16];
+    __half hi, lo;
+    prep_block_values(v, e, w, hi, lo);
+    uint32_t *dst = SA.act(sm, c) + (b >> 1) * kPairWords + 2 * (b & 1);
+#pragma unroll
+    for (int grp = 0; grp < 4; ++grp) {
+        *reinterpret_cast<uint2 *>(dst + 8 * grp) = make_uint2(w[4 * grp], w[4 * grp + 1]);
+        *reinterpret_cast<uint2 *>(dst + 8 * grp + 4) = make_uint2(w[4 * grp + 2], w[4 * grp + 3]);
+    }
+    reinterpret_cast<__half *>(SA.shi(sm, c))[b] = hi;
+    reinterpret_cast<__half *>(SA.slo(sm, c))[b] = lo;
 }
 
 // Block-wide max of non-negative values (blockDim.x <= 1024); every thread gets the result.

@@ -239,3 +239,19 @@ def test_umma_deterministic_and_ldy(env):
     q2v.q2_tiny_gemm(Wd, N, K, Ad, Y=Yp)
     assert torch.equal(Yp[:, :N].cpu(), Y1)
     assert torch.all(Yp[:, N:] == 7.0)
+
+
+def test_activation_magnitude_varies_along_k(env):
+    """The fused small-M path scales each warp's K slice of a row by its own power of two: slices
+    of one row 1e20 apart, and a row that is zero in some slices only, stay within the bound."""
+    st = synth.Streams(78)
+    M, N, K = 5, 48, 4096
+    W = synth.q2b32_weights(st, N, K)
+    a = st["A"].normal(0, 1, size=(M, K))
+    a[0, :256] *= 1e20
+    a[1, 1024:2048] = 0.0
+    a[2, ::2] *= 1e-20
+    A = synth.bf16_bits(a)
+    Y = _run(env, W, N, K, A)
+    Yo, absY = env[2].gemm(W, N, K, A)
+    check_gemm(Y, Yo, absY, "magnitudes along K")
