@@ -140,24 +140,15 @@ __global__ void __launch_bounds__(kGemmWarps * 32) q2_gemm_fused_kernel(const ui
     for (int q = 0; q < kRounds; ++q) {
         if (2 * q >= M) break;
         const int row = 2 * q + (lane >> 4), lb = lane & 15;
-        float v[32];
-        float mx = 0.0f;
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const uint32_t wv[4] = {raw[q][j].x, raw[q][j].y, raw[q][j].z, raw[q][j].w};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                v[8 * j + 2 * i] = __uint_as_float(wv[i] << 16);
-                v[8 * j + 2 * i + 1] = __uint_as_float(wv[i] & 0xFFFF0000u);
-            }
-        }
-#pragma unroll
-        for (int j = 0; j < 32; ++j) mx = fmaxf(mx, fabsf(v[j]));
+        const uint32_t w[16] = {raw[q][0].x, raw[q][0].y, raw[q][0].z, raw[q][0].w, raw[q][1].x, raw[q][1].y,
+                                raw[q][1].z, raw[q][1].w, raw[q][2].x, raw[q][2].y, raw[q][2].z, raw[q][2].w,
+                                raw[q][3].x, raw[q][3].y, raw[q][3].z, raw[q][3].w};
+        float mx = bf16x2_maxabs(w);
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
         const int e = act_exponent(mx);
         if (row < M) {
-            prep_store_block_smem(v, e, wsm, SA, row, lb);
+            prep_store_block_smem(w, e, wsm, SA, row, lb);
             if (lb == 0) s_exp[warp][row] = e;
         }
     }
