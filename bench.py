@@ -349,9 +349,33 @@ def run_device(args, rank: int, world: int):
                       ("gemm", q2v.PROBE_GEMM), ("pq_stats", q2v.PROBE_PQ_STATS), ("pq_verify", q2v.PROBE_PQ_VERIFY)):
         kern_us[name] = probe_pass(kid)
 
-    gemm_us, _ = timed(capture(part_gemm), args.steps, args.warmup)
-    moe_us, _ = timed(capture(part_moe), args.steps, args.warmup)
-    pq_us, _ = timed(capture(part_pq), args.steps, args.warmup)
+    def part_us(fn):
+        """Mean µs of one call of fn inside a graph that makes one call per input set (N_SETS
+        calls back to back, PDL between them, as inside a step), so the time per graph launch
+        does not count as the part's own."""
+        def all_sets():
+            for s in sets:
+                fn(s)
+        all_sets()  # one eager pass before capture
+        torch.cuda.synchronize()
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            all_sets()
+        reps = max(3, args.steps // N_SETS)
+        for _ in range(args.warmup):
+            gr.replay()
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            gr.replay()
+        b.record()
+        torch.cuda.synchronize()
+        return a.elapsed_time(b) / (reps * N_SETS) * 1000.0
+
+    gemm_us = part_us(part_gemm)
+    moe_us = part_us(part_moe)
+    pq_us = part_us(part_pq)
 
     def graph_us(fn, reps):
         """Mean µs of fn() replayed from one CUDA graph (3 warm-up replays first)."""
@@ -756,8 +780,15 @@ def main():
                     help="skip the chained-linear and cohort (M=60) measurements")
     ap.add_argument("--profile", action="store_true",
                     help="run warmup+steps eager steps only (for an ncu launch list); prints nothing")
+    ap.add_argument("--sets", type=int, default=None,
+                    help="with --profile: rotate over this many input sets (fewer bytes held on the device)")
     args = ap.parse_args()
     args.warmup = max(args.warmup, 3)
+    if args.sets is not None:
+        if not args.profile:
+            ap.error("--sets is for --profile runs only")
+        global N_SETS
+        N_SETS = max(1, min(args.sets, N_SETS))
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
 
