@@ -12,7 +12,8 @@
 //   smallest y whose cumulative mass exceeds u_fin times the total.
 //
 // Two tiers:
-//   * small V (<= kWarpTierMaxV): one warp per session does everything in one kernel;
+//   * small V (<= kWarpTierMaxV): one warp (V <= 512) or one CTA per session does everything
+//     in one kernel;
 //   * large V: the vocabulary of each session is split into C chunks.  Kernel 1 streams
 //     every row's chunk once (leaving the rows in L2) and writes (max, sum exp) partials;
 //     it also gathers both logits at each draft token.  Kernel 2 combines the partials,
@@ -249,122 +250,269 @@ __device__ __forceinline__ DrawRows draw_rows(const PqArgs &a, int s, int j, con
 }
 
 // ===================================================================== small-V tier
+//
+// V <= kWarpTierMaxV: a group of GW warps per session does everything in one kernel (one warp
+// per session for V <= kSmallWarpMaxV, eight warps -- the whole CTA -- above).  Every load is
+// issued in batches before any of it is used: a row's statistics take one batch per 32 x 32
+// floats (float4 loads) or 32 x 16 (scalar), the accept scan is lane-parallel (one lane per
+// draft, a ballot finds the first rejection), and the draw gives each thread a contiguous run
+// of at most 16 tokens whose logits it loads at once, then one compensated group-wide scan
+// finds the run, and the run's owner the token.
 
-constexpr int kWarpTierWarps = 8;
+constexpr int kSmallWarpMaxV = 512;   // one warp per session up to this V
+constexpr int kSmallMaxRun = 16;      // tokens per thread in the draw
 
-__global__ void __launch_bounds__(kWarpTierWarps * 32) pqv_warp_kernel(PqArgs a) {
-    __shared__ float sM[kWarpTierWarps][kMaxRows];
-    __shared__ float sL2Z[kWarpTierWarps][kMaxRows];
-    __shared__ int sArg[kWarpTierWarps][kMaxRows];
+// (max, log2 sum 2^((x - max) beta)) of one row of V logits, by one warp; loads in batches.
+template <bool VEC>
+__device__ __forceinline__ void warp_row_stats(const float *__restrict__ x, int V, float beta, int lane, float &M,
+                                               float &L2Z) {
+    float m = -INFINITY, z = 0.0f;
+    constexpr int U = VEC ? 8 : 16;
+    constexpr int W = VEC ? 4 : 1;  // floats per load
+    for (int base = 0; base < V; base += 32 * U * W) {
+        float v[U * W];
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int i = base + (u * 32 + lane) * W;
+            if (VEC) {
+                const float4 q = i < V ? __ldg(reinterpret_cast<const float4 *>(x + i))
+                                       : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                v[4 * u] = q.x; v[4 * u + 1] = q.y; v[4 * u + 2] = q.z; v[4 * u + 3] = q.w;
+            } else {
+                v[u] = i < V ? __ldg(x + i) : -INFINITY;
+            }
+        }
+        float bm = m;
+#pragma unroll
+        for (int u = 0; u < U * W; ++u) bm = fmaxf(bm, v[u]);
+        if (bm > -INFINITY) {
+            float acc = (m > -INFINITY) ? z * ex2((m - bm) * beta) : 0.0f;
+#pragma unroll
+            for (int u = 0; u < U * W; ++u) acc += ex2((v[u] - bm) * beta);  // -inf entries add 0
+            z = acc;
+            m = bm;
+        }
+    }
+    M = warp_max(m);
+    const float zz = warp_sum((m > -INFINITY) ? z * ex2((m - M) * beta) : 0.0f);
+    L2Z = log2f(zz);
+}
+
+// (max, first index of it) of one row by one warp; loads in batches of 16 per lane.
+__device__ __forceinline__ int warp_row_argmax(const float *__restrict__ x, int V, int lane) {
+    float m = -INFINITY;
+    int i = 0x7FFFFFFF;
+    for (int base = 0; base < V; base += 32 * 16) {
+        float v[16];
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int y = base + u * 32 + lane;
+            v[u] = y < V ? __ldg(x + y) : -INFINITY;
+        }
+#pragma unroll
+        for (int u = 0; u < 16; ++u) {
+            const int y = base + u * 32 + lane;
+            if (y < V && (i == 0x7FFFFFFF || v[u] > m)) {
+                m = v[u];
+                i = y;
+            }
+        }
+    }
+    warp_argmax(m, i);
+    return i;
+}
+
+// Compensated exclusive scan over the threads of one warp (lane order); `total` gets the sum.
+__device__ __forceinline__ CSum warp_excl_scan_c(const CSum &v, int lane, CSum &total) {
+    CSum inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        CSum n;
+        n.hi = __shfl_up_sync(0xffffffffu, inc.hi, o);
+        n.lo = __shfl_up_sync(0xffffffffu, inc.lo, o);
+        if (lane >= o) inc = csum_plus(n, inc);
+    }
+    CSum ex;
+    ex.hi = __shfl_up_sync(0xffffffffu, inc.hi, 1);
+    ex.lo = __shfl_up_sync(0xffffffffu, inc.lo, 1);
+    if (lane == 0) ex = CSum();
+    total.hi = __shfl_sync(0xffffffffu, inc.hi, 31);
+    total.lo = __shfl_sync(0xffffffffu, inc.lo, 31);
+    return ex;
+}
+
+template <int GW>
+struct SmallShared {
+    float M[GW == 1 ? 8 : 1][kMaxRows];
+    float L2Z[GW == 1 ? 8 : 1][kMaxRows];
+    int arg[GW == 1 ? 8 : 1][kMaxRows];
+    int j[GW == 1 ? 8 : 1];
+    float scan[64];
+    int first, lastpos;
+};
+
+template <int GW>
+__device__ __forceinline__ void group_sync() {
+    if (GW == 1) __syncwarp();
+    else __syncthreads();
+}
+
+template <int GW, bool VEC>
+__global__ void __launch_bounds__(256) pqv_small_kernel(PqArgs a) {
+    __shared__ SmallShared<GW> sh;
     pdl_wait();
     pdl_trigger();
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int gi = GW == 1 ? warp : 0;                      // this group's slot in shared memory
+    const int gt = GW == 1 ? lane : (int)threadIdx.x;        // thread index inside the group
+    const int gwarp = GW == 1 ? 0 : warp;                    // warp index inside the group
+    const int gthreads = 32 * GW;
+    const int s = GW == 1 ? (int)blockIdx.x * 8 + warp : (int)blockIdx.x;
+    if (s >= a.S) return;  // whole groups only: no group barrier is skipped by part of a group
     const int R = 2 * a.k + 1;
-    for (int s = blockIdx.x * kWarpTierWarps + warp; s < a.S; s += gridDim.x * kWarpTierWarps) {
-        float beta;
-        const int smode = session_mode(a, s, &beta);
-        if (smode < 0) {
-            if (lane == 0) {
-                set_status(a.status, Q2_ERR_BAD_TEMPERATURE);
-                write_tokens(a, s, -1, -1);
-            }
-            __syncwarp();
-            continue;
+    float beta;
+    const int smode = session_mode(a, s, &beta);
+    if (smode < 0) {
+        if (gt == 0) {
+            set_status(a.status, Q2_ERR_BAD_TEMPERATURE);
+            write_tokens(a, s, -1, -1);
         }
-        if (smode == 0) {
-            // greedy: the argmax of every row (the target rows decide; all rows for probs)
+        return;
+    }
+    if (smode == 0) {
+        // greedy: the argmax of every row (the target rows decide; all rows for probs)
+        for (int r = gwarp; r < R; r += GW) {
+            const int i = warp_row_argmax(row_ptr(a, s, r), a.V, lane);
+            if (lane == 0) sh.arg[gi][r] = i;
+        }
+        group_sync<GW>();
+        if (a.probs)
             for (int r = 0; r < R; ++r) {
-                float m;
-                int i;
-                lane_argmax(row_ptr(a, s, r), 0, a.V, lane, m, i);
-                warp_argmax(m, i);
-                if (lane == 0) sArg[warp][r] = i;
+                float *o = a.probs + ((size_t)s * R + r) * a.V;
+                const int am = sh.arg[gi][r];
+                for (int y = gt; y < a.V; y += gthreads) o[y] = (y == am) ? 1.0f : 0.0f;
             }
-            __syncwarp();
-            int j = 0;
-            if (lane == 0) j = greedy_scan(a, s, sArg[warp]);
-            j = __shfl_sync(0xffffffffu, j, 0);
-            if (a.probs)
-                for (int r = 0; r < R; ++r) {
-                    float *o = a.probs + ((size_t)s * R + r) * a.V;
-                    const int am = sArg[warp][r];
-                    for (int y = lane; y < a.V; y += 32) o[y] = (y == am) ? 1.0f : 0.0f;
-                }
-            if (lane == 0) {
-                if (j < 0) set_status(a.status, Q2_ERR_BAD_TOKEN);
-                write_tokens(a, s, j, j < 0 ? -1 : sArg[warp][j]);
-            }
-            __syncwarp();
-            continue;
+        if (gt == 0) {
+            const int j = greedy_scan(a, s, sh.arg[gi]);
+            if (j < 0) set_status(a.status, Q2_ERR_BAD_TOKEN);
+            write_tokens(a, s, j, j < 0 ? -1 : sh.arg[gi][j]);
         }
+        return;
+    }
+    // 1. every row's statistics (warps of the group take rows in turn)
+    for (int r = gwarp; r < R; r += GW) {
+        float M, L2;
+        warp_row_stats<VEC>(row_ptr(a, s, r), a.V, beta, lane, M, L2);
+        if (lane == 0) {
+            sh.M[gi][r] = M;
+            sh.L2Z[gi][r] = L2;
+        }
+    }
+    group_sync<GW>();
+    // 2. accept scan: lane i evaluates draft i, a ballot finds the first rejection
+    if (gwarp == 0) {
+        bool bad = false, rej = false;
+        if (lane < a.k) {
+            const int xv = a.drafts[(size_t)s * a.k + lane];
+            if (xv < 0 || xv >= a.V) {
+                bad = true;
+            } else {
+                const float tx = row_ptr(a, s, lane)[xv], dx = row_ptr(a, s, a.k + 1 + lane)[xv];
+                if (dx != -INFINITY) {  // q(x) == 0 accepts
+                    const float lp = (tx - sh.M[gi][lane]) * beta - sh.L2Z[gi][lane];
+                    const float lq = (dx - sh.M[gi][a.k + 1 + lane]) * beta - sh.L2Z[gi][a.k + 1 + lane];
+                    rej = !(a.u_acc[(size_t)s * a.k + lane] < ex2(lp - lq));
+                }
+            }
+        }
+        const unsigned badm = __ballot_sync(0xffffffffu, bad), rejm = __ballot_sync(0xffffffffu, rej);
+        if (lane == 0) sh.j[gi] = badm ? -1 : (rejm ? __ffs(rejm) - 1 : a.k);
+    }
+    group_sync<GW>();
+    const int j = sh.j[gi];
+    if (a.probs)
         for (int r = 0; r < R; ++r) {
             const float *x = row_ptr(a, s, r);
-            float m = -INFINITY, z = 0.0f;
-            for (int y = lane; y < a.V; y += 32) {
-                const float v = x[y];
-                if (v > m) {
-                    z = z * ex2((m - v) * beta) + 1.0f;
-                    m = v;
-                } else if (v > -INFINITY) {
-                    z += ex2((v - m) * beta);
-                }
-            }
-            const float M = warp_max(m);
-            const float zz = warp_sum((m > -INFINITY) ? z * ex2((m - M) * beta) : 0.0f);
-            if (lane == 0) {
-                sM[warp][r] = M;
-                sL2Z[warp][r] = log2f(zz);
-            }
+            float *o = a.probs + ((size_t)s * R + r) * a.V;
+            const float M = sh.M[gi][r], L2 = sh.L2Z[gi][r];
+            for (int y = gt; y < a.V; y += gthreads) o[y] = ex2((x[y] - M) * beta - L2);
         }
-        __syncwarp();
-        int j = 0;
-        if (lane == 0) j = accept_scan(a, s, beta, sM[warp], sL2Z[warp]);
-        j = __shfl_sync(0xffffffffu, j, 0);
-        if (a.probs) {
-            for (int r = 0; r < R; ++r) {
-                const float *x = row_ptr(a, s, r);
-                float *o = a.probs + ((size_t)s * R + r) * a.V;
-                const float M = sM[warp][r], L2 = sL2Z[warp][r];
-                for (int y = lane; y < a.V; y += 32) o[y] = ex2((x[y] - M) * beta - L2);
+    if (j < 0) {
+        if (gt == 0) {
+            set_status(a.status, Q2_ERR_BAD_TOKEN);
+            write_tokens(a, s, -1, -1);
+        }
+        return;
+    }
+    // 3. the draw: this thread's run of tokens, weights in registers
+    DrawRows D = draw_rows(a, s, j, sh.M[gi], sh.L2Z[gi]);
+    const int run = cdiv(a.V, gthreads);  // <= kSmallMaxRun
+    const int y0 = min(a.V, gt * run), y1 = min(a.V, y0 + run);
+    float xt[kSmallMaxRun], xd[kSmallMaxRun], w[kSmallMaxRun];
+#pragma unroll
+    for (int u = 0; u < kSmallMaxRun; ++u) {
+        const int y = y0 + u;
+        xt[u] = y < y1 ? D.t[y] : 0.0f;
+        xd[u] = (y < y1 && D.mode == 0) ? D.d[y] : xt[u];
+    }
+    CSum own, excl, tot;
+    int mode = D.mode;
+    for (int pass = 0; pass < 2; ++pass) {  // pass 1 only when the residual has no mass
+        D.mode = mode;
+        own = CSum();
+#pragma unroll
+        for (int u = 0; u < kSmallMaxRun; ++u) {
+            w[u] = y0 + u < y1 ? draw_weight(D, beta, xt[u], xd[u]) : 0.0f;
+            if (y0 + u < y1) own.add(w[u]);
+        }
+        if (GW == 1) {
+            excl = warp_excl_scan_c(own, lane, tot);
+        } else {
+            group_sync<GW>();  // sh.scan is free again
+            excl = block_excl_scan(own, sh.scan, tot);
+        }
+        if (mode == 1 || tot.hi > 0.0f) break;
+        mode = 1;  // zero residual mass: draw from p_j
+    }
+    const float target = a.u_fin[s] * (tot.hi + tot.lo);
+    const float own_m = own.hi + own.lo;
+    const bool crosses = own_m > 0.0f && excl.exceeds(own_m, target);
+    int first, lastpos;
+    if (GW == 1) {
+        const unsigned cm = __ballot_sync(0xffffffffu, crosses), pm = __ballot_sync(0xffffffffu, own_m > 0.0f);
+        first = cm ? __ffs(cm) - 1 : gthreads;
+        lastpos = pm ? 31 - __clz(pm) : -1;
+    } else {
+        if (gt == 0) {
+            sh.first = gthreads;
+            sh.lastpos = -1;
+        }
+        __syncthreads();
+        if (own_m > 0.0f) atomicMax(&sh.lastpos, gt);
+        if (crosses) atomicMin(&sh.first, gt);
+        __syncthreads();
+        first = sh.first;
+        lastpos = sh.lastpos;
+    }
+    const int owner = first < gthreads ? first : lastpos;
+    if (owner < 0) {
+        if (gt == 0) write_tokens(a, s, j, -1);
+        return;
+    }
+    if (gt == owner) {
+        // the first token of this run whose cumulative mass passes the target (else its last
+        // token with mass)
+        CSum pre = excl;
+        int found = -1, last_nz = -1;
+#pragma unroll
+        for (int u = 0; u < kSmallMaxRun; ++u) {
+            if (found < 0 && y0 + u < y1 && w[u] > 0.0f) {
+                last_nz = y0 + u;
+                if (first < gthreads && pre.exceeds(w[u], target)) found = y0 + u;
             }
+            if (found < 0) pre.add(w[u]);
         }
-        if (j < 0) {
-            if (lane == 0) {
-                set_status(a.status, Q2_ERR_BAD_TOKEN);
-                write_tokens(a, s, -1, -1);
-            }
-            __syncwarp();
-            continue;
-        }
-        DrawRows D = draw_rows(a, s, j, sM[warp], sL2Z[warp]);
-        // pass 1: the total mass, scanned in chunks of 32 exactly as pass 2 scans
-        CSum total;
-        for (int pass = 0; pass < 2; ++pass) {
-            total = CSum();
-            for (int base = 0; base < a.V; base += 32) {
-                const int y = base + lane;
-                const float w = y < a.V ? draw_weight(D, beta, D.t[y], D.d[y]) : 0.0f;
-                total.add(__shfl_sync(0xffffffffu, warp_incl_scan(w, lane), 31));
-            }
-            if (total.value() > 0.0f || D.mode == 1) break;
-            D.mode = 1;  // zero residual mass: draw from p_j
-        }
-        const float target = a.u_fin[s] * total.value();
-        CSum carry;
-        int y_sel = -1, last_pos = -1;
-        for (int base = 0; base < a.V && y_sel < 0; base += 32) {
-            const int y = base + lane;
-            const float w = y < a.V ? draw_weight(D, beta, D.t[y], D.d[y]) : 0.0f;
-            const float incl = warp_incl_scan(w, lane);
-            const unsigned hit = __ballot_sync(0xffffffffu, w > 0.0f && carry.exceeds(incl, target));
-            const unsigned pos = __ballot_sync(0xffffffffu, w > 0.0f);
-            if (pos) last_pos = base + 31 - __clz(pos);
-            if (hit) y_sel = base + __ffs(hit) - 1;
-            carry.add(__shfl_sync(0xffffffffu, incl, 31));
-        }
-        if (y_sel < 0) y_sel = last_pos;
-        if (lane == 0) write_tokens(a, s, j, y_sel);
-        __syncwarp();
+        write_tokens(a, s, j, found >= 0 ? found : last_nz);
     }
 }
 
@@ -839,9 +987,17 @@ cudaError_t launch_pdl_smem(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
 
 cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier, int num_sms, cudaStream_t st) {
     if (warp_tier) {
-        const int blocks = max(1, min(cdiv(a.S, kWarpTierWarps), num_sms * 8));
-        return probed(kProbePqVerify, st, [&] {
-            return launch_pdl(pqv_warp_kernel, dim3(blocks), dim3(kWarpTierWarps * 32), st, a);
+        const bool vec = (a.V % 4) == 0;
+        if (a.V <= kSmallWarpMaxV) {  // one warp per session, 8 sessions per CTA
+            const dim3 grid(cdiv(a.S, 8));
+            return probed(kProbePqVerify, st, [&] {
+                return vec ? launch_pdl(pqv_small_kernel<1, true>, grid, dim3(256), st, a)
+                           : launch_pdl(pqv_small_kernel<1, false>, grid, dim3(256), st, a);
+            });
+        }
+        return probed(kProbePqVerify, st, [&] {  // one CTA per session
+            return vec ? launch_pdl(pqv_small_kernel<8, true>, dim3(a.S), dim3(256), st, a)
+                       : launch_pdl(pqv_small_kernel<8, false>, dim3(a.S), dim3(256), st, a);
         });
     }
     const bool vec = (a.V % 4) == 0 && (sp.L % 4) == 0;

@@ -62,7 +62,7 @@ def test_workspace_queries(lib):
     assert lib.q2_tiny_gemm_workspace(3, 4096, 160) < 256 + 3 * 160 * 4 + 4096  # K % 128 != 0: mma.sync only
     assert lib.q2_tiny_gemm_workspace(60, 129280, 4096) >= 256 + 64 * 4096 * 2  # 60 rows pad to 64 columns
     assert lib.q2_tiny_gemm_workspace(0, 4096, 4096) == 256       # invalid sizes: header only
-    assert lib.pq_verify_workspace(1, 4, 1024) == 256             # warp tier needs only the header
+    assert lib.pq_verify_workspace(1, 4, 1024) == 256             # small-V tier needs only the header
     pq3 = lib.pq_verify_workspace(3, 4, 129280)
     assert pq3 >= 256 + 3 * 9 * 8 and pq3 < 4 << 20
     assert lib.pq_verify_workspace(3, 4, 129280) < lib.pq_verify_workspace(12, 4, 129280)

@@ -124,7 +124,7 @@ def test_fused_lm_head_verify_mixed_temperatures(cohort):
 
 
 @pytest.mark.parametrize("S,k,V,K", [(2, 4, 8192, 1024),    # M=10: mma.sync GEMM, unfused
-                                     (4, 4, 1024, 512),     # M=20 tcgen05, small-V warp tier: unfused
+                                     (4, 4, 1024, 512),     # M=20 tcgen05, small-V tier: unfused
                                      (6, 4, 20000, 512),    # M=30 tcgen05, fused, ragged last tile
                                      (1, 4, 40000, 512),    # M=5 tcgen05 (wide V), fused
                                      (2, 3, 36000, 256),    # M=8 tcgen05, fused, ragged last tile

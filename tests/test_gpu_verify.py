@@ -62,15 +62,19 @@ def test_batched_config_full_size(env):
 
 
 @pytest.mark.parametrize("S,k,V,T", [
-    (64, 4, 1024, 1.0),      # warp tier, many sessions
-    (5, 4, 4096, 0.7),       # largest warp-tier V
+    (64, 4, 1024, 1.0),      # small-V tier (a CTA per session), many sessions
+    (5, 4, 4096, 0.7),       # largest small-V tier V: 16 tokens per thread in the draw
+    (3, 16, 512, 1.0),       # largest V of one warp per session, the largest k (33 rows in one warp)
+    (6, 4, 513, 1.0),        # smallest V of a CTA per session, V % 4 != 0 (scalar loads)
+    (11, 3, 17, 0.8),        # one warp per session, scalar loads, 1 token per lane in the draw
+    (2, 16, 4000, 1.2),      # a CTA per session with 33 rows over 8 warps
     (5, 4, 4097, 1.0),       # smallest split-tier V, V % 4 != 0 (scalar loads)
     (7, 3, 10000, 1.5),      # ragged last chunk
     (40, 4, 32768, 1.0),     # many sessions: few chunks each
     (320, 2, 20000, 1.0),    # one chunk per session: segments of 2,512 tokens, 10 per thread in the draw
     (2, 16, 8192, 1.0),      # the largest k
     (3, 0, 5000, 1.0),       # k = 0: plain sampling from p_0
-    (9, 0, 300, 0.9),        # k = 0 in the warp tier
+    (9, 0, 300, 0.9),        # k = 0 in the small-V tier
     (4, 2, 1, 1.0),          # V = 1
     (4, 4, 129280, 50.0),    # near-uniform p and q: CDF cells ~7.7e-6 wide, residuals of nearly equal probabilities
 ])
