@@ -460,6 +460,33 @@ def run_device(args, rank: int, world: int):
                  "us": l_us, "GB/s": l_bytes / (l_us * 1e-6) / 1e9, "frac": l_bytes / (l_us * 1e-6) / 1e9 / peak_x}
         del layers
 
+    # the tiny configuration: the K=256, N=512 Q2B32 linear at M = 1..4 and pq_verify of one
+    # session (k=4, V=1024), each timed as 4 distinct calls back to back in one graph
+    tiny = None
+    if not args.no_extras:
+        tg = [synth.config_gemm(0, M=mm) for mm in (1, 2, 3, 4)]
+        tgd = [(D(g0["W"].reshape(-1)), D(g0["A"]), g0["M"]) for g0 in tg]
+        Yt = torch.empty((4, 512), dtype=torch.float32, device=dev)
+        wst = q2v.workspace(q2v.q2_tiny_gemm_workspace(4, 512, 256), dev)
+        tv = [synth.config_verify(0, salt=i) for i in range(4)]
+        tvd = [{n: D(v0[n]) for n in ("target", "draft", "drafts", "u_acc", "u_fin")} for v0 in tv]
+        nt = torch.empty(1, dtype=torch.int32, device=dev)
+        tt = torch.empty((1, 5), dtype=torch.int32, device=dev)
+        wsv0 = q2v.workspace(q2v.pq_verify_workspace(1, 4, 1024), dev)
+
+        def tiny_gemm():
+            for W0, A0, M0 in tgd:
+                q2v.q2_tiny_gemm(W0, 512, 256, A0, Y=Yt[:M0], ws=wst)
+
+        def tiny_pq():
+            for d0 in tvd:
+                q2v.pq_verify(d0["target"], d0["draft"], d0["drafts"], d0["u_acc"], d0["u_fin"], tv[0]["T"],
+                              n_acc=nt, tokens=tt, ws=wsv0)
+
+        tiny = {"workload": "Q2B32 linear K=256 N=512 at M=1,2,3,4; pq_verify S=1 k=4 V=1024 T=1",
+                "gemm_us_per_call": graph_us(tiny_gemm, max(5, args.steps)) / 4,
+                "pq_verify_us_per_call": graph_us(tiny_pq, max(5, args.steps)) / 4}
+
     # the cohort verify: 12 sessions x 5 rows = M=60 against a 129,280 x 4096 Q2B32 vocabulary
     # head on the tcgen05 path, then pq_verify (S=12, k=4) over those logits
     cohort = None
@@ -661,6 +688,7 @@ def run_device(args, rank: int, world: int):
         "chained_linears_m5": chain,
         "verifier_layer_m5": layer,
         "cohort_m60": cohort,
+        "tiny_cfg0": tiny,
         "clocks": clocks,
     }
     return line, dict(host0=host0, gpu0=gpu0, cohort=cohort_host)

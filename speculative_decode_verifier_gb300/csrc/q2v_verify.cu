@@ -252,7 +252,9 @@ __device__ __forceinline__ DrawRows draw_rows(const PqArgs &a, int s, int j, con
 // ===================================================================== small-V tier
 //
 // V <= kWarpTierMaxV: a group of GW warps per session does everything in one kernel (one warp
-// per session for V <= kSmallWarpMaxV, eight warps -- the whole CTA -- above).  Every load is
+// per session for V <= kSmallWarpMaxV, sixteen warps -- the whole CTA -- above).  The accept
+// scan's inputs (draft tokens, uniforms, both logits at each draft) are requested first, so
+// they arrive while the row statistics stream.  Every load is
 // issued in batches before any of it is used: a row's statistics take one batch per 32 x 32
 // floats (float4 loads) or 32 x 16 (scalar), the accept scan is lane-parallel (one lane per
 // draft, a ballot finds the first rejection), and the draw gives each thread a contiguous run
@@ -260,7 +262,7 @@ __device__ __forceinline__ DrawRows draw_rows(const PqArgs &a, int s, int j, con
 // finds the run, and the run's owner the token.
 
 constexpr int kSmallWarpMaxV = 512;   // one warp per session up to this V
-constexpr int kSmallMaxRun = 16;      // tokens per thread in the draw
+constexpr int kSmallMaxRun = 16;      // tokens per lane in the draw, one warp per session
 
 // (max, log2 sum 2^((x - max) beta)) of one row of V logits, by one warp; loads in batches.
 template <bool VEC>
@@ -341,6 +343,8 @@ __device__ __forceinline__ CSum warp_excl_scan_c(const CSum &v, int lane, CSum &
     return ex;
 }
 
+constexpr int kSmallCtaWarps = 16;  // warps of the CTA-per-session variant
+
 template <int GW>
 struct SmallShared {
     float M[GW == 1 ? 8 : 1][kMaxRows];
@@ -358,7 +362,7 @@ __device__ __forceinline__ void group_sync() {
 }
 
 template <int GW, bool VEC>
-__global__ void __launch_bounds__(256) pqv_small_kernel(PqArgs a) {
+__global__ void __launch_bounds__(GW == 1 ? 256 : 32 * GW) pqv_small_kernel(PqArgs a) {
     __shared__ SmallShared<GW> sh;
     pdl_wait();
     pdl_trigger();
@@ -399,6 +403,17 @@ __global__ void __launch_bounds__(256) pqv_small_kernel(PqArgs a) {
         }
         return;
     }
+    // 0. the accept scan's inputs, requested before the statistics (lane i: draft i)
+    int xv = 0;
+    float tx = 0.0f, dx = 0.0f, uv = 0.0f;
+    if (gwarp == 0 && lane < a.k) {
+        xv = a.drafts[(size_t)s * a.k + lane];
+        uv = a.u_acc[(size_t)s * a.k + lane];
+        if (xv >= 0 && xv < a.V) {
+            tx = row_ptr(a, s, lane)[xv];
+            dx = row_ptr(a, s, a.k + 1 + lane)[xv];
+        }
+    }
     // 1. every row's statistics (warps of the group take rows in turn)
     for (int r = gwarp; r < R; r += GW) {
         float M, L2;
@@ -413,16 +428,12 @@ __global__ void __launch_bounds__(256) pqv_small_kernel(PqArgs a) {
     if (gwarp == 0) {
         bool bad = false, rej = false;
         if (lane < a.k) {
-            const int xv = a.drafts[(size_t)s * a.k + lane];
             if (xv < 0 || xv >= a.V) {
                 bad = true;
-            } else {
-                const float tx = row_ptr(a, s, lane)[xv], dx = row_ptr(a, s, a.k + 1 + lane)[xv];
-                if (dx != -INFINITY) {  // q(x) == 0 accepts
-                    const float lp = (tx - sh.M[gi][lane]) * beta - sh.L2Z[gi][lane];
-                    const float lq = (dx - sh.M[gi][a.k + 1 + lane]) * beta - sh.L2Z[gi][a.k + 1 + lane];
-                    rej = !(a.u_acc[(size_t)s * a.k + lane] < ex2(lp - lq));
-                }
+            } else if (dx != -INFINITY) {  // q(x) == 0 accepts
+                const float lp = (tx - sh.M[gi][lane]) * beta - sh.L2Z[gi][lane];
+                const float lq = (dx - sh.M[gi][a.k + 1 + lane]) * beta - sh.L2Z[gi][a.k + 1 + lane];
+                rej = !(uv < ex2(lp - lq));
             }
         }
         const unsigned badm = __ballot_sync(0xffffffffu, bad), rejm = __ballot_sync(0xffffffffu, rej);
@@ -446,11 +457,12 @@ __global__ void __launch_bounds__(256) pqv_small_kernel(PqArgs a) {
     }
     // 3. the draw: this thread's run of tokens, weights in registers
     DrawRows D = draw_rows(a, s, j, sh.M[gi], sh.L2Z[gi]);
-    const int run = cdiv(a.V, gthreads);  // <= kSmallMaxRun
+    constexpr int MR = GW == 1 ? kSmallMaxRun : kWarpTierMaxV / (32 * GW);  // tokens per thread, at most
+    const int run = cdiv(a.V, gthreads);  // <= MR
     const int y0 = min(a.V, gt * run), y1 = min(a.V, y0 + run);
-    float xt[kSmallMaxRun], xd[kSmallMaxRun], w[kSmallMaxRun];
+    float xt[MR], xd[MR], w[MR];
 #pragma unroll
-    for (int u = 0; u < kSmallMaxRun; ++u) {
+    for (int u = 0; u < MR; ++u) {
         const int y = y0 + u;
         xt[u] = y < y1 ? D.t[y] : 0.0f;
         xd[u] = (y < y1 && D.mode == 0) ? D.d[y] : xt[u];
@@ -461,7 +473,7 @@ __global__ void __launch_bounds__(256) pqv_small_kernel(PqArgs a) {
         D.mode = mode;
         own = CSum();
 #pragma unroll
-        for (int u = 0; u < kSmallMaxRun; ++u) {
+        for (int u = 0; u < MR; ++u) {
             w[u] = y0 + u < y1 ? draw_weight(D, beta, xt[u], xd[u]) : 0.0f;
             if (y0 + u < y1) own.add(w[u]);
         }
@@ -505,7 +517,7 @@ __global__ void __launch_bounds__(256) pqv_small_kernel(PqArgs a) {
         CSum pre = excl;
         int found = -1, last_nz = -1;
 #pragma unroll
-        for (int u = 0; u < kSmallMaxRun; ++u) {
+        for (int u = 0; u < MR; ++u) {
             if (found < 0 && y0 + u < y1 && w[u] > 0.0f) {
                 last_nz = y0 + u;
                 if (first < gthreads && pre.exceeds(w[u], target)) found = y0 + u;
@@ -995,9 +1007,10 @@ cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier,
                            : launch_pdl(pqv_small_kernel<1, false>, grid, dim3(256), st, a);
             });
         }
+        const dim3 block(32 * kSmallCtaWarps);
         return probed(kProbePqVerify, st, [&] {  // one CTA per session
-            return vec ? launch_pdl(pqv_small_kernel<8, true>, dim3(a.S), dim3(256), st, a)
-                       : launch_pdl(pqv_small_kernel<8, false>, dim3(a.S), dim3(256), st, a);
+            return vec ? launch_pdl(pqv_small_kernel<kSmallCtaWarps, true>, dim3(a.S), block, st, a)
+                       : launch_pdl(pqv_small_kernel<kSmallCtaWarps, false>, dim3(a.S), block, st, a);
         });
     }
     const bool vec = (a.V % 4) == 0 && (sp.L % 4) == 0;
