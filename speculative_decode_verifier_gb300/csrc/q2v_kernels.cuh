@@ -65,6 +65,7 @@ struct PqSplit {
     // streams the draft rows and the combine reads the target rows from here.
     const float *tstats;
     int Ct;
+    unsigned int *bar;   // [S][2] arrival counters of the single-kernel path's two session barriers
 };
 
 cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier, int num_sms, cudaStream_t st);

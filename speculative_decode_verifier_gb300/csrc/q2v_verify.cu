@@ -978,6 +978,343 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
     if (tid == 0) write_tokens(a, s, j, y_sel);
 }
 
+// ===================================================================== large-V tier, one kernel
+//
+// When every session samples with the one temperature (pq_verify), V % 4 == 0 and the grid of
+// C x S chunks fits on the GPU at once with each CTA holding its chunk of all 2k+1 rows in
+// shared memory, the two kernels above become one:
+//   A. the CTA copies its chunk of every row into shared memory with one bulk copy per row
+//      (an mbarrier counts the bytes), while lanes of warp 0 fetch the accept scan's inputs;
+//   B. per-row (max, sum) partials of the chunk, from shared memory, to the workspace;
+//   C. a session barrier (an arrival counter per session, a bounded spin by one thread);
+//   D. the combine of the partials and the accept scan, as in kernel 2;
+//   E. the draw masses of the chunk's 8 segments, from shared memory, to the workspace;
+//   F. a second session barrier;
+//   G. every CTA scans the session's segment masses (the same compensated block scan as the
+//      last-arriver search) and the CTA that owns the chosen segment finds the token in its
+//      shared-memory copy of the rows and writes the session's result.
+// The grid is sized so that all its CTAs are resident together (the host checks occupancy);
+// the barriers' counters are zeroed by a one-CTA kernel launched just before.  Every wait is
+// bounded: after kPqWaitNs the thread records Q2_ERR_TIMEOUT and carries on (the results are
+// then undefined).
+
+constexpr unsigned long long kPqWaitNs = 1000000000ull;  // 1 s
+
+__device__ __forceinline__ uint32_t pq_smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
+__device__ __forceinline__ uint64_t pq_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
+    return t;
+}
+__device__ __forceinline__ bool pq_mbar_try(uint64_t *bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(pq_smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// A spin on phase 0 of `bar`, bounded; false (and Q2_ERR_TIMEOUT recorded by thread 0) if the
+// time ran out.
+__device__ __forceinline__ bool pq_mbar_wait(uint64_t *bar, unsigned int *status) {
+    if (pq_mbar_try(bar, 0)) return true;
+    const uint64_t t0 = pq_ns();
+    while (!pq_mbar_try(bar, 0)) {
+        if (pq_ns() - t0 > kPqWaitNs) {
+            if (threadIdx.x == 0) set_status(status, Q2_ERR_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
+// One thread: arrive at a session barrier of `expected` CTAs and spin (bounded) until all
+// have arrived.  The fence before the arrival releases this CTA's writes; the acquire load
+// that sees the full count makes the other CTAs' writes visible.
+__device__ __forceinline__ bool pq_session_barrier(unsigned int *ctr, unsigned int expected, unsigned int *status) {
+    __threadfence();
+    atomicAdd(ctr, 1u);
+    const uint64_t t0 = pq_ns();
+    for (;;) {
+        unsigned int v;
+        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(ctr) : "memory");
+        if (v >= expected) return true;
+        if (pq_ns() - t0 > kPqWaitNs) {
+            set_status(status, Q2_ERR_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+__global__ void __launch_bounds__(32) pqv_bar_reset_kernel(unsigned int *bar, int n) {
+    pdl_trigger();
+    pdl_wait();
+    for (int i = threadIdx.x; i < n; i += 32) bar[i] = 0u;
+}
+
+__global__ void __launch_bounds__(256) pqv_fused_kernel(PqArgs a, PqSplit sp) {
+    extern __shared__ __align__(16) float pf_rows[];  // [R][L] chunk rows, then [C * 8] segment masses
+    __shared__ __align__(8) uint64_t mbar;
+    __shared__ float rowM[kMaxRows];
+    __shared__ float rowL2Z[kMaxRows];
+    __shared__ int s_j, s_ok;
+    __shared__ float s_scan[64];
+    __shared__ int s_first, s_lastpos, s_ent;
+    __shared__ float s_pre[2];
+    pdl_wait();
+    pdl_trigger();
+    const int c = blockIdx.x, s = blockIdx.y;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nt = blockDim.x;
+    const int R = 2 * a.k + 1;
+    const float beta = a.beta;
+    const int L = sp.L, c0 = c * L, n = min(L, a.V - c0);  // n % 4 == 0
+    const int Lw = L / kSegsPerChunk;
+    float *msm = pf_rows + (size_t)R * L;
+    // A. the chunk of every row into shared memory
+    if (tid == 0) {
+        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(pq_smem_u32(&mbar)) : "memory");
+        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
+    }
+    __syncthreads();
+    if (tid == 0) {
+        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(pq_smem_u32(&mbar)),
+                     "r"((uint32_t)(R * n * 4))
+                     : "memory");
+        for (int r = 0; r < R; ++r)
+            asm volatile(
+                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
+                    pq_smem_u32(pf_rows + (size_t)r * L)),
+                "l"(row_ptr(a, s, r) + c0), "r"((uint32_t)(n * 4)), "r"(pq_smem_u32(&mbar))
+                : "memory");
+    }
+    // the accept scan's inputs, in flight while the rows stream in (lane i: draft i)
+    int xv = 0;
+    float tx = 0.0f, dx = 0.0f, uv = 0.0f;
+    if (warp == 0 && lane < a.k) {
+        xv = a.drafts[(size_t)s * a.k + lane];
+        uv = a.u_acc[(size_t)s * a.k + lane];
+        if (xv >= 0 && xv < a.V) {
+            tx = row_ptr(a, s, lane)[xv];
+            dx = row_ptr(a, s, a.k + 1 + lane)[xv];
+        }
+    }
+    if (!pq_mbar_wait(&mbar, a.status)) {
+        // the copies have not landed in time: let them land before this CTA's shared memory is
+        // used or released (bounded again), then carry on with an error recorded
+        const uint64_t t0 = pq_ns();
+        while (!pq_mbar_try(&mbar, 0) && pq_ns() - t0 < kPqWaitNs) {
+        }
+    }
+    // B. the chunk's (max, sum 2^((x - max) beta)) of every row
+    for (int r = warp; r < R; r += nt >> 5) {
+        const float4 *x4 = reinterpret_cast<const float4 *>(pf_rows + (size_t)r * L);
+        float m = -INFINITY;
+        for (int i = lane; i < (n >> 2); i += 32) {
+            const float4 v = x4[i];
+            m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+        }
+        const float M = warp_max(m);
+        float z = 0.0f;
+        if (M > -INFINITY)
+            for (int i = lane; i < (n >> 2); i += 32) {
+                const float4 v = x4[i];
+                z += ex2((v.x - M) * beta) + ex2((v.y - M) * beta) + ex2((v.z - M) * beta) + ex2((v.w - M) * beta);
+            }
+        z = warp_sum(z);
+        if (lane == 0) reinterpret_cast<float2 *>(sp.stats)[((size_t)s * R + r) * sp.C + c] = make_float2(M, z);
+    }
+    // C. every chunk's partials are written
+    __syncthreads();
+    if (tid == 0) s_ok = pq_session_barrier(sp.bar + 2 * s, (unsigned)sp.C, a.status);
+    __syncthreads();
+    // D. row statistics from the partials (16 lanes per row), then the accept scan
+    for (int r0 = 0; r0 < R; r0 += 16) {
+        const int r = r0 + (tid >> 4), sub = tid & 15;
+        const float2 *st = reinterpret_cast<const float2 *>(sp.stats) + ((size_t)s * R + min(r, R - 1)) * sp.C;
+        float m = -INFINITY;
+        for (int cc = sub; r < R && cc < sp.C; cc += 16) m = fmaxf(m, __ldcg(&st[cc].x));
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float z = 0.0f;
+        for (int cc = sub; r < R && cc < sp.C; cc += 16) {
+            const float2 w = __ldcg(&st[cc]);
+            if (w.x > -INFINITY) z += w.y * ex2((w.x - m) * beta);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
+        if (sub == 0 && r < R) {
+            rowM[r] = m;
+            rowL2Z[r] = log2f(z);
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        bool bad = false, rej = false;
+        if (lane < a.k) {
+            if (xv < 0 || xv >= a.V) {
+                bad = true;
+            } else if (dx != -INFINITY) {  // q(x) == 0 accepts
+                const float lp = (tx - rowM[lane]) * beta - rowL2Z[lane];
+                const float lq = (dx - rowM[a.k + 1 + lane]) * beta - rowL2Z[a.k + 1 + lane];
+                rej = !(uv < ex2(lp - lq));
+            }
+        }
+        const unsigned badm = __ballot_sync(0xffffffffu, bad), rejm = __ballot_sync(0xffffffffu, rej);
+        if (lane == 0) s_j = badm ? -1 : (rejm ? __ffs(rejm) - 1 : a.k);
+    }
+    __syncthreads();
+    const int j = s_j;
+    if (a.probs)
+        for (int r = 0; r < R; ++r) {
+            const float *x = pf_rows + (size_t)r * L;
+            float *o = a.probs + ((size_t)s * R + r) * a.V + c0;
+            const float M = rowM[r], L2 = rowL2Z[r];
+            for (int y = tid; y < n; y += nt) o[y] = ex2((x[y] - M) * beta - L2);
+        }
+    if (j < 0) {
+        if (c == 0 && tid == 0) {
+            set_status(a.status, Q2_ERR_BAD_TOKEN);
+            write_tokens(a, s, -1, -1);
+        }
+        return;  // every CTA of the session takes this exit: no barrier is left waiting
+    }
+    // E. the draw masses of this chunk's segments (warp w: segment w), from shared memory
+    DrawRows D = draw_rows(a, s, j, rowM, rowL2Z);
+    const float *rt = pf_rows + (size_t)j * L;
+    const float *rd = D.mode == 0 ? pf_rows + (size_t)(a.k + 1 + j) * L : rt;
+    {
+        const int ly0 = warp * Lw, ly1 = min(n, ly0 + Lw);
+        float wsum = 0.0f, psum = 0.0f;
+        for (int y = ly0 + lane; y < ly1; y += 32) {
+            const float xt = rt[y], xd = rd[y];
+            wsum += draw_weight(D, beta, xt, xd);
+            if (D.mode == 0) psum += ex2((xt - D.mt) * beta - D.lt);
+        }
+        wsum = warp_sum(wsum);
+        psum = warp_sum(psum);
+        if (lane == 0) {
+            const size_t e = ((size_t)s * sp.C + c) * kSegsPerChunk + warp;
+            sp.mass[e] = wsum;
+            sp.pmass[e] = psum;
+        }
+    }
+    // F. every chunk's masses are written
+    __syncthreads();
+    if (tid == 0) s_ok = pq_session_barrier(sp.bar + 2 * s + 1, (unsigned)sp.C, a.status);
+    __syncthreads();
+    // G. level 1 (every CTA): the segment holding the crossing of u_fin * total
+    const int nseg = sp.C * kSegsPerChunk;
+    const int q = cdiv(nseg, nt);
+    const int e0 = min(nseg, tid * q), e1 = min(nseg, e0 + q);
+    CSum own, excl, tot;
+    int mode = D.mode;
+    for (int pass = 0; pass < 2; ++pass) {  // pass 1 only when the residual has no mass
+        const float *wsrc = (pass == 0 ? sp.mass : sp.pmass) + (size_t)s * nseg;
+        for (int e = tid; e < nseg; e += 8 * nt) {
+            float v[8];
+#pragma unroll
+            for (int u = 0; u < 8; ++u) v[u] = e + u * nt < nseg ? __ldcg(wsrc + e + u * nt) : 0.0f;
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (e + u * nt < nseg) msm[e + u * nt] = v[u];
+        }
+        __syncthreads();
+        own = CSum();
+        for (int e = e0; e < e1; ++e) own.add(msm[e]);
+        excl = block_excl_scan(own, s_scan, tot);
+        if (mode == 1 || tot.hi > 0.0f) break;
+        mode = 1;  // zero residual mass: draw from p_j
+        __syncthreads();
+    }
+    D.mode = mode;
+    const float target = a.u_fin[s] * (tot.hi + tot.lo);
+    if (tid == 0) {
+        s_first = nt;
+        s_lastpos = -1;
+    }
+    __syncthreads();
+    const float own_m = own.hi + own.lo;
+    if (own_m > 0.0f) {
+        atomicMax(&s_lastpos, tid);
+        if (excl.exceeds(own_m, target)) atomicMin(&s_first, tid);
+    }
+    __syncthreads();
+    const int owner1 = s_first < nt ? s_first : s_lastpos;
+    if (owner1 < 0) {
+        if (c == 0 && tid == 0) write_tokens(a, s, j, -1);
+        return;
+    }
+    if (tid == owner1) {
+        CSum pre = excl, last_pre;
+        int found = -1, last_nz = -1;
+        CSum found_pre;
+        for (int e = e0; e < e1; ++e) {
+            const float me = msm[e];
+            if (me > 0.0f) {
+                last_nz = e;
+                last_pre = pre;
+                if (s_first < nt && pre.exceeds(me, target)) {
+                    found = e;
+                    found_pre = pre;
+                    break;
+                }
+            }
+            pre.add(me);
+        }
+        s_ent = found >= 0 ? found : last_nz;
+        const CSum pr = found >= 0 ? found_pre : last_pre;
+        s_pre[0] = pr.hi;
+        s_pre[1] = pr.lo;
+    }
+    __syncthreads();
+    const int ent = s_ent;
+    if (ent / kSegsPerChunk != c) return;  // another CTA of the session owns the segment
+    // level 2 (the owning CTA): the token inside the segment, from shared memory
+    const int sw = ent - c * kSegsPerChunk;
+    const int ly0s = sw * Lw, ly1s = min(n, ly0s + Lw);
+    const int r = cdiv(max(ly1s - ly0s, 0), nt);
+    const int y0 = min(ly1s, ly0s + tid * r), y1 = min(ly1s, y0 + r);
+    const float *rd2 = D.mode == 0 ? rd : rt;
+    CSum seg_pre;
+    seg_pre.hi = s_pre[0];
+    seg_pre.lo = s_pre[1];
+    CSum own2, tot2;
+    for (int y = y0; y < y1; ++y) own2.add(draw_weight(D, beta, rt[y], rd2[y]));
+    __syncthreads();  // s_scan is reused
+    const CSum excl2 = csum_plus(seg_pre, block_excl_scan(own2, s_scan, tot2));
+    if (tid == 0) {
+        s_first = nt;
+        s_lastpos = -1;
+    }
+    __syncthreads();
+    const float own2_m = own2.hi + own2.lo;
+    if (own2_m > 0.0f) {
+        atomicMax(&s_lastpos, tid);
+        if (excl2.exceeds(own2_m, target)) atomicMin(&s_first, tid);
+    }
+    __syncthreads();
+    const int owner2 = s_first < nt ? s_first : s_lastpos;
+    if (tid == owner2) {
+        CSum pre = excl2;
+        int found = -1, last_nz = -1;
+        for (int y = y0; y < y1; ++y) {
+            const float w = draw_weight(D, beta, rt[y], rd2[y]);
+            if (w > 0.0f) {
+                last_nz = y;
+                if (s_first < nt && pre.exceeds(w, target)) {
+                    found = y;
+                    break;
+                }
+            }
+            pre.add(w);
+        }
+        write_tokens(a, s, j, c0 + (found >= 0 ? found : last_nz));
+    }
+    if (owner2 < 0 && tid == 0) write_tokens(a, s, j, -1);
+}
+
 namespace {
 // launch_pdl with dynamic shared memory
 template <typename... KArgs, typename... Args>
@@ -996,6 +1333,34 @@ cudaError_t launch_pdl_smem(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 }  // namespace
+
+// Resident CTAs per SM of pqv_fused_kernel with `smem` bytes of dynamic shared memory (0 if it
+// cannot run), with the shared-memory opt-in it needs; cached per device for the last size.
+int fused_blocks_per_sm(size_t smem) {
+    static size_t cached_smem[kCacheDevices];
+    static int cached_blocks[kCacheDevices];
+    static size_t optin[kCacheDevices];
+    const int dv = cache_device();
+    if (dv >= 0 && cached_smem[dv] == smem && cached_blocks[dv] > 0) return cached_blocks[dv];
+    if (dv < 0 || optin[dv] < smem) {
+        if (cudaFuncSetAttribute(pqv_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess) {
+            (void)cudaGetLastError();  // an unsupported size is not an error of the call: the split path runs
+            return 0;
+        }
+        if (dv >= 0) optin[dv] = smem;
+    }
+    int blocks = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, pqv_fused_kernel, 256, smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    if (dv >= 0) {
+        cached_smem[dv] = smem;
+        cached_blocks[dv] = blocks;
+    }
+    return blocks;
+}
 
 cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier, int num_sms, cudaStream_t st) {
     if (warp_tier) {
@@ -1016,6 +1381,22 @@ cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier,
     const bool vec = (a.V % 4) == 0 && (sp.L % 4) == 0;
     const int R = 2 * a.k + 1;
     const dim3 grid(sp.C, a.S);
+    // the one-kernel path when it applies (one temperature, no partials from elsewhere, rows of
+    // 16-byte multiples, and the whole grid resident at once with its rows in shared memory)
+    if (!a.temps && !sp.tstats && vec && sp.bar) {
+        const size_t smem = ((size_t)R * sp.L + (size_t)sp.C * kSegsPerChunk) * sizeof(float);
+        const int blocks = fused_blocks_per_sm(smem);
+        if (blocks > 0 && (long long)blocks * num_sms >= (long long)sp.C * a.S) {
+            cudaError_t e = launch_pdl(pqv_bar_reset_kernel, dim3(1), dim3(32), st, sp.bar, 2 * a.S);
+            if (e != cudaSuccess) return e;
+            // both probes bracket the one kernel (it is the statistics pass and the draw)
+            return probed(kProbePqStats, st, [&] {
+                return probed(kProbePqVerify, st, [&] {
+                    return launch_pdl_smem(pqv_fused_kernel, grid, dim3(256), smem, st, a, sp);
+                });
+            });
+        }
+    }
     const int warps1 = min(R + 1, 16);  // a spare warp gathers the accept-scan inputs
     cudaError_t e = probed(kProbePqStats, st, [&] {
         return vec ? launch_pdl(pqv_stats_kernel<true>, grid, dim3(warps1 * 32), st, a, sp)
