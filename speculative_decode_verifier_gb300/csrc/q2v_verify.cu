@@ -1107,23 +1107,37 @@ __global__ void __launch_bounds__(256) pqv_fused_kernel(PqArgs a, PqSplit sp) {
         while (!pq_mbar_try(&mbar, 0) && pq_ns() - t0 < kPqWaitNs) {
         }
     }
-    // B. the chunk's (max, sum 2^((x - max) beta)) of every row
+    // B. the chunk's (max, sum 2^((x - max) beta)) of every row, in the statistics kernel's
+    //    order of operations (so the two paths give bit-identical results)
     for (int r = warp; r < R; r += nt >> 5) {
         const float4 *x4 = reinterpret_cast<const float4 *>(pf_rows + (size_t)r * L);
-        float m = -INFINITY;
-        for (int i = lane; i < (n >> 2); i += 32) {
-            const float4 v = x4[i];
-            m = fmaxf(m, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
+        const int n4 = n >> 2;
+        float m = -INFINITY, z = 0.0f;
+        constexpr int U = 12;
+        for (int base = 0; base < n4; base += 32 * U) {
+            float4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = base + u * 32 + lane;
+                v[u] = i < n4 ? x4[i] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+            float bm = m;
+#pragma unroll
+            for (int u = 0; u < U; ++u) bm = fmaxf(bm, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
+            if (bm > -INFINITY) {
+                float acc = (m > -INFINITY) ? z * ex2((m - bm) * beta) : 0.0f;
+#pragma unroll
+                for (int u = 0; u < U; ++u) {
+                    acc += ex2((v[u].x - bm) * beta) + ex2((v[u].y - bm) * beta);
+                    acc += ex2((v[u].z - bm) * beta) + ex2((v[u].w - bm) * beta);
+                }
+                z = acc;
+                m = bm;
+            }
         }
         const float M = warp_max(m);
-        float z = 0.0f;
-        if (M > -INFINITY)
-            for (int i = lane; i < (n >> 2); i += 32) {
-                const float4 v = x4[i];
-                z += ex2((v.x - M) * beta) + ex2((v.y - M) * beta) + ex2((v.z - M) * beta) + ex2((v.w - M) * beta);
-            }
-        z = warp_sum(z);
-        if (lane == 0) reinterpret_cast<float2 *>(sp.stats)[((size_t)s * R + r) * sp.C + c] = make_float2(M, z);
+        const float zz = warp_sum((m > -INFINITY) ? z * ex2((m - M) * beta) : 0.0f);
+        if (lane == 0) reinterpret_cast<float2 *>(sp.stats)[((size_t)s * R + r) * sp.C + c] = make_float2(M, zz);
     }
     // C. every chunk's partials are written
     __syncthreads();
@@ -1185,12 +1199,29 @@ __global__ void __launch_bounds__(256) pqv_fused_kernel(PqArgs a, PqSplit sp) {
     const float *rt = pf_rows + (size_t)j * L;
     const float *rd = D.mode == 0 ? pf_rows + (size_t)(a.k + 1 + j) * L : rt;
     {
+        // in the draw kernel's order of operations: four float4 of each row per lane per round
+        const float4 *t4 = reinterpret_cast<const float4 *>(rt);
+        const float4 *d4 = reinterpret_cast<const float4 *>(rd);
         const int ly0 = warp * Lw, ly1 = min(n, ly0 + Lw);
+        const int i1 = ly1 >> 2;
         float wsum = 0.0f, psum = 0.0f;
-        for (int y = ly0 + lane; y < ly1; y += 32) {
-            const float xt = rt[y], xd = rd[y];
-            wsum += draw_weight(D, beta, xt, xd);
-            if (D.mode == 0) psum += ex2((xt - D.mt) * beta - D.lt);
+        for (int i0 = (ly0 >> 2) + lane; i0 < i1; i0 += 4 * 32) {
+            float4 xt[4], xd[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                const int i = i0 + 32 * u;
+                xt[u] = i < i1 ? t4[i] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+                xd[u] = (i < i1 && D.mode == 0) ? d4[i] : xt[u];
+            }
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                if (i0 + 32 * u >= i1) break;
+                wsum += draw_weight(D, beta, xt[u].x, xd[u].x) + draw_weight(D, beta, xt[u].y, xd[u].y) +
+                        draw_weight(D, beta, xt[u].z, xd[u].z) + draw_weight(D, beta, xt[u].w, xd[u].w);
+                if (D.mode == 0)
+                    psum += ex2((xt[u].x - D.mt) * beta - D.lt) + ex2((xt[u].y - D.mt) * beta - D.lt) +
+                            ex2((xt[u].z - D.mt) * beta - D.lt) + ex2((xt[u].w - D.mt) * beta - D.lt);
+            }
         }
         wsum = warp_sum(wsum);
         psum = warp_sum(psum);
