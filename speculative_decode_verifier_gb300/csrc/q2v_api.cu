@@ -82,7 +82,7 @@ PqCarve pq_carve_from(Carver &c, int S, int k, int V) {
     r.pmass = static_cast<float *>(c.take((size_t)S * C * kSegsPerChunk * sizeof(float)));
     r.tickets = static_cast<unsigned int *>(c.take((size_t)S * sizeof(unsigned int)));
     r.xin = static_cast<float2 *>(c.take((size_t)S * std::max(k, 1) * sizeof(float2)));
-    r.bar = static_cast<unsigned int *>(c.take((size_t)S * 2 * sizeof(unsigned int)));
+    r.bar = static_cast<unsigned int *>(c.take((size_t)S * 2 * kPqBarStride * sizeof(unsigned int)));
     r.bytes = c.off - off0 + Q2_WORKSPACE_HEADER_BYTES;  // as a workspace of its own
     return r;
 }

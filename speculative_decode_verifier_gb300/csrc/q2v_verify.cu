@@ -999,6 +999,7 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
 // then undefined).
 
 constexpr unsigned long long kPqWaitNs = 1000000000ull;  // 1 s
+constexpr int kFusedThreads = 512;   // one warp per row for up to 16 rows
 
 __device__ __forceinline__ uint32_t pq_smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
 __device__ __forceinline__ uint64_t pq_ns() {
@@ -1051,10 +1052,10 @@ __device__ __forceinline__ bool pq_session_barrier(unsigned int *ctr, unsigned i
 __global__ void __launch_bounds__(32) pqv_bar_reset_kernel(unsigned int *bar, int n) {
     pdl_trigger();
     pdl_wait();
-    for (int i = threadIdx.x; i < n; i += 32) bar[i] = 0u;
+    for (int i = threadIdx.x; i < n; i += 32) bar[(size_t)i * kPqBarStride] = 0u;
 }
 
-__global__ void __launch_bounds__(256) pqv_fused_kernel(PqArgs a, PqSplit sp) {
+__global__ void __launch_bounds__(kFusedThreads) pqv_fused_kernel(PqArgs a, PqSplit sp) {
     extern __shared__ __align__(16) float pf_rows[];  // [R][L] chunk rows, then [C * 8] segment masses
     __shared__ __align__(8) uint64_t mbar;
     __shared__ float rowM[kMaxRows];
@@ -1141,20 +1142,37 @@ __global__ void __launch_bounds__(256) pqv_fused_kernel(PqArgs a, PqSplit sp) {
     }
     // C. every chunk's partials are written
     __syncthreads();
-    if (tid == 0) s_ok = pq_session_barrier(sp.bar + 2 * s, (unsigned)sp.C, a.status);
+    if (tid == 0) s_ok = pq_session_barrier(sp.bar + (size_t)(2 * s) * kPqBarStride, (unsigned)sp.C, a.status);
     __syncthreads();
-    // D. row statistics from the partials (16 lanes per row), then the accept scan
-    for (int r0 = 0; r0 < R; r0 += 16) {
+    // D. row statistics from the partials (16 lanes per row; up to 128 chunks: every lane's
+    //    partials in one round of loads, as in the draw kernel), then the accept scan
+    for (int r0 = 0; r0 < R; r0 += nt >> 4) {
         const int r = r0 + (tid >> 4), sub = tid & 15;
         const float2 *st = reinterpret_cast<const float2 *>(sp.stats) + ((size_t)s * R + min(r, R - 1)) * sp.C;
+        float2 v[8];
         float m = -INFINITY;
-        for (int cc = sub; r < R && cc < sp.C; cc += 16) m = fmaxf(m, __ldcg(&st[cc].x));
+        if (sp.C <= 16 * 8) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u) {
+                const int cc = sub + 16 * u;
+                v[u] = (r < R && cc < sp.C) ? __ldcg(&st[cc]) : make_float2(-INFINITY, 0.0f);
+                m = fmaxf(m, v[u].x);
+            }
+        } else {
+            for (int cc = sub; r < R && cc < sp.C; cc += 16) m = fmaxf(m, __ldcg(&st[cc].x));
+        }
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
         float z = 0.0f;
-        for (int cc = sub; r < R && cc < sp.C; cc += 16) {
-            const float2 w = __ldcg(&st[cc]);
-            if (w.x > -INFINITY) z += w.y * ex2((w.x - m) * beta);
+        if (sp.C <= 16 * 8) {
+#pragma unroll
+            for (int u = 0; u < 8; ++u)
+                if (v[u].x > -INFINITY) z += v[u].y * ex2((v[u].x - m) * beta);
+        } else {
+            for (int cc = sub; r < R && cc < sp.C; cc += 16) {
+                const float2 w = __ldcg(&st[cc]);
+                if (w.x > -INFINITY) z += w.y * ex2((w.x - m) * beta);
+            }
         }
 #pragma unroll
         for (int o = 8; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
@@ -1198,7 +1216,7 @@ __global__ void __launch_bounds__(256) pqv_fused_kernel(PqArgs a, PqSplit sp) {
     DrawRows D = draw_rows(a, s, j, rowM, rowL2Z);
     const float *rt = pf_rows + (size_t)j * L;
     const float *rd = D.mode == 0 ? pf_rows + (size_t)(a.k + 1 + j) * L : rt;
-    {
+    if (warp < kSegsPerChunk) {
         // in the draw kernel's order of operations: four float4 of each row per lane per round
         const float4 *t4 = reinterpret_cast<const float4 *>(rt);
         const float4 *d4 = reinterpret_cast<const float4 *>(rd);
@@ -1233,7 +1251,7 @@ __global__ void __launch_bounds__(256) pqv_fused_kernel(PqArgs a, PqSplit sp) {
     }
     // F. every chunk's masses are written
     __syncthreads();
-    if (tid == 0) s_ok = pq_session_barrier(sp.bar + 2 * s + 1, (unsigned)sp.C, a.status);
+    if (tid == 0) s_ok = pq_session_barrier(sp.bar + (size_t)(2 * s + 1) * kPqBarStride, (unsigned)sp.C, a.status);
     __syncthreads();
     // G. level 1 (every CTA): the segment holding the crossing of u_fin * total
     const int nseg = sp.C * kSegsPerChunk;
@@ -1382,7 +1400,8 @@ int fused_blocks_per_sm(size_t smem) {
         if (dv >= 0) optin[dv] = smem;
     }
     int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, pqv_fused_kernel, 256, smem) != cudaSuccess) {
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, pqv_fused_kernel, kFusedThreads, smem) !=
+        cudaSuccess) {
         (void)cudaGetLastError();
         return 0;
     }
@@ -1423,7 +1442,7 @@ cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier,
             // both probes bracket the one kernel (it is the statistics pass and the draw)
             return probed(kProbePqStats, st, [&] {
                 return probed(kProbePqVerify, st, [&] {
-                    return launch_pdl_smem(pqv_fused_kernel, grid, dim3(256), smem, st, a, sp);
+                    return launch_pdl_smem(pqv_fused_kernel, grid, dim3(kFusedThreads), smem, st, a, sp);
                 });
             });
         }
