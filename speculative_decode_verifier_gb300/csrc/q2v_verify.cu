@@ -528,6 +528,91 @@ __global__ void __launch_bounds__(GW == 1 ? 256 : 32 * GW) pqv_small_kernel(PqAr
     }
 }
 
+// Level 1 of a large-V draw: the segment (one of the session's nseg segment masses) holding
+// the crossing of u_fin * total.  The whole block stages the masses in shared memory (`sm`,
+// nseg floats; the p_j masses in the zero-residual fallback), then warp 0 alone decides: lane l
+// sums the contiguous run of cdiv(nseg, 32) entries it owns, a compensated warp scan gives each
+// lane its prefix, the first lane whose run crosses walks it (if rounding puts the target past
+// the end, the last entry with mass is taken).  Returns, in every thread, the entry (-1: no
+// mass at all), the compensated prefix before it, the target and the mode (0 residual, 1 p_j).
+struct SegPick {
+    int ent, mode;
+    float pre_hi, pre_lo, target;
+};
+
+__device__ __forceinline__ SegPick pick_segment(const float *mass, const float *pmass, int nseg, int mode0, float u,
+                                                float *sm, SegPick *shared_out) {
+    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31;
+    const bool w0 = tid < 32;
+    const int q = cdiv(nseg, 32);
+    const int e0 = min(nseg, lane * q), e1 = min(nseg, e0 + q);
+    CSum own, excl, tot;
+    int mode = mode0;
+    for (int pass = 0; pass < 2; ++pass) {  // pass 1 only when the residual has no mass
+        const float *wsrc = pass == 0 ? mass : pmass;
+        // up to 8 loads per thread in flight before any is stored
+        for (int e = tid; e < nseg; e += 8 * nt) {
+            float v[8];
+#pragma unroll
+            for (int k = 0; k < 8; ++k) v[k] = e + k * nt < nseg ? __ldcg(wsrc + e + k * nt) : 0.0f;
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+                if (e + k * nt < nseg) sm[e + k * nt] = v[k];
+        }
+        __syncthreads();
+        if (w0) {
+            own = CSum();
+            for (int e = e0; e < e1; ++e) own.add(sm[e]);
+            excl = warp_excl_scan_c(own, lane, tot);
+            if (lane == 0) shared_out->pre_hi = tot.hi;  // whether the pass found mass, for all
+        }
+        __syncthreads();
+        const float th = shared_out->pre_hi;
+        __syncthreads();
+        if (mode == 1 || th > 0.0f) break;
+        mode = 1;  // zero residual mass: draw from p_j
+    }
+    if (w0) {
+        const float target = u * (tot.hi + tot.lo);
+        const float own_m = own.hi + own.lo;
+        const unsigned cm = __ballot_sync(0xffffffffu, own_m > 0.0f && excl.exceeds(own_m, target));
+        const unsigned pm = __ballot_sync(0xffffffffu, own_m > 0.0f);
+        const int first = cm ? __ffs(cm) - 1 : 32;
+        const int owner = first < 32 ? first : (pm ? 31 - __clz(pm) : -1);
+        if (owner < 0 && lane == 0) {
+            shared_out->ent = -1;
+            shared_out->mode = mode;
+            shared_out->target = target;
+        }
+        if (lane == owner) {
+            // the first entry of this run whose end passes the target (else its last entry with mass)
+            CSum pre = excl, last_pre, found_pre;
+            int found = -1, last_nz = -1;
+            for (int e = e0; e < e1; ++e) {
+                const float me = sm[e];
+                if (me > 0.0f) {
+                    last_nz = e;
+                    last_pre = pre;
+                    if (first < 32 && pre.exceeds(me, target)) {
+                        found = e;
+                        found_pre = pre;
+                        break;
+                    }
+                }
+                pre.add(me);
+            }
+            const CSum pr = found >= 0 ? found_pre : last_pre;
+            shared_out->ent = found >= 0 ? found : last_nz;
+            shared_out->pre_hi = pr.hi;
+            shared_out->pre_lo = pr.lo;
+            shared_out->mode = mode;
+            shared_out->target = target;
+        }
+    }
+    __syncthreads();
+    return *shared_out;
+}
+
 // ===================================================================== large-V tier
 
 // Kernel 1: (max, sum 2^((x-max) beta)) of every row's chunk.  grid (C, S); warp w takes
@@ -843,77 +928,26 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
     __syncthreads();
     if (!s_last) return;
 
-    // 4. last CTA, all threads: the segment holding the crossing of u_fin * total, then the
-    //    token inside it.  Each level is a block-wide compensated scan: every thread sums a
-    //    contiguous run of entries, the scan gives its prefix, the first thread whose run
-    //    crosses walks that run.  If rounding puts the target past the end, the last entry
+    // 4. last CTA: the segment holding the crossing of u_fin * total (pick_segment), then the
+    //    token inside it, by a block-wide compensated scan: every thread sums a contiguous run
+    //    of the segment's tokens, the scan gives its prefix, the first thread whose run
+    //    crosses walks that run.  If rounding puts the target past the end, the last token
     //    with mass is taken.
     __shared__ float s_scan[64];
     __shared__ int s_first, s_lastpos, s_ent;
     __shared__ float s_pre[2];
+    __shared__ SegPick s_pick;
     const int nseg = sp.C * kSegsPerChunk;
     const int nt = blockDim.x;
-    float *sm = pq_dyn;
-    int mode = D.mode;
-    // level 1: segments
-    const int q = cdiv(nseg, nt);
-    const int e0 = min(nseg, tid * q), e1 = min(nseg, e0 + q);
-    CSum own, excl, tot;
-    for (int pass = 0; pass < 2; ++pass) {  // pass 1 only when the residual has no mass
-        const float *wsrc = (pass == 0 ? sp.mass : sp.pmass) + (size_t)s * nseg;
-        // up to 8 loads per thread in flight before any is stored
-        for (int e = tid; e < nseg; e += 8 * nt) {
-            float v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = e + u * nt < nseg ? __ldcg(wsrc + e + u * nt) : 0.0f;
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (e + u * nt < nseg) sm[e + u * nt] = v[u];
-        }
-        __syncthreads();
-        own = CSum();
-        for (int e = e0; e < e1; ++e) own.add(sm[e]);
-        excl = block_excl_scan(own, s_scan, tot);
-        if (mode == 1 || tot.hi > 0.0f) break;
-        mode = 1;  // zero residual mass: draw from p_j
-        __syncthreads();
-    }
-    D.mode = mode;
-    const float target = a.u_fin[s] * (tot.hi + tot.lo);
+    const SegPick pk = pick_segment(sp.mass + (size_t)s * nseg, sp.pmass + (size_t)s * nseg, nseg, D.mode,
+                                    a.u_fin[s], pq_dyn, &s_pick);
+    D.mode = pk.mode;
+    const float target = pk.target;
+    const int owner1 = pk.ent;
     if (tid == 0) {
-        s_first = nt;
-        s_lastpos = -1;
-    }
-    __syncthreads();
-    const float own_m = own.hi + own.lo;
-    if (own_m > 0.0f) {
-        atomicMax(&s_lastpos, tid);
-        if (excl.exceeds(own_m, target)) atomicMin(&s_first, tid);
-    }
-    __syncthreads();
-    const int owner1 = s_first < nt ? s_first : s_lastpos;
-    if (tid == owner1) {
-        // the first entry of this run whose end passes the target (else its last entry with mass)
-        CSum pre = excl, last_pre;
-        int found = -1, last_nz = -1;
-        CSum found_pre;
-        for (int e = e0; e < e1; ++e) {
-            const float me = sm[e];
-            if (me > 0.0f) {
-                last_nz = e;
-                last_pre = pre;
-                if (s_first < nt && pre.exceeds(me, target)) {
-                    found = e;
-                    found_pre = pre;
-                    break;
-                }
-            }
-            pre.add(me);
-        }
-        s_ent = found >= 0 ? found : last_nz;
-        const CSum pr = found >= 0 ? found_pre : last_pre;
-        s_pre[0] = pr.hi;
-        s_pre[1] = pr.lo;
+        s_ent = pk.ent;
+        s_pre[0] = pk.pre_hi;
+        s_pre[1] = pk.pre_lo;
     }
     __syncthreads();
     int y_sel = -1;
@@ -1055,9 +1089,8 @@ __global__ void __launch_bounds__(32) pqv_bar_reset_kernel(unsigned int *bar, in
     for (int i = threadIdx.x; i < n; i += 32) bar[(size_t)i * kPqBarStride] = 0u;
 }
 
-__global__ void __launch_bounds__(kFusedThreads) pqv_fused_kernel(PqArgs a, PqSplit sp) {
+__global__ void __launch_bounds__(kFusedThreads, 2) pqv_fused_kernel(PqArgs a, PqSplit sp) {
     extern __shared__ __align__(16) float pf_rows[];  // [R][L] chunk rows, then [C * 8] segment masses
-    __shared__ __align__(8) uint64_t mbar;
     __shared__ float rowM[kMaxRows];
     __shared__ float rowL2Z[kMaxRows];
     __shared__ int s_j, s_ok;
@@ -1073,24 +1106,7 @@ __global__ void __launch_bounds__(kFusedThreads) pqv_fused_kernel(PqArgs a, PqSp
     const int L = sp.L, c0 = c * L, n = min(L, a.V - c0);  // n % 4 == 0
     const int Lw = L / kSegsPerChunk;
     float *msm = pf_rows + (size_t)R * L;
-    // A. the chunk of every row into shared memory
-    if (tid == 0) {
-        asm volatile("mbarrier.init.shared::cta.b64 [%0], 1;\n" ::"r"(pq_smem_u32(&mbar)) : "memory");
-        asm volatile("fence.mbarrier_init.release.cluster;\n" ::: "memory");
-    }
-    __syncthreads();
-    if (tid == 0) {
-        asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(pq_smem_u32(&mbar)),
-                     "r"((uint32_t)(R * n * 4))
-                     : "memory");
-        for (int r = 0; r < R; ++r)
-            asm volatile(
-                "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-                    pq_smem_u32(pf_rows + (size_t)r * L)),
-                "l"(row_ptr(a, s, r) + c0), "r"((uint32_t)(n * 4)), "r"(pq_smem_u32(&mbar))
-                : "memory");
-    }
-    // the accept scan's inputs, in flight while the rows stream in (lane i: draft i)
+    // the accept scan's inputs, requested first (lane i: draft i)
     int xv = 0;
     float tx = 0.0f, dx = 0.0f, uv = 0.0f;
     if (warp == 0 && lane < a.k) {
@@ -1101,17 +1117,12 @@ __global__ void __launch_bounds__(kFusedThreads) pqv_fused_kernel(PqArgs a, PqSp
             dx = row_ptr(a, s, a.k + 1 + lane)[xv];
         }
     }
-    if (!pq_mbar_wait(&mbar, a.status)) {
-        // the copies have not landed in time: let them land before this CTA's shared memory is
-        // used or released (bounded again), then carry on with an error recorded
-        const uint64_t t0 = pq_ns();
-        while (!pq_mbar_try(&mbar, 0) && pq_ns() - t0 < kPqWaitNs) {
-        }
-    }
-    // B. the chunk's (max, sum 2^((x - max) beta)) of every row, in the statistics kernel's
-    //    order of operations (so the two paths give bit-identical results)
+    // A + B. warp r streams row r's chunk (16-byte loads, every load of a lane in one round at
+    //    these sizes), keeps it in shared memory and reduces it to (max, sum 2^((x - max) beta))
+    //    in the statistics kernel's order of operations (so the two paths agree bit for bit)
     for (int r = warp; r < R; r += nt >> 5) {
-        const float4 *x4 = reinterpret_cast<const float4 *>(pf_rows + (size_t)r * L);
+        const float4 *x4 = reinterpret_cast<const float4 *>(row_ptr(a, s, r) + c0);
+        float4 *s4 = reinterpret_cast<float4 *>(pf_rows + (size_t)r * L);
         const int n4 = n >> 2;
         float m = -INFINITY, z = 0.0f;
         constexpr int U = 12;
@@ -1120,7 +1131,12 @@ __global__ void __launch_bounds__(kFusedThreads) pqv_fused_kernel(PqArgs a, PqSp
 #pragma unroll
             for (int u = 0; u < U; ++u) {
                 const int i = base + u * 32 + lane;
-                v[u] = i < n4 ? x4[i] : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+                v[u] = i < n4 ? __ldg(x4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int i = base + u * 32 + lane;
+                if (i < n4) s4[i] = v[u];
             }
             float bm = m;
 #pragma unroll
@@ -1254,84 +1270,32 @@ __global__ void __launch_bounds__(kFusedThreads) pqv_fused_kernel(PqArgs a, PqSp
     if (tid == 0) s_ok = pq_session_barrier(sp.bar + (size_t)(2 * s + 1) * kPqBarStride, (unsigned)sp.C, a.status);
     __syncthreads();
     // G. level 1 (every CTA): the segment holding the crossing of u_fin * total
+    __shared__ SegPick s_pick;
     const int nseg = sp.C * kSegsPerChunk;
-    const int q = cdiv(nseg, nt);
-    const int e0 = min(nseg, tid * q), e1 = min(nseg, e0 + q);
-    CSum own, excl, tot;
-    int mode = D.mode;
-    for (int pass = 0; pass < 2; ++pass) {  // pass 1 only when the residual has no mass
-        const float *wsrc = (pass == 0 ? sp.mass : sp.pmass) + (size_t)s * nseg;
-        for (int e = tid; e < nseg; e += 8 * nt) {
-            float v[8];
-#pragma unroll
-            for (int u = 0; u < 8; ++u) v[u] = e + u * nt < nseg ? __ldcg(wsrc + e + u * nt) : 0.0f;
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (e + u * nt < nseg) msm[e + u * nt] = v[u];
-        }
-        __syncthreads();
-        own = CSum();
-        for (int e = e0; e < e1; ++e) own.add(msm[e]);
-        excl = block_excl_scan(own, s_scan, tot);
-        if (mode == 1 || tot.hi > 0.0f) break;
-        mode = 1;  // zero residual mass: draw from p_j
-        __syncthreads();
-    }
-    D.mode = mode;
-    const float target = a.u_fin[s] * (tot.hi + tot.lo);
-    if (tid == 0) {
-        s_first = nt;
-        s_lastpos = -1;
-    }
-    __syncthreads();
-    const float own_m = own.hi + own.lo;
-    if (own_m > 0.0f) {
-        atomicMax(&s_lastpos, tid);
-        if (excl.exceeds(own_m, target)) atomicMin(&s_first, tid);
-    }
-    __syncthreads();
-    const int owner1 = s_first < nt ? s_first : s_lastpos;
-    if (owner1 < 0) {
+    const SegPick pk = pick_segment(sp.mass + (size_t)s * nseg, sp.pmass + (size_t)s * nseg, nseg, D.mode,
+                                    a.u_fin[s], msm, &s_pick);
+    D.mode = pk.mode;
+    const float target = pk.target;
+    if (pk.ent < 0) {
         if (c == 0 && tid == 0) write_tokens(a, s, j, -1);
         return;
     }
-    if (tid == owner1) {
-        CSum pre = excl, last_pre;
-        int found = -1, last_nz = -1;
-        CSum found_pre;
-        for (int e = e0; e < e1; ++e) {
-            const float me = msm[e];
-            if (me > 0.0f) {
-                last_nz = e;
-                last_pre = pre;
-                if (s_first < nt && pre.exceeds(me, target)) {
-                    found = e;
-                    found_pre = pre;
-                    break;
-                }
-            }
-            pre.add(me);
-        }
-        s_ent = found >= 0 ? found : last_nz;
-        const CSum pr = found >= 0 ? found_pre : last_pre;
-        s_pre[0] = pr.hi;
-        s_pre[1] = pr.lo;
-    }
-    __syncthreads();
-    const int ent = s_ent;
+    const int ent = pk.ent;
     if (ent / kSegsPerChunk != c) return;  // another CTA of the session owns the segment
     // level 2 (the owning CTA): the token inside the segment, from shared memory
     const int sw = ent - c * kSegsPerChunk;
     const int ly0s = sw * Lw, ly1s = min(n, ly0s + Lw);
-    const int r = cdiv(max(ly1s - ly0s, 0), nt);
-    const int y0 = min(ly1s, ly0s + tid * r), y1 = min(ly1s, y0 + r);
+    // the token runs of the two-kernel path's 256-thread draw (the other threads take none), so
+    // both paths sum in the same order
+    const int nt2 = min(nt, 256);
+    const int r = cdiv(max(ly1s - ly0s, 0), nt2);
+    const int y0 = tid < nt2 ? min(ly1s, ly0s + tid * r) : ly1s, y1 = min(ly1s, y0 + r);
     const float *rd2 = D.mode == 0 ? rd : rt;
     CSum seg_pre;
-    seg_pre.hi = s_pre[0];
-    seg_pre.lo = s_pre[1];
+    seg_pre.hi = pk.pre_hi;
+    seg_pre.lo = pk.pre_lo;
     CSum own2, tot2;
     for (int y = y0; y < y1; ++y) own2.add(draw_weight(D, beta, rt[y], rd2[y]));
-    __syncthreads();  // s_scan is reused
     const CSum excl2 = csum_plus(seg_pre, block_excl_scan(own2, s_scan, tot2));
     if (tid == 0) {
         s_first = nt;
