@@ -1106,10 +1106,12 @@ __global__ void __launch_bounds__(kFusedThreads, 2) pqv_fused_kernel(PqArgs a, P
     const int L = sp.L, c0 = c * L, n = min(L, a.V - c0);  // n % 4 == 0
     const int Lw = L / kSegsPerChunk;
     float *msm = pf_rows + (size_t)R * L;
-    // the accept scan's inputs, requested first (lane i: draft i)
+    // the accept scan's inputs (lane i: draft i), fetched by the last warp, which streams no row
+    // when there are fewer rows than warps (else by warp 0 after its rows)
+    const int gw = (nt >> 5) > R ? (nt >> 5) - 1 : 0;
     int xv = 0;
     float tx = 0.0f, dx = 0.0f, uv = 0.0f;
-    if (warp == 0 && lane < a.k) {
+    if (warp == gw && gw > 0 && lane < a.k) {
         xv = a.drafts[(size_t)s * a.k + lane];
         uv = a.u_acc[(size_t)s * a.k + lane];
         if (xv >= 0 && xv < a.V) {
@@ -1156,6 +1158,14 @@ __global__ void __launch_bounds__(kFusedThreads, 2) pqv_fused_kernel(PqArgs a, P
         const float zz = warp_sum((m > -INFINITY) ? z * ex2((m - M) * beta) : 0.0f);
         if (lane == 0) reinterpret_cast<float2 *>(sp.stats)[((size_t)s * R + r) * sp.C + c] = make_float2(M, zz);
     }
+    if (gw == 0 && warp == 0 && lane < a.k) {
+        xv = a.drafts[(size_t)s * a.k + lane];
+        uv = a.u_acc[(size_t)s * a.k + lane];
+        if (xv >= 0 && xv < a.V) {
+            tx = row_ptr(a, s, lane)[xv];
+            dx = row_ptr(a, s, a.k + 1 + lane)[xv];
+        }
+    }
     // C. every chunk's partials are written
     __syncthreads();
     if (tid == 0) s_ok = pq_session_barrier(sp.bar + (size_t)(2 * s) * kPqBarStride, (unsigned)sp.C, a.status);
@@ -1198,7 +1208,7 @@ __global__ void __launch_bounds__(kFusedThreads, 2) pqv_fused_kernel(PqArgs a, P
         }
     }
     __syncthreads();
-    if (warp == 0) {
+    if (warp == gw) {
         bool bad = false, rej = false;
         if (lane < a.k) {
             if (xv < 0 || xv >= a.V) {
