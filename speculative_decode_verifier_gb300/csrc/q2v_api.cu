@@ -69,7 +69,6 @@ struct PqCarve {
     float *mass, *pmass;
     unsigned int *tickets;
     float2 *xin;
-    unsigned int *bar;
     size_t bytes;
 };
 
@@ -82,7 +81,6 @@ PqCarve pq_carve_from(Carver &c, int S, int k, int V) {
     r.pmass = static_cast<float *>(c.take((size_t)S * C * kSegsPerChunk * sizeof(float)));
     r.tickets = static_cast<unsigned int *>(c.take((size_t)S * sizeof(unsigned int)));
     r.xin = static_cast<float2 *>(c.take((size_t)S * std::max(k, 1) * sizeof(float2)));
-    r.bar = static_cast<unsigned int *>(c.take((size_t)S * 2 * kPqBarStride * sizeof(unsigned int)));
     r.bytes = c.off - off0 + Q2_WORKSPACE_HEADER_BYTES;  // as a workspace of its own
     return r;
 }
@@ -462,7 +460,6 @@ void pq_setup(PqArgs &a, PqSplit &sp, Carver &c, const float *target_logits, con
         sp.mass = pc.mass;
         sp.pmass = pc.pmass;
         sp.tickets = pc.tickets;
-        sp.bar = pc.bar;
     }
 }
 

@@ -52,8 +52,6 @@ struct PqArgs {
     unsigned int *status;
 };
 
-constexpr int kPqBarStride = 32;  // words between session-barrier counters (one 128-byte line each)
-
 struct PqSplit {
     int C;               // chunks per session
     int L;               // chunk length (multiple of kChunkAlign)
@@ -67,8 +65,6 @@ struct PqSplit {
     // streams the draft rows and the combine reads the target rows from here.
     const float *tstats;
     int Ct;
-    unsigned int *bar;   // [S][2] arrival counters of the single-kernel path's two session barriers,
-                         // kPqBarStride words (128 bytes) apart
 };
 
 cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier, int num_sms, cudaStream_t st);

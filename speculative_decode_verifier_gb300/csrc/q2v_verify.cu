@@ -1012,332 +1012,6 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
     if (tid == 0) write_tokens(a, s, j, y_sel);
 }
 
-// ===================================================================== large-V tier, one kernel
-//
-// When every session samples with the one temperature (pq_verify), V % 4 == 0 and the grid of
-// C x S chunks fits on the GPU at once with each CTA holding its chunk of all 2k+1 rows in
-// shared memory, the two kernels above become one:
-//   A. the CTA copies its chunk of every row into shared memory with one bulk copy per row
-//      (an mbarrier counts the bytes), while lanes of warp 0 fetch the accept scan's inputs;
-//   B. per-row (max, sum) partials of the chunk, from shared memory, to the workspace;
-//   C. a session barrier (an arrival counter per session, a bounded spin by one thread);
-//   D. the combine of the partials and the accept scan, as in kernel 2;
-//   E. the draw masses of the chunk's 8 segments, from shared memory, to the workspace;
-//   F. a second session barrier;
-//   G. every CTA scans the session's segment masses (the same compensated block scan as the
-//      last-arriver search) and the CTA that owns the chosen segment finds the token in its
-//      shared-memory copy of the rows and writes the session's result.
-// The grid is sized so that all its CTAs are resident together (the host checks occupancy);
-// the barriers' counters are zeroed by a one-CTA kernel launched just before.  Every wait is
-// bounded: after kPqWaitNs the thread records Q2_ERR_TIMEOUT and carries on (the results are
-// then undefined).
-
-constexpr unsigned long long kPqWaitNs = 1000000000ull;  // 1 s
-constexpr int kFusedThreads = 512;   // one warp per row for up to 16 rows
-
-__device__ __forceinline__ uint32_t pq_smem_u32(const void *p) { return (uint32_t)__cvta_generic_to_shared(p); }
-__device__ __forceinline__ uint64_t pq_ns() {
-    uint64_t t;
-    asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
-    return t;
-}
-__device__ __forceinline__ bool pq_mbar_try(uint64_t *bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
-        : "=r"(ok)
-        : "r"(pq_smem_u32(bar)), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-// A spin on phase 0 of `bar`, bounded; false (and Q2_ERR_TIMEOUT recorded by thread 0) if the
-// time ran out.
-__device__ __forceinline__ bool pq_mbar_wait(uint64_t *bar, unsigned int *status) {
-    if (pq_mbar_try(bar, 0)) return true;
-    const uint64_t t0 = pq_ns();
-    while (!pq_mbar_try(bar, 0)) {
-        if (pq_ns() - t0 > kPqWaitNs) {
-            if (threadIdx.x == 0) set_status(status, Q2_ERR_TIMEOUT);
-            return false;
-        }
-    }
-    return true;
-}
-
-// One thread: arrive at a session barrier of `expected` CTAs and spin (bounded) until all
-// have arrived.  The fence before the arrival releases this CTA's writes; the acquire load
-// that sees the full count makes the other CTAs' writes visible.
-__device__ __forceinline__ bool pq_session_barrier(unsigned int *ctr, unsigned int expected, unsigned int *status) {
-    __threadfence();
-    atomicAdd(ctr, 1u);
-    const uint64_t t0 = pq_ns();
-    for (;;) {
-        unsigned int v;
-        asm volatile("ld.acquire.gpu.global.u32 %0, [%1];\n" : "=r"(v) : "l"(ctr) : "memory");
-        if (v >= expected) return true;
-        if (pq_ns() - t0 > kPqWaitNs) {
-            set_status(status, Q2_ERR_TIMEOUT);
-            return false;
-        }
-    }
-}
-
-__global__ void __launch_bounds__(32) pqv_bar_reset_kernel(unsigned int *bar, int n) {
-    pdl_trigger();
-    pdl_wait();
-    for (int i = threadIdx.x; i < n; i += 32) bar[(size_t)i * kPqBarStride] = 0u;
-}
-
-__global__ void __launch_bounds__(kFusedThreads, 2) pqv_fused_kernel(PqArgs a, PqSplit sp) {
-    extern __shared__ __align__(16) float pf_rows[];  // [R][L] chunk rows, then [C * 8] segment masses
-    __shared__ float rowM[kMaxRows];
-    __shared__ float rowL2Z[kMaxRows];
-    __shared__ int s_j, s_ok;
-    __shared__ float s_scan[64];
-    __shared__ int s_first, s_lastpos, s_ent;
-    __shared__ float s_pre[2];
-    pdl_wait();
-    pdl_trigger();
-    const int c = blockIdx.x, s = blockIdx.y;
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nt = blockDim.x;
-    const int R = 2 * a.k + 1;
-    const float beta = a.beta;
-    const int L = sp.L, c0 = c * L, n = min(L, a.V - c0);  // n % 4 == 0
-    const int Lw = L / kSegsPerChunk;
-    float *msm = pf_rows + (size_t)R * L;
-    // the accept scan's inputs (lane i: draft i), fetched by the last warp, which streams no row
-    // when there are fewer rows than warps (else by warp 0 after its rows)
-    const int gw = (nt >> 5) > R ? (nt >> 5) - 1 : 0;
-    int xv = 0;
-    float tx = 0.0f, dx = 0.0f, uv = 0.0f;
-    if (warp == gw && gw > 0 && lane < a.k) {
-        xv = a.drafts[(size_t)s * a.k + lane];
-        uv = a.u_acc[(size_t)s * a.k + lane];
-        if (xv >= 0 && xv < a.V) {
-            tx = row_ptr(a, s, lane)[xv];
-            dx = row_ptr(a, s, a.k + 1 + lane)[xv];
-        }
-    }
-    // A + B. warp r streams row r's chunk (16-byte loads, every load of a lane in one round at
-    //    these sizes), keeps it in shared memory and reduces it to (max, sum 2^((x - max) beta))
-    //    in the statistics kernel's order of operations (so the two paths agree bit for bit)
-    for (int r = warp; r < R; r += nt >> 5) {
-        const float4 *x4 = reinterpret_cast<const float4 *>(row_ptr(a, s, r) + c0);
-        float4 *s4 = reinterpret_cast<float4 *>(pf_rows + (size_t)r * L);
-        const int n4 = n >> 2;
-        float m = -INFINITY, z = 0.0f;
-        constexpr int U = 12;
-        for (int base = 0; base < n4; base += 32 * U) {
-            float4 v[U];
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int i = base + u * 32 + lane;
-                v[u] = i < n4 ? __ldg(x4 + i) : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
-            }
-#pragma unroll
-            for (int u = 0; u < U; ++u) {
-                const int i = base + u * 32 + lane;
-                if (i < n4) s4[i] = v[u];
-            }
-            float bm = m;
-#pragma unroll
-            for (int u = 0; u < U; ++u) bm = fmaxf(bm, fmaxf(fmaxf(v[u].x, v[u].y), fmaxf(v[u].z, v[u].w)));
-            if (bm > -INFINITY) {
-                float acc = (m > -INFINITY) ? z * ex2((m - bm) * beta) : 0.0f;
-#pragma unroll
-                for (int u = 0; u < U; ++u) {
-                    acc += ex2((v[u].x - bm) * beta) + ex2((v[u].y - bm) * beta);
-                    acc += ex2((v[u].z - bm) * beta) + ex2((v[u].w - bm) * beta);
-                }
-                z = acc;
-                m = bm;
-            }
-        }
-        const float M = warp_max(m);
-        const float zz = warp_sum((m > -INFINITY) ? z * ex2((m - M) * beta) : 0.0f);
-        if (lane == 0) reinterpret_cast<float2 *>(sp.stats)[((size_t)s * R + r) * sp.C + c] = make_float2(M, zz);
-    }
-    if (gw == 0 && warp == 0 && lane < a.k) {
-        xv = a.drafts[(size_t)s * a.k + lane];
-        uv = a.u_acc[(size_t)s * a.k + lane];
-        if (xv >= 0 && xv < a.V) {
-            tx = row_ptr(a, s, lane)[xv];
-            dx = row_ptr(a, s, a.k + 1 + lane)[xv];
-        }
-    }
-    // C. every chunk's partials are written
-    __syncthreads();
-    if (tid == 0) s_ok = pq_session_barrier(sp.bar + (size_t)(2 * s) * kPqBarStride, (unsigned)sp.C, a.status);
-    __syncthreads();
-    // D. row statistics from the partials (16 lanes per row; up to 128 chunks: every lane's
-    //    partials in one round of loads, as in the draw kernel), then the accept scan
-    for (int r0 = 0; r0 < R; r0 += nt >> 4) {
-        const int r = r0 + (tid >> 4), sub = tid & 15;
-        const float2 *st = reinterpret_cast<const float2 *>(sp.stats) + ((size_t)s * R + min(r, R - 1)) * sp.C;
-        float2 v[8];
-        float m = -INFINITY;
-        if (sp.C <= 16 * 8) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u) {
-                const int cc = sub + 16 * u;
-                v[u] = (r < R && cc < sp.C) ? __ldcg(&st[cc]) : make_float2(-INFINITY, 0.0f);
-                m = fmaxf(m, v[u].x);
-            }
-        } else {
-            for (int cc = sub; r < R && cc < sp.C; cc += 16) m = fmaxf(m, __ldcg(&st[cc].x));
-        }
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        float z = 0.0f;
-        if (sp.C <= 16 * 8) {
-#pragma unroll
-            for (int u = 0; u < 8; ++u)
-                if (v[u].x > -INFINITY) z += v[u].y * ex2((v[u].x - m) * beta);
-        } else {
-            for (int cc = sub; r < R && cc < sp.C; cc += 16) {
-                const float2 w = __ldcg(&st[cc]);
-                if (w.x > -INFINITY) z += w.y * ex2((w.x - m) * beta);
-            }
-        }
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) z += __shfl_xor_sync(0xffffffffu, z, o);
-        if (sub == 0 && r < R) {
-            rowM[r] = m;
-            rowL2Z[r] = log2f(z);
-        }
-    }
-    __syncthreads();
-    if (warp == gw) {
-        bool bad = false, rej = false;
-        if (lane < a.k) {
-            if (xv < 0 || xv >= a.V) {
-                bad = true;
-            } else if (dx != -INFINITY) {  // q(x) == 0 accepts
-                const float lp = (tx - rowM[lane]) * beta - rowL2Z[lane];
-                const float lq = (dx - rowM[a.k + 1 + lane]) * beta - rowL2Z[a.k + 1 + lane];
-                rej = !(uv < ex2(lp - lq));
-            }
-        }
-        const unsigned badm = __ballot_sync(0xffffffffu, bad), rejm = __ballot_sync(0xffffffffu, rej);
-        if (lane == 0) s_j = badm ? -1 : (rejm ? __ffs(rejm) - 1 : a.k);
-    }
-    __syncthreads();
-    const int j = s_j;
-    if (a.probs)
-        for (int r = 0; r < R; ++r) {
-            const float *x = pf_rows + (size_t)r * L;
-            float *o = a.probs + ((size_t)s * R + r) * a.V + c0;
-            const float M = rowM[r], L2 = rowL2Z[r];
-            for (int y = tid; y < n; y += nt) o[y] = ex2((x[y] - M) * beta - L2);
-        }
-    if (j < 0) {
-        if (c == 0 && tid == 0) {
-            set_status(a.status, Q2_ERR_BAD_TOKEN);
-            write_tokens(a, s, -1, -1);
-        }
-        return;  // every CTA of the session takes this exit: no barrier is left waiting
-    }
-    // E. the draw masses of this chunk's segments (warp w: segment w), from shared memory
-    DrawRows D = draw_rows(a, s, j, rowM, rowL2Z);
-    const float *rt = pf_rows + (size_t)j * L;
-    const float *rd = D.mode == 0 ? pf_rows + (size_t)(a.k + 1 + j) * L : rt;
-    if (warp < kSegsPerChunk) {
-        // in the draw kernel's order of operations: four float4 of each row per lane per round
-        const float4 *t4 = reinterpret_cast<const float4 *>(rt);
-        const float4 *d4 = reinterpret_cast<const float4 *>(rd);
-        const int ly0 = warp * Lw, ly1 = min(n, ly0 + Lw);
-        const int i1 = ly1 >> 2;
-        float wsum = 0.0f, psum = 0.0f;
-        for (int i0 = (ly0 >> 2) + lane; i0 < i1; i0 += 4 * 32) {
-            float4 xt[4], xd[4];
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                const int i = i0 + 32 * u;
-                xt[u] = i < i1 ? t4[i] : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-                xd[u] = (i < i1 && D.mode == 0) ? d4[i] : xt[u];
-            }
-#pragma unroll
-            for (int u = 0; u < 4; ++u) {
-                if (i0 + 32 * u >= i1) break;
-                wsum += draw_weight(D, beta, xt[u].x, xd[u].x) + draw_weight(D, beta, xt[u].y, xd[u].y) +
-                        draw_weight(D, beta, xt[u].z, xd[u].z) + draw_weight(D, beta, xt[u].w, xd[u].w);
-                if (D.mode == 0)
-                    psum += ex2((xt[u].x - D.mt) * beta - D.lt) + ex2((xt[u].y - D.mt) * beta - D.lt) +
-                            ex2((xt[u].z - D.mt) * beta - D.lt) + ex2((xt[u].w - D.mt) * beta - D.lt);
-            }
-        }
-        wsum = warp_sum(wsum);
-        psum = warp_sum(psum);
-        if (lane == 0) {
-            const size_t e = ((size_t)s * sp.C + c) * kSegsPerChunk + warp;
-            sp.mass[e] = wsum;
-            sp.pmass[e] = psum;
-        }
-    }
-    // F. every chunk's masses are written
-    __syncthreads();
-    if (tid == 0) s_ok = pq_session_barrier(sp.bar + (size_t)(2 * s + 1) * kPqBarStride, (unsigned)sp.C, a.status);
-    __syncthreads();
-    // G. level 1 (every CTA): the segment holding the crossing of u_fin * total
-    __shared__ SegPick s_pick;
-    const int nseg = sp.C * kSegsPerChunk;
-    const SegPick pk = pick_segment(sp.mass + (size_t)s * nseg, sp.pmass + (size_t)s * nseg, nseg, D.mode,
-                                    a.u_fin[s], msm, &s_pick);
-    D.mode = pk.mode;
-    const float target = pk.target;
-    if (pk.ent < 0) {
-        if (c == 0 && tid == 0) write_tokens(a, s, j, -1);
-        return;
-    }
-    const int ent = pk.ent;
-    if (ent / kSegsPerChunk != c) return;  // another CTA of the session owns the segment
-    // level 2 (the owning CTA): the token inside the segment, from shared memory
-    const int sw = ent - c * kSegsPerChunk;
-    const int ly0s = sw * Lw, ly1s = min(n, ly0s + Lw);
-    // the token runs of the two-kernel path's 256-thread draw (the other threads take none), so
-    // both paths sum in the same order
-    const int nt2 = min(nt, 256);
-    const int r = cdiv(max(ly1s - ly0s, 0), nt2);
-    const int y0 = tid < nt2 ? min(ly1s, ly0s + tid * r) : ly1s, y1 = min(ly1s, y0 + r);
-    const float *rd2 = D.mode == 0 ? rd : rt;
-    CSum seg_pre;
-    seg_pre.hi = pk.pre_hi;
-    seg_pre.lo = pk.pre_lo;
-    CSum own2, tot2;
-    for (int y = y0; y < y1; ++y) own2.add(draw_weight(D, beta, rt[y], rd2[y]));
-    const CSum excl2 = csum_plus(seg_pre, block_excl_scan(own2, s_scan, tot2));
-    if (tid == 0) {
-        s_first = nt;
-        s_lastpos = -1;
-    }
-    __syncthreads();
-    const float own2_m = own2.hi + own2.lo;
-    if (own2_m > 0.0f) {
-        atomicMax(&s_lastpos, tid);
-        if (excl2.exceeds(own2_m, target)) atomicMin(&s_first, tid);
-    }
-    __syncthreads();
-    const int owner2 = s_first < nt ? s_first : s_lastpos;
-    if (tid == owner2) {
-        CSum pre = excl2;
-        int found = -1, last_nz = -1;
-        for (int y = y0; y < y1; ++y) {
-            const float w = draw_weight(D, beta, rt[y], rd2[y]);
-            if (w > 0.0f) {
-                last_nz = y;
-                if (s_first < nt && pre.exceeds(w, target)) {
-                    found = y;
-                    break;
-                }
-            }
-            pre.add(w);
-        }
-        write_tokens(a, s, j, c0 + (found >= 0 ? found : last_nz));
-    }
-    if (owner2 < 0 && tid == 0) write_tokens(a, s, j, -1);
-}
-
 namespace {
 // launch_pdl with dynamic shared memory
 template <typename... KArgs, typename... Args>
@@ -1356,35 +1030,6 @@ cudaError_t launch_pdl_smem(void (*kernel)(KArgs...), dim3 grid, dim3 block, siz
     return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 }  // namespace
-
-// Resident CTAs per SM of pqv_fused_kernel with `smem` bytes of dynamic shared memory (0 if it
-// cannot run), with the shared-memory opt-in it needs; cached per device for the last size.
-int fused_blocks_per_sm(size_t smem) {
-    static size_t cached_smem[kCacheDevices];
-    static int cached_blocks[kCacheDevices];
-    static size_t optin[kCacheDevices];
-    const int dv = cache_device();
-    if (dv >= 0 && cached_smem[dv] == smem && cached_blocks[dv] > 0) return cached_blocks[dv];
-    if (dv < 0 || optin[dv] < smem) {
-        if (cudaFuncSetAttribute(pqv_fused_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-            cudaSuccess) {
-            (void)cudaGetLastError();  // an unsupported size is not an error of the call: the split path runs
-            return 0;
-        }
-        if (dv >= 0) optin[dv] = smem;
-    }
-    int blocks = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, pqv_fused_kernel, kFusedThreads, smem) !=
-        cudaSuccess) {
-        (void)cudaGetLastError();
-        return 0;
-    }
-    if (dv >= 0) {
-        cached_smem[dv] = smem;
-        cached_blocks[dv] = blocks;
-    }
-    return blocks;
-}
 
 cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier, int num_sms, cudaStream_t st) {
     if (warp_tier) {
@@ -1405,22 +1050,6 @@ cudaError_t launch_pq_verify(const PqArgs &a, const PqSplit &sp, bool warp_tier,
     const bool vec = (a.V % 4) == 0 && (sp.L % 4) == 0;
     const int R = 2 * a.k + 1;
     const dim3 grid(sp.C, a.S);
-    // the one-kernel path when it applies (one temperature, no partials from elsewhere, rows of
-    // 16-byte multiples, and the whole grid resident at once with its rows in shared memory)
-    if (!a.temps && !sp.tstats && vec && sp.bar) {
-        const size_t smem = ((size_t)R * sp.L + (size_t)sp.C * kSegsPerChunk) * sizeof(float);
-        const int blocks = fused_blocks_per_sm(smem);
-        if (blocks > 0 && (long long)blocks * num_sms >= (long long)sp.C * a.S) {
-            cudaError_t e = launch_pdl(pqv_bar_reset_kernel, dim3(1), dim3(32), st, sp.bar, 2 * a.S);
-            if (e != cudaSuccess) return e;
-            // both probes bracket the one kernel (it is the statistics pass and the draw)
-            return probed(kProbePqStats, st, [&] {
-                return probed(kProbePqVerify, st, [&] {
-                    return launch_pdl_smem(pqv_fused_kernel, grid, dim3(kFusedThreads), smem, st, a, sp);
-                });
-            });
-        }
-    }
     const int warps1 = min(R + 1, 16);  // a spare warp gathers the accept-scan inputs
     cudaError_t e = probed(kProbePqStats, st, [&] {
         return vec ? launch_pdl(pqv_stats_kernel<true>, grid, dim3(warps1 * 32), st, a, sp)
