@@ -367,12 +367,6 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
                 UnitInfo cui;
                 if (cu < seg1) cui = um(cu);
                 int ctile = cui.t0;
-                // Whole units (no K split) are 16 contiguous weight rows: each is also requested
-                // into L2 in one bulk prefetch, the warp's first unit now and each next unit
-                // halfway through the current one, so the ring's copies find their lines in L2.
-                const bool whole = um.tps >= L.ntk;
-                const uint32_t unit_bytes = (uint32_t)(kRowsPerCta * um.row_bytes);
-                if (whole && lane == 0 && cu < seg1) prefetch_l2_bulk(cui.W0, unit_bytes);
                 float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
                 for (int it = 0; cu < seg1; ++it) {
                     produce((it + kRingStages - 1) % kRingStages);
@@ -381,8 +375,6 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
                     TileRegs cur;
                     read_tile_smem(cur, ring + (it % kRingStages) * kTileWords, lane);
                     compute_tile_smem(cur, sm_act, SA, mc, ctile, lane, acc, scale_max);
-                    if (whole && lane == 0 && ctile == ((cui.t0 + cui.t1) >> 1) && cu + nwarps < seg1)
-                        prefetch_l2_bulk(um(cu + nwarps).W0, unit_bytes);
                     if (++ctile >= cui.t1) {
                         store_unit(cui, acc);
                         cu += nwarps;
