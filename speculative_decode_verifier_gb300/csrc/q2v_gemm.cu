@@ -162,7 +162,12 @@ __global__ void __launch_bounds__(kGemmWarps * 32) q2_gemm_fused_kernel(const ui
     for (int j = threadIdx.x; j < kRowsPerCta * M; j += blockDim.x) {
         const int r = j % kRowsPerCta, m = j / kRowsPerCta;
         float s = 0.0f;
-        for (int w = 0; w < nwarps; ++w) s += ldexpf(red[w * kRowsPerCta * 8 + r * 8 + m], s_exp[w][m]);
+        for (int w = 0; w < nwarps; ++w) {
+            const int e = s_exp[w][m];
+            const float x = red[w * kRowsPerCta * 8 + r * 8 + m];
+            // x * 2^e: one exact multiply when 2^e is a normal fp32 number
+            s += (e >= -126 && e <= 127) ? x * exp2i(e) : ldexpf(x, e);
+        }
         if (r < rows_valid) Y[(size_t)m * ldy + n0 + r] = s;
     }
     if (scale_mag_out_of_range(scale_max)) set_status(status, Q2_ERR_RANGE);
