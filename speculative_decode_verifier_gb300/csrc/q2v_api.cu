@@ -228,10 +228,6 @@ q2_status q2_tiny_gemm(const void *W, int N, int K, const uint16_t *A, int M, in
             return launch_gemm_umma(W, N, K, M, img, Y, ldy, status_word(ws), sms, s, UmFuse{});
         }));
     }
-    if (M <= kFusedMaxM)  // one kernel: the activation prep happens inside the GEMM
-        return cuda_status(probed(kProbeGemm, s, [&] {
-            return launch_gemm_fused(W, N, K, A, lda, M, Y, ldy, status_word(ws), s);
-        }));
     const PrepLayout L(K);
     const PrepPtrs P = PrepPtrs::carve(c.take(L.bytes(M)), L, M);
     const cudaError_t e = launch_prep_bf16(A, lda, nullptr, M, K, P, L, s);
@@ -357,11 +353,6 @@ q2_status q2_lm_head_verify(const void *W, int V, int K, const uint16_t *A, int 
         }
         e = probed(kProbeGemm, s, [&] {
             return launch_gemm_umma(W, V, K, (int)M, img, target_logits, V, status, sms, s, fz);
-        });
-    } else if (M <= kFusedMaxM) {
-        c.take(PrepLayout(K).bytes((int)M));  // the same carve as the unfused path
-        e = probed(kProbeGemm, s, [&] {
-            return launch_gemm_fused(W, V, K, A, lda, (int)M, target_logits, V, status, s);
         });
     } else {
         const PrepLayout L(K);

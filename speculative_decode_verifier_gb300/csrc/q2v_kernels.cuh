@@ -22,11 +22,6 @@ cudaError_t launch_prep_bf16(const uint16_t *src, int ld, const int *rows, int R
                              const PrepLayout &L, cudaStream_t s);
 cudaError_t launch_gemm_small(const void *W, int N, int K, const PrepPtrs &P, const PrepLayout &L, int M,
                               float *Y, int ldy, unsigned int *status, cudaStream_t s);
-// M <= kFusedMaxM: the same GEMM with the activation prep fused into it (no prep kernel, no
-// workspace beyond the status word).
-constexpr int kFusedMaxM = 8;
-cudaError_t launch_gemm_fused(const void *W, int N, int K, const uint16_t *A, int lda, int M, float *Y, int ldy,
-                              unsigned int *status, cudaStream_t s);
 
 // ------------------------------------------------------------------ p/q verify
 

@@ -305,10 +305,8 @@ __device__ __forceinline__ int act_exponent(float maxabs) {
 // (the row scale and the code-position factor of dequant_pos, both exact), and the sum of
 // the block's f16 activations under the row scale alone, split into hi + lo f16.  The
 // padding blocks (v all zero) store zeros.
-// The prepared form of one block: its 16 pair slots and its hi + lo block sum (see
-// prep_store_block).
-__device__ __forceinline__ void prep_block_values(const float (&v)[32], int e, uint32_t (&w)[16], __half &hi,
-                                                  __half &lo) {
+__device__ __forceinline__ void prep_store_block(const float (&v)[32], int e, uint32_t *act_row, __half *sh,
+                                                 __half *sl, int b) {
     __half h[32];
     float s = 0.0f;
 #pragma unroll
@@ -316,94 +314,21 @@ __device__ __forceinline__ void prep_block_values(const float (&v)[32], int e, u
         h[j] = __float2half_rn(ldexpf(v[j], -e - 2 * (j & 3)));
         s += __half2float(__float2half_rn(ldexpf(v[j], -e)));
     }
+    uint32_t w[16];
 #pragma unroll
     for (int p = 0; p < 16; ++p) {
         const int k0 = 16 * (p >> 3) + (p & 7);
         w[p] = pack_half2(h[k0], h[k0 + 8]);
     }
-    hi = __float2half_rn(s);
-    lo = __float2half_rn(s - __half2float(hi));
-}
-
-// Largest magnitude of 32 bf16 activations held as 16 packed words (NaNs are skipped): a
-// packed |.|-max tree, then the two halves.
-__device__ __forceinline__ float bf16x2_maxabs(const uint32_t (&w)[16]) {
-    uint32_t m[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i)
-        asm("max.xorsign.abs.bf16x2 %0, %1, %2;\n" : "=r"(m[i]) : "r"(w[2 * i]), "r"(w[2 * i + 1]));
-#pragma unroll
-    for (int s = 4; s > 0; s >>= 1)
-#pragma unroll
-        for (int i = 0; i < s; ++i) asm("max.xorsign.abs.bf16x2 %0, %1, %2;\n" : "=r"(m[i]) : "r"(m[i]), "r"(m[i + s]));
-    return fmaxf(__uint_as_float((m[0] << 16) & 0x7FFF0000u), __uint_as_float(m[0] & 0x7FFF0000u));
-}
-
-// 2^n as an fp32 for -126 <= n <= 127 (exact).
-__device__ __forceinline__ float exp2i(int n) { return __int_as_float((n + 127) << 23); }
-
-// prep_block_values from 32 bf16 activations in 16 packed words (element 2i in the low half of
-// word i), with the row exponent e: the same prepared values, formed with exact power-of-two
-// multiplies and packed conversions when 2^-e and 2^(-e-6) are normal fp32 numbers, and
-// through prep_block_values otherwise.  The block sum is the fp32 sum of the scaled (not
-// f16-rounded) activations, split into hi + lo f16.
-__device__ __forceinline__ void prep_block_values_bf16(const uint32_t (&w)[16], int e, uint32_t (&out)[16],
-                                                       __half &hi, __half &lo) {
-    float v[32];
-#pragma unroll
-    for (int i = 0; i < 16; ++i) {
-        v[2 * i] = __uint_as_float(w[i] << 16);
-        v[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
-    }
-    if (e < -120 || e > 120) {
-        prep_block_values(v, e, out, hi, lo);
-        return;
-    }
-    const float sc[4] = {exp2i(-e), exp2i(-e - 2), exp2i(-e - 4), exp2i(-e - 6)};
-    float ssum = 0.0f;  // scaled before summing, so it cannot overflow
-#pragma unroll
-    for (int j = 0; j < 32; ++j) ssum = fmaf(v[j], sc[0], ssum);
-#pragma unroll
-    for (int p = 0; p < 16; ++p) {
-        const int k0 = 16 * (p >> 3) + (p & 7);
-        const float a = v[k0] * sc[k0 & 3], b = v[k0 + 8] * sc[k0 & 3];
-        asm("cvt.rn.f16x2.f32 %0, %1, %2;\n" : "=r"(out[p]) : "f"(b), "f"(a));  // a in the low half
-    }
-    hi = __float2half_rn(ssum);
-    lo = __float2half_rn(ssum - __half2float(hi));
-}
-
-__device__ __forceinline__ void prep_store_block(const float (&v)[32], int e, uint32_t *act_row, __half *sh,
-                                                 __half *sl, int b) {
-    uint32_t w[16];
-    __half hi, lo;
-    prep_block_values(v, e, w, hi, lo);
     uint4 *dst = reinterpret_cast<uint4 *>(act_row + (size_t)b * 16);
 #pragma unroll
     for (int j = 0; j < 4; ++j) dst[j] = make_uint4(w[4 * j], w[4 * j + 1], w[4 * j + 2], w[4 * j + 3]);
+    const __half hi = __float2half_rn(s);
     sh[b] = hi;
-    sl[b] = lo;
+    sl[b] = __float2half_rn(s - __half2float(hi));
 }
 
-// The same prepared block written straight into a staged operand (the SmemAct layout that
-// stage_act_issue produces): slot p of block b of column c lands at pair (b / 2), fragment
-// group p / 4, block half b % 2, and word (p & 2 ? 4 : 0) + (p & 1) inside the group.
-__device__ __forceinline__ void prep_store_block_smem(const uint32_t (&raw)[16], int e, uint32_t *sm,
-                                                      const SmemAct &SA, int c, int b) {
-    uint32_t w[16];
-    __half hi, lo;
-    prep_block_values_bf16(raw, e, w, hi, lo);
-    uint32_t *dst = SA.act(sm, c) + (b >> 1) * kPairWords + 2 * (b & 1);
-#pragma unroll
-    for (int grp = 0; grp < 4; ++grp) {
-        *reinterpret_cast<uint2 *>(dst + 8 * grp) = make_uint2(w[4 * grp], w[4 * grp + 1]);
-        *reinterpret_cast<uint2 *>(dst + 8 * grp + 4) = make_uint2(w[4 * grp + 2], w[4 * grp + 3]);
-    }
-    reinterpret_cast<__half *>(SA.shi(sm, c))[b] = hi;
-    reinterpret_cast<__half *>(SA.slo(sm, c))[b] = lo;
-}
-
-// Block-wide max of non-negative values (blockDim.x <= 1024); every thread gets the result.// Block-wide max of non-negative values (blockDim.x <= 1024); every thread gets the result.
+// Block-wide max of non-negative values (blockDim.x <= 1024); every thread gets the result.
 __device__ __forceinline__ float block_max_nonneg(float v, float *scratch32) {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));

@@ -242,8 +242,8 @@ def test_umma_deterministic_and_ldy(env):
 
 
 def test_activation_magnitude_varies_along_k(env):
-    """The fused small-M path scales each warp's K slice of a row by its own power of two: slices
-    of one row 1e20 apart, and a row that is zero in some slices only, stay within the bound."""
+    """One power-of-two scale per activation row: slices of one row 1e20 apart, and a row that is
+    zero in some slices only, stay within the bound."""
     st = synth.Streams(78)
     M, N, K = 5, 48, 4096
     W = synth.q2b32_weights(st, N, K)
