@@ -166,68 +166,45 @@ __global__ void __launch_bounds__(kRoutePrepThreads) moe_route_prep_kernel(MoeAr
 }
 
 
-// h for grouped pairs r0 .. r0+n-1: silu(sum_ks G[ks][r]) * sum_ks U[ks][r] (fixed order),
-// prepared as the down GEMM's B operand.  The block covers several rows at once: thread t takes
-// block t % nbp of row t / nbp (nbp = F/32 rounded to whole tiles, F <= 8192), and a row's
-// maximum is combined over its threads in shared memory.  The gate/up outputs were written by
-// other CTAs of the same kernel, so they are read from L2, every load of a thread before any use.
-__device__ __forceinline__ void prep_h_rows(const float *__restrict__ gu, int P, int F, int KS, int r0, int n,
-                                            const PrepPtrs &Pp, const PrepLayout &L, int *smax) {
-    const int nbp = L.nbp;                     // threads per row
-    const int rows_per_pass = blockDim.x / nbp;  // >= 1
-    for (int p0 = 0; p0 < n; p0 += rows_per_pass) {
-        const int ri = threadIdx.x / nbp, b = threadIdx.x - ri * nbp;
-        const int r = r0 + p0 + ri;
-        const bool live = ri < rows_per_pass && p0 + ri < n;
-        float v[32];
-        float mx = 0.0f;
-        if (live && b < L.nb) {
-            float4 x[8], y[8];
-            const float4 *G = reinterpret_cast<const float4 *>(gu + ((size_t)0 * P + r) * F + (size_t)b * 32);
-            const float4 *U = reinterpret_cast<const float4 *>(gu + ((size_t)1 * P + r) * F + (size_t)b * 32);
+// h for grouped pair r: silu(sum_ks G[ks][r]) * sum_ks U[ks][r] (fixed order), prepared as
+// the down GEMM's B operand.  The whole block takes part, one thread per 32-element block of F
+// (F <= 8192); the gate/up outputs were written by other CTAs of the same kernel, so they are
+// read from L2.
+__device__ __forceinline__ void prep_h_row(const float *__restrict__ gu, int P, int F, int KS, int r,
+                                           const PrepPtrs &Pp, const PrepLayout &L, float *scratch) {
+    const int b = threadIdx.x;
+    float v[32];
+    float mx = 0.0f;
+    if (b < L.nb) {
+        float g[32], u[32];
+#pragma unroll
+        for (int j = 0; j < 32; ++j) g[j] = u[j] = 0.0f;
+        for (int ks = 0; ks < KS; ++ks) {
+            const float4 *G = reinterpret_cast<const float4 *>(gu + ((size_t)(ks * 2 + 0) * P + r) * F + (size_t)b * 32);
+            const float4 *U = reinterpret_cast<const float4 *>(gu + ((size_t)(ks * 2 + 1) * P + r) * F + (size_t)b * 32);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                x[j] = __ldcg(G + j);
-                y[j] = __ldcg(U + j);
+                const float4 x = __ldcg(G + j), y = __ldcg(U + j);
+                g[4 * j] += x.x; g[4 * j + 1] += x.y; g[4 * j + 2] += x.z; g[4 * j + 3] += x.w;
+                u[4 * j] += y.x; u[4 * j + 1] += y.y; u[4 * j + 2] += y.z; u[4 * j + 3] += y.w;
             }
-            for (int ks = 1; ks < KS; ++ks) {
-                const float4 *G2 = reinterpret_cast<const float4 *>(gu + ((size_t)(ks * 2 + 0) * P + r) * F + (size_t)b * 32);
-                const float4 *U2 = reinterpret_cast<const float4 *>(gu + ((size_t)(ks * 2 + 1) * P + r) * F + (size_t)b * 32);
-#pragma unroll
-                for (int j = 0; j < 8; ++j) {
-                    const float4 g2 = __ldcg(G2 + j), u2 = __ldcg(U2 + j);
-                    x[j].x += g2.x; x[j].y += g2.y; x[j].z += g2.z; x[j].w += g2.w;
-                    y[j].x += u2.x; y[j].y += u2.y; y[j].z += u2.z; y[j].w += u2.w;
-                }
-            }
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const float gg[4] = {x[j].x, x[j].y, x[j].z, x[j].w}, uu[4] = {y[j].x, y[j].y, y[j].z, y[j].w};
-#pragma unroll
-                for (int i = 0; i < 4; ++i) {
-                    v[4 * j + i] = gg[i] / (1.0f + expf(-gg[i])) * uu[i];
-                    mx = fmaxf(mx, fabsf(v[4 * j + i]));
-                }
-            }
-        } else {
-#pragma unroll
-            for (int j = 0; j < 32; ++j) v[j] = 0.0f;
         }
-        // the row's maximum (non-negative floats order like their bit patterns)
-        if (threadIdx.x < rows_per_pass) smax[threadIdx.x] = 0;
-        __syncthreads();
-        if (live) atomicMax(&smax[ri], __float_as_int(mx));
-        __syncthreads();
-        const float rmax = live ? __int_as_float(smax[ri]) : 0.0f;
-        const int e = act_exponent(rmax);
-        if (live) {
-            if (b == 0) Pp.exps[r] = e;
-            prep_store_block(v, e, Pp.act + (size_t)r * L.act_words_per_row(),
-                             reinterpret_cast<__half *>(Pp.shi + (size_t)r * L.sum_words_per_row()),
-                             reinterpret_cast<__half *>(Pp.slo + (size_t)r * L.sum_words_per_row()), b);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            v[j] = g[j] / (1.0f + expf(-g[j])) * u[j];
+            mx = fmaxf(mx, fabsf(v[j]));
         }
-        __syncthreads();  // smax is free again
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) v[j] = 0.0f;
     }
+    const int e = act_exponent(block_max_nonneg(mx, scratch));
+    if (b == 0) Pp.exps[r] = e;
+    if (b < L.nbp)
+        prep_store_block(v, e, Pp.act + (size_t)r * L.act_words_per_row(),
+                         reinterpret_cast<__half *>(Pp.shi + (size_t)r * L.sum_words_per_row()),
+                         reinterpret_cast<__half *>(Pp.slo + (size_t)r * L.sum_words_per_row()), b);
+    __syncthreads();  // scratch is free again
 }
 
 // Grouped small-M GEMM over units u = (active expert, matrix, 16-row group, K split),
@@ -288,7 +265,7 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
     __shared__ int s_cnt[256];
     __shared__ int s_prow[64 * 16];
     __shared__ int s_rows[8], s_exps[8], s_orow[8];
-    __shared__ int s_rowmax[32];
+    __shared__ float s_scratch[32];
     __shared__ int s_done_n, s_done_off[kMaxRunsPerCta], s_done_cnt[kMaxRunsPerCta];
     pdl_wait();
     pdl_trigger();
@@ -458,7 +435,8 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
             __syncthreads();
             const PrepLayout LH(a.F);
             for (int d = 0; d < s_done_n; ++d)
-                prep_h_rows(w.h, P, a.F, KS, s_done_off[d], s_done_cnt[d], w.prepH, LH, s_rowmax);
+                for (int c = 0; c < s_done_cnt[d]; ++c)
+                    prep_h_row(w.h, P, a.F, KS, s_done_off[d] + c, w.prepH, LH, s_scratch);
         }
     }
     if (scale_mag_out_of_range(scale_max)) set_status(a.status, Q2_ERR_RANGE);
