@@ -42,7 +42,7 @@ METRIC = "verifier step µs & Q2B32 GEMM HBM GB/s (% peak) at M=5; pq_verify row
 WORKLOAD = ("verifier step at M=5: Q2B32 linear K=N=4096 M=5 + routed MoE FFN 64 experts "
             "H=4096 F=2048 top-6 M=5 + pq_verify S=3 k=4 V=129280 T=1")
 N_SETS = 4
-LAUNCHES_PER_STEP = 2 + 4 + 2   # prep + gemm; route with X prep, gate/up (with the h prep), down, combine; stats + verify
+LAUNCHES_PER_STEP = 2 + 5 + 2   # prep + gemm; route with X prep, gate/up, prep h, down, combine; stats + verify
 EXPERT_BYTES = 3 * 2048 * (4096 // 32) * 12   # gate + up + down of one expert
 
 

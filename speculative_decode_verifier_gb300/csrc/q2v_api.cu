@@ -108,7 +108,6 @@ MoeCarve moe_carve(void *ws, int M, int E, int topk, int H, int F) {
     r.w.pair_of = static_cast<int *>(c.take(P * sizeof(int)));
     r.w.slot_of = static_cast<int *>(c.take(P * sizeof(int)));
     r.w.gate_w = static_cast<float *>(c.take(P * sizeof(float)));
-    r.w.gu_done = static_cast<int *>(c.take((size_t)E * sizeof(int)));
     r.w.h = static_cast<float *>(c.take((size_t)kMaxKSplits * 2 * P * (size_t)F * sizeof(float)));
     r.w.out = static_cast<float *>(c.take((size_t)kMaxKSplits * P * (size_t)H * sizeof(float)));
     const PrepLayout LX(H), LH(F);

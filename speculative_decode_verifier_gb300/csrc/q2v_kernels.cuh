@@ -93,7 +93,6 @@ struct MoeWs {
     int *pair_of;     // [M*topk] grouped position of (row, slot)
     int *slot_of;     // [M*topk] (row, slot) index r*topk + t of each grouped position
     float *gate_w;    // [M*topk] gate weight of (row, slot)
-    int *gu_done;     // [E] finished gate/up units of each active expert (by active index), zeroed by the routing
     float *h;         // [KS][2][M*topk][F] fp32 gate and up partial sums per K split
     float *out;       // [KS][M*topk][H] fp32 down projection partial sums per K split, by (row, slot)
     PrepPtrs prepX;   // prepared X rows (K = H)

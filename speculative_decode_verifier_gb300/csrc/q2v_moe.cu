@@ -17,8 +17,7 @@
 //                each warp streams its units' weight tiles through its own cp.async ring;
 //                every active expert's weights are read once for all rows routed to it;
 //   4. prep h:   h = silu(sum of gate splits) * (sum of up splits), fused into the B-operand
-//                prep of the down GEMM, done for each expert by the gate/up CTA that finishes the
-//                expert's last units (a per-expert count; the last arriver prepares, nobody waits);
+//                prep of the down GEMM;
 //   5. down:     the same grouped GEMM over (active expert, 16-row group, K split) units;
 //   6. combine:  Y[r] = sum over slots, in slot order, of g * (sum of the down splits).
 // Every sum runs in a fixed order, so the result is deterministic.
@@ -38,7 +37,6 @@ __device__ __forceinline__ void route_rows(const MoeArgs &a, const MoeWs &w, int
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31, nw = blockDim.x >> 5;
     const int E = a.E, K = a.topk, M = a.M;
     for (int e = tid; e <= E; e += blockDim.x) s_cnt[e] = 0;
-    for (int e = tid; e < E; e += blockDim.x) w.gu_done[e] = 0;
     __syncthreads();
     for (int r = warp; r < M; r += nw) {
         const float *l = a.router + (size_t)r * E;
@@ -167,12 +165,13 @@ __global__ void __launch_bounds__(kRoutePrepThreads) moe_route_prep_kernel(MoeAr
 
 
 // h for grouped pair r: silu(sum_ks G[ks][r]) * sum_ks U[ks][r] (fixed order), prepared as
-// the down GEMM's B operand.  The whole block takes part, one thread per 32-element block of F
-// (F <= 8192); the gate/up outputs were written by other CTAs of the same kernel, so they are
-// read from L2.
-__device__ __forceinline__ void prep_h_row(const float *__restrict__ gu, int P, int F, int KS, int r,
-                                           const PrepPtrs &Pp, const PrepLayout &L, float *scratch) {
-    const int b = threadIdx.x;
+// the down GEMM's B operand.  One CTA per pair, one thread per 32-element block of F.
+__global__ void __launch_bounds__(256) moe_prep_h_kernel(const float *__restrict__ gu, int P, int F, int KS,
+                                                         PrepPtrs Pp, PrepLayout L) {
+    __shared__ float scratch[32];
+    pdl_wait();
+    pdl_trigger();
+    const int r = blockIdx.x, b = threadIdx.x;
     float v[32];
     float mx = 0.0f;
     if (b < L.nb) {
@@ -184,7 +183,7 @@ __device__ __forceinline__ void prep_h_row(const float *__restrict__ gu, int P, 
             const float4 *U = reinterpret_cast<const float4 *>(gu + ((size_t)(ks * 2 + 1) * P + r) * F + (size_t)b * 32);
 #pragma unroll
             for (int j = 0; j < 8; ++j) {
-                const float4 x = __ldcg(G + j), y = __ldcg(U + j);
+                const float4 x = G[j], y = U[j];
                 g[4 * j] += x.x; g[4 * j + 1] += x.y; g[4 * j + 2] += x.z; g[4 * j + 3] += x.w;
                 u[4 * j] += y.x; u[4 * j + 1] += y.y; u[4 * j + 2] += y.z; u[4 * j + 3] += y.w;
             }
@@ -204,7 +203,6 @@ __device__ __forceinline__ void prep_h_row(const float *__restrict__ gu, int P, 
         prep_store_block(v, e, Pp.act + (size_t)r * L.act_words_per_row(),
                          reinterpret_cast<__half *>(Pp.shi + (size_t)r * L.sum_words_per_row()),
                          reinterpret_cast<__half *>(Pp.slo + (size_t)r * L.sum_words_per_row()), b);
-    __syncthreads();  // scratch is free again
 }
 
 // Grouped small-M GEMM over units u = (active expert, matrix, 16-row group, K split),
@@ -251,10 +249,6 @@ struct UnitMap {
 };
 
 constexpr int kRingStages = 4;  // weight tiles per warp in the shared-memory ring
-// Expert runs one gate/up CTA can complete.  A CTA's units are a contiguous range of fewer
-// units than one expert has (the grid holds at least 2 CTAs per SM and units are expert-major),
-// so its range meets at most 2 experts; the bound leaves room for small shapes.
-constexpr int kMaxRunsPerCta = 64;
 
 template <bool GATEUP, bool ALIGN8>
 __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, int KS, int ncols,
@@ -265,8 +259,6 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
     __shared__ int s_cnt[256];
     __shared__ int s_prow[64 * 16];
     __shared__ int s_rows[8], s_exps[8], s_orow[8];
-    __shared__ float s_scratch[32];
-    __shared__ int s_done_n, s_done_off[kMaxRunsPerCta], s_done_cnt[kMaxRunsPerCta];
     pdl_wait();
     pdl_trigger();
     const int P = a.M * a.topk;
@@ -309,7 +301,6 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
     const bool ring_path = (um.Nrows % kRowsPerCta) == 0 && L.nb == L.ntk * kTileBlocks && (L.nb % 4) == 0;
     uint32_t scale_max = 0u;  // running max of |d|, |m| (f16x2)
 
-    if (threadIdx.x == 0) s_done_n = 0;
     for (int seg0 = i0; seg0 < i1;) {
         // the run of units of one expert
         const int ai = seg0 / per_expert;
@@ -410,34 +401,7 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
                 }
             }
         }
-        if (GATEUP) {
-            // This CTA's units of expert e are stored.  The CTA that completes the expert's
-            // count (every unit of every CTA) turns the expert's gate/up outputs into h, the down
-            // GEMM's operand, once its own units are all done (below): last arriver, no CTA waits
-            // for another.
-            __syncthreads();
-            if (threadIdx.x == 0) {
-                __threadfence();  // release this CTA's outputs before its count
-                const int done = atomicAdd(&w.gu_done[ai], seg1 - seg0) + (seg1 - seg0);
-                if (done == per_expert && s_done_n < kMaxRunsPerCta) {
-                    s_done_off[s_done_n] = off;
-                    s_done_cnt[s_done_n] = cnt;
-                    ++s_done_n;
-                }
-            }
-        }
         seg0 = seg1;
-    }
-    if (GATEUP) {
-        __syncthreads();
-        if (s_done_n > 0) {
-            if (threadIdx.x == 0) __threadfence();  // acquire: the other CTAs' outputs of these experts
-            __syncthreads();
-            const PrepLayout LH(a.F);
-            for (int d = 0; d < s_done_n; ++d)
-                for (int c = 0; c < s_done_cnt[d]; ++c)
-                    prep_h_row(w.h, P, a.F, KS, s_done_off[d] + c, w.prepH, LH, s_scratch);
-        }
     }
     if (scale_mag_out_of_range(scale_max)) set_status(a.status, Q2_ERR_RANGE);
 }
@@ -525,6 +489,8 @@ cudaError_t launch_moe(const MoeArgs &a, const MoeWs &w, int num_sms, cudaStream
     const int ks_gu = choose_ks(expect_active * 2 * cdiv(a.F, kRowsPerCta), LX.ntk, resident_warps);
     const int ks_d = choose_ks(expect_active * cdiv(a.H, kRowsPerCta), LH.ntk, resident_warps);
     err = probed(kProbeMoeGateUp, s, [&] { return launch_stream<true>(a, w, ks_gu, w.h, num_sms, LX, s); });
+    if (err != cudaSuccess) return err;
+    err = launch_pdl(moe_prep_h_kernel, dim3(P), dim3(256), s, (const float *)w.h, P, a.F, ks_gu, w.prepH, LH);
     if (err != cudaSuccess) return err;
     err = probed(kProbeMoeDown, s, [&] { return launch_stream<false>(a, w, ks_d, w.out, num_sms, LH, s); });
     if (err != cudaSuccess) return err;

@@ -12,8 +12,8 @@ import bench  # noqa: E402
 
 
 def test_launches_per_step():
-    # prep + GEMM; route with X prep, gate/up (with the h prep), down, combine; statistics + draw
-    assert bench.LAUNCHES_PER_STEP == 8
+    # prep + GEMM; route with X prep, gate/up, prep h, down, combine; statistics + draw
+    assert bench.LAUNCHES_PER_STEP == 9
 
 
 def test_traffic_record_parses():
