@@ -64,13 +64,15 @@ def _kernel_source_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def _traffic_record():
-    """The `traffic-record:` line of the step's launch-list summary under profiles/, as a dict."""
+def _traffic_record(tag: str = "traffic-record"):
+    """A `<tag>:` line of the step's launch-list summary under profiles/, as a dict: `traffic-record`
+    (one eager launch, caches flushed) or `traffic-timed` (graph-replayed launches of the timed
+    configuration)."""
     path = os.path.join(ROOT, "profiles", "verifier_step_m5_launch_list.md")
     try:
         with open(path) as f:
             for line in f:
-                if line.startswith("traffic-record:"):
+                if line.startswith(tag + ":"):
                     return dict(kv.split("=", 1) for kv in line.split(":", 1)[1].split())
     except OSError:
         pass
@@ -658,12 +660,16 @@ def run_device(args, rank: int, world: int):
             d["frac_of_read_probe"] = d["GB/s"] / read_gbs
         kernels[name] = d
     dom = kernels["moe_gate_up"]
-    # DRAM traffic of one launch from the recorded ncu capture, scaled to the mean launch by
-    # active experts; null when the kernel's source has changed since the capture
-    traffic = None
-    rec = _traffic_record()
-    if rec and rec.get("sources") == _kernel_source_digest():
-        traffic = float(rec["bytes"]) * statistics.mean(active[si] for si in kern_us["moe_gate_up"][1]) / float(rec["units"])
+    # DRAM traffic per launch from the recorded ncu captures (the graph-replayed timed
+    # configuration, and an eager launch with flushed caches), scaled to the mean launch by active
+    # experts; null when the kernel's source has changed since the capture
+    def scaled_traffic(tag):
+        rec = _traffic_record(tag)
+        if rec and rec.get("sources") == _kernel_source_digest():
+            return float(rec["bytes"]) * statistics.mean(active[si] for si in kern_us["moe_gate_up"][1]) / float(rec["units"])
+        return None
+    traffic = scaled_traffic("traffic-timed")
+    traffic_eager = scaled_traffic("traffic-record")
     line = {
         "metric": METRIC, "value": step_us, "unit": "µs", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": step_us / 1000.0, "higher_is_better": False,
@@ -679,7 +685,7 @@ def run_device(args, rank: int, world: int):
         "kernels": kernels,
         "roofline": {"bound": "hbm", "kernel": "moe_stream_kernel<gate+up> (MoE gate+up grouped dequant GEMM)",
                      "achieved": dom["GB/s"], "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
-                     "frac": dom["frac"], "traffic": traffic,
+                     "frac": dom["frac"], "traffic": traffic, "traffic_eager": traffic_eager,
                      "read_probe_GB/s": read_gbs, "frac_of_read_probe": dom["GB/s"] / read_gbs,
                      "algorithmic_bytes_per_launch": dom["bytes"], "us_per_launch": dom["us"]},
         "e2e": {"value": e2e_us, "unit": "µs", "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -41,3 +41,11 @@ def test_near_tie_counter():
                       mismatches_without_near_tie=0)
     t[0, 1] = 8
     assert bench._near_ties(n, t, o, u_acc, u_fin, 2)["mismatches_without_near_tie"] == 1
+
+
+def test_timed_traffic_record_parses():
+    rec = bench._traffic_record("traffic-timed")
+    assert rec is not None and rec["unit"] == "active_experts"
+    assert rec["sources"] == bench._traffic_record()["sources"]
+    # the timed launches read what the weights need, give or take the L2's write-backs
+    assert 6_291_456 <= int(rec["bytes"]) / int(rec["units"]) < 1.1 * 6_291_456
