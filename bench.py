@@ -12,8 +12,9 @@ are random, not trained.  Device timing replays one CUDA graph per input set, ro
 
 Prints one JSON line.  `value` is the device-timed step time in microseconds (inputs resident
 in HBM); `e2e` is the same step through the Python binding with pinned host buffers copied
-in and results copied out inside the timed region, every step; the input copies run on a
-second stream, so step i+1's copies overlap step i's kernels.  `cpu_baseline` is the fp64 CPU
+in and results copied out inside the timed region, every step (the step's library calls replayed
+from one captured graph per input slot); the input copies run on a second stream, so step i+1's
+copies overlap step i's kernels.  `cpu_baseline` is the fp64 CPU
 oracle timed on the host cores over the full step of input set 0 (all cores, and one core);
 the same oracle outputs check the GPU's results of that set's graph-replayed step (`parity`:
 GEMM and MoE bounds, accepted counts and tokens with the near-ties counted), and of the M=60
@@ -601,6 +602,20 @@ def run_device(args, rank: int, world: int):
             cstream.wait_event(ev_done[j])
             res_host[j].copy_(res_slots[j][0], non_blocking=True)
 
+    # The step's library calls for each slot, captured once into a CUDA graph (the calls are
+    # graph-capturable by design), as a serving loop would replay them; the copies stay outside
+    # the graphs, on the copy stream.
+    for j in range(N_SETS):
+        step(dev_in[j][1], res_slots[j][1])  # one eager pass first
+    torch.cuda.synchronize()
+    e2e_graphs = []
+    for j in range(N_SETS):
+        gr = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(gr):
+            step(dev_in[j][1], res_slots[j][1])
+        e2e_graphs.append(gr)
+    torch.cuda.synchronize()
+
     def run_steps(n):
         for i in range(min(AHEAD, n)):
             copy_in(i)
@@ -609,7 +624,7 @@ def run_device(args, rank: int, world: int):
                 copy_in(i + AHEAD)
             j = i % N_SETS
             comp.wait_event(ev_in[j])
-            step(dev_in[j][1], res_slots[j][1])
+            e2e_graphs[j].replay()
             ev_done[j].record(comp)
             copy_out(i)
 
