@@ -221,6 +221,14 @@ q2_status q2_tiny_gemm(const void *W, int N, int K, const uint16_t *A, int M, in
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
     Carver c(ws);
     const int sms = device_sms();
+    if (stream_gemm_preferred(M, N, K, sms)) {  // few activation rows, many weight rows
+        const PrepLayout L(K);
+        const PrepPtrs P = PrepPtrs::carve(c.take(L.bytes(M)), L, M);
+        if (launch_prep_bf16(A, lda, nullptr, M, K, P, L, s) != cudaSuccess) return Q2_ERR_CUDA;
+        return cuda_status(probed(kProbeGemm, s, [&] {
+            return launch_gemm_stream(W, N, K, P, L, M, Y, ldy, status_word(ws), sms, s);
+        }));
+    }
     if (umma_gemm_preferred(M, N, K, sms)) {
         void *img = c.take(umma_gemm_ws_bytes(M, K));
         if (launch_prep_umma(A, lda, M, K, img, s) != cudaSuccess) return Q2_ERR_CUDA;
@@ -329,7 +337,8 @@ q2_status q2_lm_head_verify(const void *W, int V, int K, const uint16_t *A, int 
     const int sms = device_sms();
     unsigned int *status = status_word(ws);
     if (flags & ~Q2_LM_HEAD_FUSE_STATS) return Q2_ERR_INVALID_ARG;
-    const bool umma = umma_gemm_preferred((int)M, V, K, sms);
+    const bool streamed = stream_gemm_preferred((int)M, V, K, sms);
+    const bool umma = !streamed && umma_gemm_preferred((int)M, V, K, sms);
     const bool fused = (flags & Q2_LM_HEAD_FUSE_STATS) && umma && V > kWarpTierMaxV;
     Carver c(ws);
     // 1. target logits = A W^T (rows s*(k+1) + i), with the target rows' softmax partials
@@ -360,7 +369,8 @@ q2_status q2_lm_head_verify(const void *W, int V, int K, const uint16_t *A, int 
         e = launch_prep_bf16(A, lda, nullptr, (int)M, K, P, L, s);
         if (e != cudaSuccess) return Q2_ERR_CUDA;
         e = probed(kProbeGemm, s, [&] {
-            return launch_gemm_small(W, V, K, P, L, (int)M, target_logits, V, status, s);
+            return streamed ? launch_gemm_stream(W, V, K, P, L, (int)M, target_logits, V, status, sms, s)
+                          : launch_gemm_small(W, V, K, P, L, (int)M, target_logits, V, status, s);
         });
     }
     if (e != cudaSuccess) return Q2_ERR_CUDA;

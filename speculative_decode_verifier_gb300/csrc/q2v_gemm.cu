@@ -87,6 +87,121 @@ __global__ void __launch_bounds__(kGemmWarps * 32) q2_gemm_mma_kernel(const uint
     if (scale_mag_out_of_range(scale_max)) set_status(status, Q2_ERR_RANGE);
 }
 
+// Small M (<= 8) against many weight rows: a persistent grid (2 CTAs of 8 warps per SM), the
+// prepared activation rows staged in shared memory once per CTA, and 16-row units (all of K)
+// taken by the CTA's warps from its contiguous range of units, each warp streaming its units'
+// 16 x 256 weight tiles through its own 4-deep cp.async ring and decoding them with the same
+// exact mma.sync tile decode (the MoE stream kernel's arrangement, for one matrix).  The first
+// ring tiles are requested before the programmatic wait (the weights do not depend on the
+// previous kernel); the staged activations after it.  Requires K % 256 == 0 and N % 16 == 0.
+constexpr int kStreamRing = 4;
+constexpr int kStreamWarps = 8;
+
+__global__ void __launch_bounds__(kStreamWarps * 32, 2)
+    q2_gemm_stream_kernel(const uint8_t *__restrict__ W, int N, int K, PrepPtrs P, PrepLayout L, int M,
+                          float *__restrict__ Y, int ldy, unsigned int *status) {
+    extern __shared__ __align__(16) uint32_t sm_dyn[];
+    __shared__ int s_rows[8], s_exps[8];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const SmemAct SA(L, M);
+    uint32_t *sm_act = sm_dyn;
+    uint32_t *ring = sm_dyn + SA.words() + (size_t)warp * kStreamRing * kTileWords;
+    const size_t row_bytes = (size_t)L.nb * kBlockBytes;
+    const int units = N / kRowsPerCta;
+    const int q = cdiv(units, gridDim.x);
+    const int u0 = blockIdx.x * q, u1 = min(units, u0 + q);
+    // producer cursor: this warp's units u0 + warp, + kStreamWarps, ..., tiles 0 .. ntk-1 each
+    int pu = u0 + warp, ptile = 0;
+    auto produce = [&](int stage) {
+        if (pu < u1) {
+            issue_tile_cpasync(ring + stage * kTileWords, W + (size_t)pu * kRowsPerCta * row_bytes, row_bytes, ptile,
+                               lane);
+            if (++ptile == L.ntk) {
+                ptile = 0;
+                pu += kStreamWarps;
+            }
+        }
+        cp_async_commit();  // one group per slot, empty or not, keeps the count uniform
+    };
+#pragma unroll
+    for (int sidx = 0; sidx < kStreamRing - 1; ++sidx) produce(sidx);
+    pdl_wait();
+    pdl_trigger();
+    if (threadIdx.x < 8) {
+        s_rows[threadIdx.x] = threadIdx.x < M ? (int)threadIdx.x : 0;
+        s_exps[threadIdx.x] = threadIdx.x < M ? P.exps[threadIdx.x] : 0;
+    }
+    __syncthreads();
+    stage_act_issue(sm_act, SA, P, L, s_rows, M);  // the newest group: wait for every group
+    cp_async_wait<0>();
+    __syncthreads();
+    uint32_t scale_max = 0u;  // running max of |d|, |m| (f16x2)
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    int cu = u0 + warp, ctile = 0;
+    for (int it = 0; cu < u1; ++it) {
+        produce((it + kStreamRing - 1) % kStreamRing);
+        cp_async_wait<kStreamRing - 1>();  // this tile's group has landed
+        __syncwarp();
+        TileRegs cur;
+        read_tile_smem(cur, ring + (it % kStreamRing) * kTileWords, lane);
+        compute_tile_smem(cur, sm_act, SA, M, ctile, lane, acc, scale_max);
+        if (++ctile == L.ntk) {
+            // rows g, g+8 of the unit, activation rows 2t, 2t+1
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                const int m = 2 * t + (qq & 1), n = cu * kRowsPerCta + g + 8 * (qq >> 1);
+                if (m < M) Y[(size_t)m * ldy + n] = ldexpf(acc[0][qq] + acc[1][qq], s_exps[m]);
+                acc[0][qq] = 0.0f;
+                acc[1][qq] = 0.0f;
+            }
+            ctile = 0;
+            cu += kStreamWarps;
+        }
+        __syncwarp();  // every lane has read this stage before a later copy refills it
+    }
+    cp_async_wait<0>();
+    if (scale_mag_out_of_range(scale_max)) set_status(status, Q2_ERR_RANGE);
+}
+
+bool stream_gemm_usable(int M, int N, int K) {
+    return M >= 1 && M <= 8 && K % (kTileBlocks * kBlockK) == 0 && N % kRowsPerCta == 0;
+}
+
+// The streaming kernel pays off once every warp of the persistent grid has at least one 16-row
+// unit to stream (N >= 16 rows x 8 warps x 2 CTAs x SMs).
+bool stream_gemm_preferred(int M, int N, int K, int sms) {
+    return stream_gemm_usable(M, N, K) && (long long)N >= (long long)kRowsPerCta * kStreamWarps * 2 * sms;
+}
+
+namespace {
+size_t g_stream_smem_cfg[kCacheDevices];
+}  // namespace
+
+cudaError_t launch_gemm_stream(const void *W, int N, int K, const PrepPtrs &P, const PrepLayout &L, int M, float *Y,
+                               int ldy, unsigned int *status, int num_sms, cudaStream_t s) {
+    auto kern = q2_gemm_stream_kernel;
+    const size_t smem = SmemAct(L, M).bytes() + (size_t)kStreamWarps * kStreamRing * kTileWords * 4;
+    const int dv = cache_device();
+    if (dv < 0 || g_stream_smem_cfg[dv] < smem) {
+        const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (dv >= 0) g_stream_smem_cfg[dv] = smem;
+    }
+    const int units = N / kRowsPerCta;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(max(1, min(units, 2 * num_sms)));
+    cfg.blockDim = dim3(kStreamWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, static_cast<const uint8_t *>(W), N, K, P, L, M, Y, ldy, status);
+}
+
 namespace {
 size_t g_gemm_smem[kCacheDevices][2];  // dynamic shared memory each variant was configured for, per device
 

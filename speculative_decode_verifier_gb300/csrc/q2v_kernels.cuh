@@ -22,6 +22,12 @@ cudaError_t launch_prep_bf16(const uint16_t *src, int ld, const int *rows, int R
                              const PrepLayout &L, cudaStream_t s);
 cudaError_t launch_gemm_small(const void *W, int N, int K, const PrepPtrs &P, const PrepLayout &L, int M,
                               float *Y, int ldy, unsigned int *status, cudaStream_t s);
+// The streaming variant for M <= 8 against many weight rows (q2v_gemm.cu): persistent CTAs with
+// per-warp weight rings; K % 256 == 0 and N % 16 == 0 (stream_gemm_usable).
+bool stream_gemm_usable(int M, int N, int K);
+bool stream_gemm_preferred(int M, int N, int K, int sms);
+cudaError_t launch_gemm_stream(const void *W, int N, int K, const PrepPtrs &P, const PrepLayout &L, int M, float *Y,
+                               int ldy, unsigned int *status, int num_sms, cudaStream_t s);
 
 // ------------------------------------------------------------------ p/q verify
 
