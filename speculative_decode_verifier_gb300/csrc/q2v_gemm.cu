@@ -87,17 +87,19 @@ __global__ void __launch_bounds__(kGemmWarps * 32) q2_gemm_mma_kernel(const uint
     if (scale_mag_out_of_range(scale_max)) set_status(status, Q2_ERR_RANGE);
 }
 
-// Small M (<= 8) against many weight rows: a persistent grid (2 CTAs of 8 warps per SM), the
+// Small M (<= 8) against many weight rows: a persistent grid (one CTA of 24 warps per SM), the
 // prepared activation rows staged in shared memory once per CTA, and 16-row units (all of K)
 // taken by the CTA's warps from its contiguous range of units, each warp streaming its units'
-// 16 x 256 weight tiles through its own 4-deep cp.async ring and decoding them with the same
-// exact mma.sync tile decode (the MoE stream kernel's arrangement, for one matrix).  The first
+// 16 x 256 weight tiles through its own 3-deep cp.async ring and decoding them with the same
+// exact mma.sync tile decode (the MoE stream kernel's arrangement, for one matrix).  Measured
+// on the M=5 x 129,280 x 4,096 head: 60.5 us with 24 warps and 3-tile rings, 62.8 with 16 warps
+// and 4-tile rings, 64.1 with two CTAs of 8 warps and 4-tile rings.  The first
 // ring tiles are requested before the programmatic wait (the weights do not depend on the
 // previous kernel); the staged activations after it.  Requires K % 256 == 0 and N % 16 == 0.
-constexpr int kStreamRing = 4;
-constexpr int kStreamWarps = 8;
+constexpr int kStreamRing = 3;
+constexpr int kStreamWarps = 24;
 
-__global__ void __launch_bounds__(kStreamWarps * 32, 2)
+__global__ void __launch_bounds__(kStreamWarps * 32, 1)
     q2_gemm_stream_kernel(const uint8_t *__restrict__ W, int N, int K, PrepPtrs P, PrepLayout L, int M,
                           float *__restrict__ Y, int ldy, unsigned int *status) {
     extern __shared__ __align__(16) uint32_t sm_dyn[];
@@ -164,14 +166,20 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 2)
     if (scale_mag_out_of_range(scale_max)) set_status(status, Q2_ERR_RANGE);
 }
 
-bool stream_gemm_usable(int M, int N, int K) {
-    return M >= 1 && M <= 8 && K % (kTileBlocks * kBlockK) == 0 && N % kRowsPerCta == 0;
+size_t stream_smem_bytes(int M, int K) {
+    return SmemAct(PrepLayout(K), M).bytes() + (size_t)kStreamWarps * kStreamRing * kTileWords * 4;
 }
 
-// The streaming kernel pays off once every warp of the persistent grid has at least one 16-row
-// unit to stream (N >= 16 rows x 8 warps x 2 CTAs x SMs).
+bool stream_gemm_usable(int M, int N, int K) {
+    return M >= 1 && M <= 8 && K % (kTileBlocks * kBlockK) == 0 && N % kRowsPerCta == 0 &&
+           stream_smem_bytes(M, K) <= (size_t)220 * 1024;
+}
+
+// The streaming kernel pays off once the persistent grid has about 16 rows for each of 16
+// warps per SM (N >= 16 x 16 x SMs: 38,912 rows on 152 SMs); at fewer rows the per-CTA kernel or
+// the tcgen05 kernel is used.
 bool stream_gemm_preferred(int M, int N, int K, int sms) {
-    return stream_gemm_usable(M, N, K) && (long long)N >= (long long)kRowsPerCta * kStreamWarps * 2 * sms;
+    return stream_gemm_usable(M, N, K) && (long long)N >= (long long)kRowsPerCta * 16 * sms;
 }
 
 namespace {
@@ -181,7 +189,7 @@ size_t g_stream_smem_cfg[kCacheDevices];
 cudaError_t launch_gemm_stream(const void *W, int N, int K, const PrepPtrs &P, const PrepLayout &L, int M, float *Y,
                                int ldy, unsigned int *status, int num_sms, cudaStream_t s) {
     auto kern = q2_gemm_stream_kernel;
-    const size_t smem = SmemAct(L, M).bytes() + (size_t)kStreamWarps * kStreamRing * kTileWords * 4;
+    const size_t smem = stream_smem_bytes(M, K);
     const int dv = cache_device();
     if (dv < 0 || g_stream_smem_cfg[dv] < smem) {
         const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
@@ -190,7 +198,7 @@ cudaError_t launch_gemm_stream(const void *W, int N, int K, const PrepPtrs &P, c
     }
     const int units = N / kRowsPerCta;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(max(1, min(units, 2 * num_sms)));
+    cfg.gridDim = dim3(max(1, min(units, num_sms)));
     cfg.blockDim = dim3(kStreamWarps * 32);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;

@@ -57,6 +57,8 @@ def test_verifier_linear_config(env):
     (5, 40960, 4096),  # the streaming kernel (many weight rows per SM): one session against a head
     (1, 65536, 256),   # streaming, one activation row, one K tile
     (8, 40000, 1024),  # streaming, all 8 columns of the MMA, units not a multiple of the warps
+    (5, 40960, 8192),  # streaming at the largest K (the staged rows and the rings fill shared memory)
+    (8, 39936, 8192),  # 8 rows at the largest K do not fit: the other kernels take it
 ])
 def test_shapes(env, M, N, K):
     st = synth.Streams(1000 + M * 7 + N + K)
