@@ -248,11 +248,10 @@ struct UnitMap {
     }
 };
 
-constexpr int kRingStages = 3;  // weight tiles per warp in the shared-memory ring
-constexpr int kMoeWarps = 24;   // warps of a stream-kernel CTA (one CTA per SM)
+constexpr int kRingStages = 4;  // weight tiles per warp in the shared-memory ring
 
 template <bool GATEUP, bool ALIGN8>
-__global__ void __launch_bounds__(kMoeWarps * 32, 1) moe_stream_kernel(MoeArgs a, MoeWs w, int KS, int ncols,
+__global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, int KS, int ncols,
                                                             float *__restrict__ outp) {
     extern __shared__ __align__(16) uint32_t sm_dyn[];
     __shared__ int s_active[257];
@@ -427,33 +426,30 @@ __global__ void __launch_bounds__(256) moe_combine_kernel(MoeArgs a, MoeWs w, in
 }
 
 namespace {
-// per device: resident CTAs per SM of the four stream-kernel variants (0 = unknown), and the
-// dynamic shared memory and block size they were configured for
+// per device: resident CTAs per SM of the four stream-kernel variants (0 = unknown) and the
+// dynamic shared memory each was configured for
 int g_stream_blocks[kCacheDevices][4];
 size_t g_stream_smem[kCacheDevices][4];
-int g_stream_warps[kCacheDevices][4];
 
 template <bool GU, bool A8>
 cudaError_t launch_stream_variant(int idx, const MoeArgs &a, const MoeWs &w, int KS, float *out, int num_sms,
-                                  size_t smem, int warps, cudaStream_t s) {
+                                  size_t smem, cudaStream_t s) {
     auto kern = moe_stream_kernel<GU, A8>;
     const int dv = cache_device();
     int blocks = dv >= 0 ? g_stream_blocks[dv][idx] : 0;
-    if (dv < 0 || g_stream_smem[dv][idx] != smem || g_stream_warps[dv][idx] != warps) {
+    if (dv < 0 || g_stream_smem[dv][idx] < smem) {
         cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e != cudaSuccess) return e;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, warps * 32, smem) != cudaSuccess ||
-            blocks <= 0)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&blocks, kern, 256, smem) != cudaSuccess || blocks <= 0)
             blocks = 1;
         if (dv >= 0) {
             g_stream_blocks[dv][idx] = blocks;
             g_stream_smem[dv][idx] = smem;
-            g_stream_warps[dv][idx] = warps;
         }
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(num_sms * blocks);
-    cfg.blockDim = dim3(warps * 32);
+    cfg.blockDim = dim3(256);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cudaLaunchAttribute attr[1];
@@ -464,17 +460,12 @@ cudaError_t launch_stream_variant(int idx, const MoeArgs &a, const MoeWs &w, int
     return cudaLaunchKernelEx(&cfg, kern, a, w, KS, min(8, a.M), out);
 }
 
-// kMoeWarps warps per CTA, or 8 when the staged rows leave too little shared memory for 24 rings
-// (8 staged columns at K = 8192).
 template <bool GU>
 cudaError_t launch_stream(const MoeArgs &a, const MoeWs &w, int KS, float *out, int num_sms, const PrepLayout &L,
                           cudaStream_t s) {
-    const size_t act = SmemAct(L, min(8, a.M)).bytes();
-    int warps = kMoeWarps;
-    if (act + (size_t)warps * kRingStages * kTileWords * 4 > (size_t)220 * 1024) warps = 8;
-    const size_t smem = act + (size_t)warps * kRingStages * kTileWords * 4;
-    if (L.nb % 2 == 0) return launch_stream_variant<GU, true>(GU ? 0 : 2, a, w, KS, out, num_sms, smem, warps, s);
-    return launch_stream_variant<GU, false>(GU ? 1 : 3, a, w, KS, out, num_sms, smem, warps, s);
+    const size_t smem = SmemAct(L, min(8, a.M)).bytes() + (size_t)8 * kRingStages * kTileWords * 4;
+    if (L.nb % 2 == 0) return launch_stream_variant<GU, true>(GU ? 0 : 2, a, w, KS, out, num_sms, smem, s);
+    return launch_stream_variant<GU, false>(GU ? 1 : 3, a, w, KS, out, num_sms, smem, s);
 }
 
 // K splits so that the expected number of units is a few per resident warp.  Split ks takes

@@ -58,7 +58,6 @@ def test_moe_config_full_size(env):
     dict(E=8, H=4352, F=64, M=3, topk=2),      # 17 K tiles: 8 splits of 3 would leave 2 empty, so 6 are used
     dict(E=1, H=256, F=128, M=5, topk=1),      # one expert: every row routed to it with gate weight 1
     dict(E=2, H=512, F=256, M=8, topk=2),      # top-k = E: every row routed to every expert
-    dict(E=4, H=8192, F=128, M=8, topk=2),     # 8 staged columns at K = 8192: the gate/up CTAs run 8 warps
 ])
 def test_shapes(env, over):
     m = synth.config_moe(2, salt=sum(over.values()), **over)
