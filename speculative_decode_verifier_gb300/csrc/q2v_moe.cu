@@ -259,13 +259,19 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
     __shared__ int s_cnt[256];
     __shared__ int s_prow[64 * 16];
     __shared__ int s_rows[8], s_exps[8], s_orow[8];
-    pdl_wait();
-    pdl_trigger();
+    // The gate/up GEMM needs the routing its predecessor writes.  The down GEMM's predecessor is
+    // the h prep; the routing it needs was written two kernels earlier, by a grid that completed
+    // before this one was launched, so the down GEMM reads it (from L2) before its programmatic
+    // wait and has its first weight tiles requested by then.
+    if (GATEUP) {
+        pdl_wait();
+        pdl_trigger();
+    }
     const int P = a.M * a.topk;
-    for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_active[i] = w.active[i];
+    for (int i = threadIdx.x; i <= a.E; i += blockDim.x) s_active[i] = __ldcg(w.active + i);
     for (int i = threadIdx.x; i < a.E; i += blockDim.x) {
-        s_off[i] = w.offsets[i];
-        s_cnt[i] = w.counts[i];
+        s_off[i] = __ldcg(w.offsets + i);
+        s_cnt[i] = __ldcg(w.counts + i);
     }
     if (GATEUP)
         for (int i = threadIdx.x; i < P; i += blockDim.x) s_prow[i] = w.pair_row[i];
@@ -300,6 +306,20 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
     // the ring path: whole 16-row groups, whole tiles, 16-byte aligned rows
     const bool ring_path = (um.Nrows % kRowsPerCta) == 0 && L.nb == L.ntk * kTileBlocks && (L.nb % 4) == 0;
     uint32_t scale_max = 0u;  // running max of |d|, |m| (f16x2)
+    if (!GATEUP) {
+        // this warp's first ring tiles into L2 (the lines each lane's copies will read)
+        if (ring_path && i0 + warp < min(i1, (i0 / per_expert + 1) * per_expert)) {
+            const UnitInfo ui = um(i0 + warp);
+            for (int tt = ui.t0; tt < min(ui.t1, ui.t0 + kRingStages - 1); ++tt) {
+                const uint8_t *p = ui.W0 + (size_t)(lane >> 1) * um.row_bytes + (size_t)tt * (kTileBlocks * kBlockBytes) +
+                                   (lane & 1) * 48;
+                prefetch_l2(p);
+                prefetch_l2(p + 47);
+            }
+        }
+        pdl_wait();
+        pdl_trigger();
+    }
 
     for (int seg0 = i0; seg0 < i1;) {
         // the run of units of one expert
