@@ -426,6 +426,111 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
     if (scale_mag_out_of_range(scale_max)) set_status(a.status, Q2_ERR_RANGE);
 }
 
+// Gate+up for M <= 8 activation rows and no K split: the streaming arrangement of the dense
+// small-M GEMM (q2_gemm_stream_kernel) over the active experts' gate and up matrices.  One CTA of
+// kGuWarps warps per SM; all M prepared X rows are staged in shared memory once per CTA (each
+// expert's MMA columns are all of them, and only the rows routed to the expert are stored);
+// units (active expert, gate|up, 16-row group) are taken from the CTA's contiguous range by its
+// warps in turn, each streaming its units' 16 x 256 tiles through its own cp.async ring.
+// Compared with moe_stream_kernel there is no per-expert staging or barrier, and the smaller
+// register footprint leaves room for three times the warps per scheduler.
+constexpr int kGuWarps = 24;
+constexpr int kGuRing = 3;
+
+__global__ void __launch_bounds__(kGuWarps * 32, 1) moe_gateup_stream_kernel(MoeArgs a, MoeWs w) {
+    extern __shared__ __align__(16) uint32_t sm_dyn[];
+    __shared__ int s_active[256];
+    __shared__ int s_pos[256][8];  // grouped position of (active expert, X row), -1: not routed
+    __shared__ int s_rows[8], s_exps[8];
+    __shared__ int s_na;
+    pdl_wait();
+    pdl_trigger();
+    const int M = a.M, F = a.F, P = a.M * a.topk;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    if (threadIdx.x == 0) s_na = w.active[a.E];
+    for (int i = threadIdx.x; i < a.E; i += blockDim.x) {
+        s_active[i] = w.active[i];
+#pragma unroll
+        for (int c = 0; c < 8; ++c) s_pos[i][c] = -1;
+    }
+    if (threadIdx.x < 8) {
+        s_rows[threadIdx.x] = threadIdx.x < M ? (int)threadIdx.x : 0;
+        s_exps[threadIdx.x] = threadIdx.x < M ? w.prepX.exps[threadIdx.x] : 0;
+    }
+    __syncthreads();
+    const int na = s_na;
+    for (int ai = threadIdx.x; ai < na; ai += blockDim.x) {
+        const int e = s_active[ai], off = w.offsets[e], cnt = w.counts[e];
+        for (int c = 0; c < cnt; ++c) s_pos[ai][w.pair_row[off + c]] = off + c;
+    }
+    const PrepLayout L(a.H);
+    const SmemAct SA(L, M);
+    uint32_t *sm_act = sm_dyn;
+    uint32_t *ring = sm_dyn + SA.words() + (size_t)warp * kGuRing * kTileWords;
+    const size_t row_bytes = (size_t)L.nb * kBlockBytes;
+    const size_t mat_bytes = (size_t)F * row_bytes;
+    const int groups = F / kRowsPerCta, per_expert = 2 * groups;
+    const int total = na * per_expert;
+    const int q = cdiv(total, gridDim.x);
+    const int u0 = blockIdx.x * q, u1 = min(total, u0 + q);
+    auto unit_w = [&](int u) {
+        const int ai = u / per_expert, r = u - ai * per_expert;
+        const int mat = r / groups, grp = r - mat * groups;
+        return (mat ? a.Wu : a.Wg) + (size_t)s_active[ai] * mat_bytes + (size_t)grp * kRowsPerCta * row_bytes;
+    };
+    int pu = u0 + warp, ptile = 0;
+    const uint8_t *pW = nullptr;
+    __syncthreads();  // s_pos complete
+    if (pu < u1) pW = unit_w(pu);
+    auto produce = [&](int stage) {
+        if (pu < u1) {
+            issue_tile_cpasync(ring + stage * kTileWords, pW, row_bytes, ptile, lane);
+            if (++ptile == L.ntk) {
+                ptile = 0;
+                pu += kGuWarps;
+                if (pu < u1) pW = unit_w(pu);
+            }
+        }
+        cp_async_commit();  // one group per slot, empty or not, keeps the count uniform
+    };
+#pragma unroll
+    for (int sidx = 0; sidx < kGuRing - 1; ++sidx) produce(sidx);
+    stage_act_issue(sm_act, SA, w.prepX, L, s_rows, M);  // the newest group: wait for every group
+    cp_async_wait<0>();
+    __syncthreads();
+    uint32_t scale_max = 0u;  // running max of |d|, |m| (f16x2)
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    int cu = u0 + warp, ctile = 0;
+    for (int it = 0; cu < u1; ++it) {
+        produce((it + kGuRing - 1) % kGuRing);
+        cp_async_wait<kGuRing - 1>();  // this tile's group has landed
+        __syncwarp();
+        TileRegs cur;
+        read_tile_smem(cur, ring + (it % kGuRing) * kTileWords, lane);
+        compute_tile_smem(cur, sm_act, SA, M, ctile, lane, acc, scale_max);
+        if (++ctile == L.ntk) {
+            // rows g, g+8 of the unit for X rows 2t, 2t+1, stored for the rows routed here
+            const int ai = cu / per_expert, r = cu - ai * per_expert;
+            const int mat = r / groups, grp = r - mat * groups;
+            float *dst = w.h + (size_t)mat * P * F + (size_t)grp * kRowsPerCta;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                const int c = 2 * t + (qq & 1), rr = g + 8 * (qq >> 1);
+                const int pos = c < M ? s_pos[ai][c] : -1;
+                if (pos >= 0) dst[(size_t)pos * F + rr] = ldexpf(acc[0][qq] + acc[1][qq], s_exps[c]);
+                acc[0][qq] = 0.0f;
+                acc[1][qq] = 0.0f;
+            }
+            ctile = 0;
+            cu += kGuWarps;
+        }
+        __syncwarp();  // every lane has read this stage before a later copy refills it
+    }
+    cp_async_wait<0>();
+    if (scale_mag_out_of_range(scale_max)) set_status(a.status, Q2_ERR_RANGE);
+}
+
 __global__ void __launch_bounds__(256) moe_combine_kernel(MoeArgs a, MoeWs w, int KS) {
     pdl_wait();
     pdl_trigger();
@@ -488,6 +593,29 @@ cudaError_t launch_stream(const MoeArgs &a, const MoeWs &w, int KS, float *out, 
     return launch_stream_variant<GU, false>(GU ? 1 : 3, a, w, KS, out, num_sms, smem, s);
 }
 
+size_t g_gu_smem[kCacheDevices];
+
+cudaError_t launch_gateup_stream(const MoeArgs &a, const MoeWs &w, int num_sms, size_t smem, cudaStream_t s) {
+    const int dv = cache_device();
+    if (dv < 0 || g_gu_smem[dv] < smem) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(moe_gateup_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (dv >= 0) g_gu_smem[dv] = smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(kGuWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, moe_gateup_stream_kernel, a, w);
+}
+
 // K splits so that the expected number of units is a few per resident warp.  Split ks takes
 // tiles [ks * tps, min(ntk, (ks + 1) * tps)) with tps = cdiv(ntk, KS); the count is then
 // reduced to cdiv(ntk, tps) so that no split is empty (the weight ring would otherwise fetch
@@ -508,7 +636,15 @@ cudaError_t launch_moe(const MoeArgs &a, const MoeWs &w, int num_sms, cudaStream
     const int resident_warps = num_sms * 24;
     const int ks_gu = choose_ks(expect_active * 2 * cdiv(a.F, kRowsPerCta), LX.ntk, resident_warps);
     const int ks_d = choose_ks(expect_active * cdiv(a.H, kRowsPerCta), LH.ntk, resident_warps);
-    err = probed(kProbeMoeGateUp, s, [&] { return launch_stream<true>(a, w, ks_gu, w.h, num_sms, LX, s); });
+    // the streaming gate+up when it applies: at most 8 X rows, no K split, whole 16-row groups and
+    // whole K tiles, and the staged rows plus the rings fit in shared memory
+    const size_t gu_smem = SmemAct(LX, min(8, a.M)).bytes() + (size_t)kGuWarps * kGuRing * kTileWords * 4;
+    const bool gu_stream = a.M <= 8 && ks_gu == 1 && a.F % kRowsPerCta == 0 && LX.nb == LX.ntk * kTileBlocks &&
+                           LX.nb % 4 == 0 && gu_smem <= (size_t)220 * 1024;
+    err = probed(kProbeMoeGateUp, s, [&] {
+        return gu_stream ? launch_gateup_stream(a, w, num_sms, gu_smem, s)
+                         : launch_stream<true>(a, w, ks_gu, w.h, num_sms, LX, s);
+    });
     if (err != cudaSuccess) return err;
     err = launch_pdl(moe_prep_h_kernel, dim3(P), dim3(256), s, (const float *)w.h, P, a.F, ks_gu, w.prepH, LH);
     if (err != cudaSuccess) return err;
