@@ -240,11 +240,12 @@ __device__ __forceinline__ void stage_act(uint32_t *sm, const SmemAct &SA, const
 
 // acc[0] += block 2t and the offsets' hi part, acc[1] += block 2t+1 and the lo part: two
 // independent MMA chains, issued alternately.  B fragments come from the staged operand,
-// column g (column 0 when g has no row in the current slice of n columns; see SmemAct).
+// column c0 + g (column c0 when g has no row in the current slice of n columns; see SmemAct).
 __device__ __forceinline__ void compute_tile_smem(const TileRegs &r, uint32_t *sm, const SmemAct &SA, int n,
-                                                  int tile, int lane, float (&acc)[2][4], uint32_t &scale_max) {
+                                                  int tile, int lane, float (&acc)[2][4], uint32_t &scale_max,
+                                                  int c0 = 0) {
     const int g = lane >> 2, t = lane & 3;
-    const int cg = g < n ? g : 0;
+    const int cg = (g < n ? g : 0) + c0;  // staged columns c0 .. c0 + n - 1 are this MMA's 8 columns
     const uint32_t *base = SA.act(sm, cg) + (tile * 4 + t) * kPairWords;  // block pair (2t, 2t+1)
     uint32_t d2[2][2], nd[2][2];  // [block 2t | 2t+1][row g | g+8]
 #pragma unroll

@@ -433,8 +433,10 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
 // units (active expert, gate|up, 16-row group) are taken from the CTA's contiguous range by its
 // warps in turn, each streaming its units' 16 x 256 tiles through its own cp.async ring.
 // Compared with moe_stream_kernel there is no per-expert staging or barrier, and the smaller
-// register footprint leaves room for three times the warps per scheduler.
-constexpr int kGuWarps = 24;
+// register footprint (71 registers) leaves room for 3.5 times the warps per scheduler.  Measured
+// at the verifier shape (gate+up µs): 28 warps with 3-tile rings 56.3; 24 x 3: 57.8; 28 x 4: 57.9;
+// 24 x 4: 57.4; 32 x 3: 59.9; 32 x 2: 59.7; 20 x 4: 63.4; 16 x 5: 62.5; moe_stream_kernel 60.0.
+constexpr int kGuWarps = 28;
 constexpr int kGuRing = 3;
 
 __global__ void __launch_bounds__(kGuWarps * 32, 1) moe_gateup_stream_kernel(MoeArgs a, MoeWs w) {
