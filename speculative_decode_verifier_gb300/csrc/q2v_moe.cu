@@ -210,7 +210,7 @@ __global__ void __launch_bounds__(256) moe_prep_h_kernel(const float *__restrict
 //   GATEUP: matrices {Wg, Wu} [E][F][H/32], K = H; activation column c of expert e is the
 //           prepared X row pair_row[offsets[e] + c]; output gu[ks][matrix][pos][F].
 //   DOWN:   matrix Wd [E][H][F/32], K = F; activation column c is prepared h row
-//           offsets[e] + c; output out[ks][pos][H].
+//           offsets[e] + c; output out[ks][slot_of[pos]][H] (by (row, slot), for the combine).
 // Each CTA takes a contiguous range of units.  Within it, for each run of units of one
 // expert (and each slice of 8 of its rows), the CTA stages those rows' prepared
 // activations in shared memory once; its warps then take the run's units round-robin and
@@ -533,6 +533,125 @@ __global__ void __launch_bounds__(kGuWarps * 32, 1) moe_gateup_stream_kernel(Moe
     if (scale_mag_out_of_range(scale_max)) set_status(a.status, Q2_ERR_RANGE);
 }
 
+// Down for M <= 8 and no K split, on the same streaming arrangement.  Units (active expert,
+// 16-row group of H) are taken by the CTA's warps from its contiguous range; at these sizes a
+// range meets at most kDnMaxExperts experts, so the CTA stages the h rows of all of their pairs
+// (a window of consecutive grouped positions) once, and an expert's MMA columns are its pairs'
+// columns in that window.  The routing comes from two kernels back (complete before this grid
+// was launched), so the unit addresses are known and the first ring tiles are requested before
+// the programmatic wait, which only the h rows need.
+// warps per CTA: measured at the 5-row, 64-expert top-6 shape (whole verifier step, us):
+// 20 -> 121.5, 24 -> 119.0, 28 -> 120.8; the grouped kernel it replaces -> 123.5
+constexpr int kDnWarps = 24;
+constexpr int kDnRing = 3;
+constexpr int kDnMaxExperts = 2;
+
+__global__ void __launch_bounds__(kDnWarps * 32, 1) moe_down_stream_kernel(MoeArgs a, MoeWs w, int win_max) {
+    extern __shared__ __align__(16) uint32_t sm_dyn[];
+    __shared__ int s_rows[64], s_exps[64], s_slot[64];
+    __shared__ int s_pos0, s_win;
+    const int H = a.H, P = a.M * a.topk;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int g = lane >> 2, t = lane & 3;
+    const PrepLayout L(a.F);
+    const size_t row_bytes = (size_t)L.nb * kBlockBytes;
+    const size_t mat_bytes = (size_t)H * row_bytes;
+    const int groups = H / kRowsPerCta;
+    // the routing (written two kernels back), read from L2
+    const int na = __ldcg(w.active + a.E);
+    const int total = na * groups;
+    const int q = cdiv(total, gridDim.x);
+    const int u0 = blockIdx.x * q, u1 = min(total, u0 + q);
+    auto unit_expert = [&](int u) { return __ldcg(w.active + u / groups); };
+    auto unit_w = [&](int u) {
+        return a.Wd + (size_t)unit_expert(u) * mat_bytes + (size_t)(u % groups) * kRowsPerCta * row_bytes;
+    };
+    const SmemAct SA(L, win_max);
+    uint32_t *sm_act = sm_dyn;
+    uint32_t *ring = sm_dyn + SA.words() + (size_t)warp * kDnRing * kTileWords;
+    int pu = u0 + warp, ptile = 0;
+    const uint8_t *pW = pu < u1 ? unit_w(pu) : nullptr;
+    auto produce = [&](int stage) {
+        if (pu < u1) {
+            issue_tile_cpasync(ring + stage * kTileWords, pW, row_bytes, ptile, lane);
+            if (++ptile == L.ntk) {
+                ptile = 0;
+                pu += kDnWarps;
+                if (pu < u1) pW = unit_w(pu);
+            }
+        }
+        cp_async_commit();  // one group per slot, empty or not, keeps the count uniform
+    };
+#pragma unroll
+    for (int sidx = 0; sidx < kDnRing - 1; ++sidx) produce(sidx);
+    // the window of grouped positions this CTA's experts cover
+    if (threadIdx.x == 0) {
+        int pos0 = 0, win = 0;
+        if (u0 < u1) {
+            const int ai0 = u0 / groups;
+            const int ai1 = (u1 - 1) / groups;
+            const int e0 = __ldcg(w.active + ai0), e1 = __ldcg(w.active + ai1);
+            pos0 = __ldcg(w.offsets + e0);
+            win = __ldcg(w.offsets + e1) + __ldcg(w.counts + e1) - pos0;
+        }
+        s_pos0 = pos0;
+        s_win = win;
+    }
+    pdl_wait();
+    pdl_trigger();
+    __syncthreads();
+    const int pos0 = s_pos0, win = s_win;
+    if (win > win_max) {
+        // a range over more experts than the host sized the window for: refuse, no partial output
+        if (threadIdx.x == 0) set_status(a.status, Q2_ERR_UNSUPPORTED);
+        cp_async_wait<0>();
+        return;
+    }
+    if (threadIdx.x < win) {
+        s_rows[threadIdx.x] = pos0 + threadIdx.x;
+        s_exps[threadIdx.x] = w.prepH.exps[pos0 + threadIdx.x];
+        s_slot[threadIdx.x] = __ldcg(w.slot_of + pos0 + threadIdx.x);
+    }
+    __syncthreads();
+    stage_act_issue(sm_act, SA, w.prepH, L, s_rows, win);  // the newest group: wait for every group
+    cp_async_wait<0>();
+    __syncthreads();
+    uint32_t scale_max = 0u;  // running max of |d|, |m| (f16x2)
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    int cu = u0 + warp, ctile = 0;
+    int ce = cu < u1 ? unit_expert(cu) : 0;
+    int coff = cu < u1 ? __ldcg(w.offsets + ce) - pos0 : 0, ccnt = cu < u1 ? __ldcg(w.counts + ce) : 0;
+    for (int it = 0; cu < u1; ++it) {
+        produce((it + kDnRing - 1) % kDnRing);
+        cp_async_wait<kDnRing - 1>();  // this tile's group has landed
+        __syncwarp();
+        TileRegs cur;
+        read_tile_smem(cur, ring + (it % kDnRing) * kTileWords, lane);
+        compute_tile_smem(cur, sm_act, SA, ccnt, ctile, lane, acc, scale_max, coff);
+        if (++ctile == L.ntk) {
+            // rows g, g+8 of the unit for the expert's pairs 2t, 2t+1, stored by (row, slot)
+            float *dst = w.out + (size_t)(cu % groups) * kRowsPerCta;
+#pragma unroll
+            for (int qq = 0; qq < 4; ++qq) {
+                const int c = 2 * t + (qq & 1), rr = g + 8 * (qq >> 1);
+                if (c < ccnt) dst[(size_t)s_slot[coff + c] * H + rr] = ldexpf(acc[0][qq] + acc[1][qq], s_exps[coff + c]);
+                acc[0][qq] = 0.0f;
+                acc[1][qq] = 0.0f;
+            }
+            ctile = 0;
+            cu += kDnWarps;
+            if (cu < u1) {
+                ce = unit_expert(cu);
+                coff = __ldcg(w.offsets + ce) - pos0;
+                ccnt = __ldcg(w.counts + ce);
+            }
+        }
+        __syncwarp();  // every lane has read this stage before a later copy refills it
+    }
+    cp_async_wait<0>();
+    if (scale_mag_out_of_range(scale_max)) set_status(a.status, Q2_ERR_RANGE);
+}
+
 __global__ void __launch_bounds__(256) moe_combine_kernel(MoeArgs a, MoeWs w, int KS) {
     pdl_wait();
     pdl_trigger();
@@ -618,6 +737,30 @@ cudaError_t launch_gateup_stream(const MoeArgs &a, const MoeWs &w, int num_sms, 
     return cudaLaunchKernelEx(&cfg, moe_gateup_stream_kernel, a, w);
 }
 
+size_t g_dn_smem[kCacheDevices];
+
+cudaError_t launch_down_stream(const MoeArgs &a, const MoeWs &w, int num_sms, int win_max, size_t smem,
+                               cudaStream_t s) {
+    const int dv = cache_device();
+    if (dv < 0 || g_dn_smem[dv] < smem) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(moe_down_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        if (e != cudaSuccess) return e;
+        if (dv >= 0) g_dn_smem[dv] = smem;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(num_sms);
+    cfg.blockDim = dim3(kDnWarps * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, moe_down_stream_kernel, a, w, win_max);
+}
+
 // K splits so that the expected number of units is a few per resident warp.  Split ks takes
 // tiles [ks * tps, min(ntk, (ks + 1) * tps)) with tps = cdiv(ntk, KS); the count is then
 // reduced to cdiv(ntk, tps) so that no split is empty (the weight ring would otherwise fetch
@@ -650,7 +793,20 @@ cudaError_t launch_moe(const MoeArgs &a, const MoeWs &w, int num_sms, cudaStream
     if (err != cudaSuccess) return err;
     err = launch_pdl(moe_prep_h_kernel, dim3(P), dim3(256), s, (const float *)w.h, P, a.F, ks_gu, w.prepH, LH);
     if (err != cudaSuccess) return err;
-    err = probed(kProbeMoeDown, s, [&] { return launch_stream<false>(a, w, ks_d, w.out, num_sms, LH, s); });
+    // the streaming down GEMM when it applies: at most 8 X rows, no K split, whole groups and tiles,
+    // every CTA's unit range within kDnMaxExperts experts (its staged window then holds at most
+    // kDnMaxExperts x M pairs), and the window plus the rings fit in shared memory
+    const int dn_units_max = expect_active * cdiv(a.H, kRowsPerCta);
+    const int dn_q = cdiv(dn_units_max, num_sms);
+    const int dn_win = min(P, kDnMaxExperts * a.M);
+    const size_t dn_smem = SmemAct(LH, dn_win).bytes() + (size_t)kDnWarps * kDnRing * kTileWords * 4;
+    const bool dn_stream = a.M <= 8 && ks_d == 1 && a.H % kRowsPerCta == 0 && LH.nb == LH.ntk * kTileBlocks &&
+                           LH.nb % 4 == 0 && dn_q <= cdiv(a.H, kRowsPerCta) && dn_win <= 64 &&
+                           dn_smem <= (size_t)220 * 1024;
+    err = probed(kProbeMoeDown, s, [&] {
+        return dn_stream ? launch_down_stream(a, w, num_sms, dn_win, dn_smem, s)
+                         : launch_stream<false>(a, w, ks_d, w.out, num_sms, LH, s);
+    });
     if (err != cudaSuccess) return err;
     return launch_pdl(moe_combine_kernel, dim3(max(1, min(cdiv(a.M * a.H, 256), 4 * num_sms))), dim3(256), s, a,
                       w, ks_d);
