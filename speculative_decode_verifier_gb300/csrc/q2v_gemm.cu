@@ -88,16 +88,17 @@ __global__ void __launch_bounds__(kGemmWarps * 32) q2_gemm_mma_kernel(const uint
 }
 
 // Small M (<= 8) against many weight rows: a persistent grid (one CTA of 24 warps per SM), the
-// prepared activation rows staged in shared memory once per CTA, and 16-row units (all of K)
-// taken by the CTA's warps from its contiguous range of units, each warp streaming its units'
+// prepared activation rows staged in shared memory once per CTA, and the CTA's contiguous range
+// of 16-row units (all of K) split evenly over its warps by tiles, each warp streaming its
 // 16 x 256 weight tiles through its own 3-deep cp.async ring and decoding them with the same
-// exact mma.sync tile decode (the MoE stream kernel's arrangement, for one matrix).  Measured
-// on the M=5 x 129,280 x 4,096 head: 60.5 us with 24 warps and 3-tile rings, 62.8 with 16 warps
-// and 4-tile rings, 64.1 with two CTAs of 8 warps and 4-tile rings.  The first
-// ring tiles are requested before the programmatic wait (the weights do not depend on the
+// exact mma.sync tile decode (the MoE stream kernels' arrangement, for one matrix).  Measured on
+// the M=5 x 129,280 x 4,096 head (head GEMM + verify, us): even split 77.0, strided units 80.2;
+// with strided units, 16 warps and 4-tile rings or two CTAs of 8 warps were slower still.  The
+// first ring tiles are requested before the programmatic wait (the weights do not depend on the
 // previous kernel); the staged activations after it.  Requires K % 256 == 0 and N % 16 == 0.
 constexpr int kStreamRing = 3;
 constexpr int kStreamWarps = 24;
+constexpr bool kStreamEven = true;
 
 __global__ void __launch_bounds__(kStreamWarps * 32, 1)
     q2_gemm_stream_kernel(const uint8_t *__restrict__ W, int N, int K, PrepPtrs P, PrepLayout L, int M,
@@ -113,21 +114,12 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
     const int units = N / kRowsPerCta;
     const int q = cdiv(units, gridDim.x);
     const int u0 = blockIdx.x * q, u1 = min(units, u0 + q);
-    // producer cursor: this warp's units u0 + warp, + kStreamWarps, ..., tiles 0 .. ntk-1 each
-    int pu = u0 + warp, ptile = 0;
-    auto produce = [&](int stage) {
-        if (pu < u1) {
-            issue_tile_cpasync(ring + stage * kTileWords, W + (size_t)pu * kRowsPerCta * row_bytes, row_bytes, ptile,
-                               lane);
-            if (++ptile == L.ntk) {
-                ptile = 0;
-                pu += kStreamWarps;
-            }
-        }
-        cp_async_commit();  // one group per slot, empty or not, keeps the count uniform
-    };
+    auto unit_w = [&](int u) { return W + (size_t)u * kRowsPerCta * row_bytes; };
+    TileCursor<kStreamEven, decltype(unit_w)> pc;
+    pc.begin(u0, u1, L.ntk, kStreamWarps, warp, unit_w);
 #pragma unroll
-    for (int sidx = 0; sidx < kStreamRing - 1; ++sidx) produce(sidx);
+    for (int sidx = 0; sidx < kStreamRing - 1; ++sidx)
+        pc.produce(ring + sidx * kTileWords, row_bytes, L.ntk, kStreamWarps, lane, unit_w);
     pdl_wait();
     pdl_trigger();
     if (threadIdx.x < 8) {
@@ -139,35 +131,23 @@ __global__ void __launch_bounds__(kStreamWarps * 32, 1)
     cp_async_wait<0>();
     __syncthreads();
     uint32_t scale_max = 0u;  // running max of |d|, |m| (f16x2)
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    int cu = u0 + warp, ctile = 0;
-    for (int it = 0; cu < u1; ++it) {
-        produce((it + kStreamRing - 1) % kStreamRing);
-        cp_async_wait<kStreamRing - 1>();  // this tile's group has landed
-        __syncwarp();
-        TileRegs cur;
-        read_tile_smem(cur, ring + (it % kStreamRing) * kTileWords, lane);
-        compute_tile_smem(cur, sm_act, SA, M, ctile, lane, acc, scale_max);
-        if (++ctile == L.ntk) {
-            // rows g, g+8 of the unit, activation rows 2t, 2t+1
+    auto cols = [&](int) { return make_int2(M, 0); };
+    // rows g, g+8 of the unit, activation rows 2t, 2t+1
+    auto store = [&](int u, int2, const float *v) {
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                const int m = 2 * t + (qq & 1), n = cu * kRowsPerCta + g + 8 * (qq >> 1);
-                if (m < M) Y[(size_t)m * ldy + n] = ldexpf(acc[0][qq] + acc[1][qq], s_exps[m]);
-                acc[0][qq] = 0.0f;
-                acc[1][qq] = 0.0f;
-            }
-            ctile = 0;
-            cu += kStreamWarps;
+        for (int qq = 0; qq < 4; ++qq) {
+            const int m = 2 * t + (qq & 1), n = u * kRowsPerCta + g + 8 * (qq >> 1);
+            if (m < M) Y[(size_t)m * ldy + n] = ldexpf(v[qq], s_exps[m]);
         }
-        __syncwarp();  // every lane has read this stage before a later copy refills it
-    }
-    cp_async_wait<0>();
+    };
+    float *part = reinterpret_cast<float *>(sm_dyn + SA.words() + (size_t)kStreamWarps * kStreamRing * kTileWords);
+    stream_warp_tiles<kStreamRing, kStreamEven>(pc, ring, sm_act, SA, part, u0, u1, L.ntk, row_bytes, kStreamWarps, warp, lane,
+                                   unit_w, cols, store, scale_max);
     if (scale_mag_out_of_range(scale_max)) set_status(status, Q2_ERR_RANGE);
 }
 
 size_t stream_smem_bytes(int M, int K) {
-    return SmemAct(PrepLayout(K), M).bytes() + (size_t)kStreamWarps * kStreamRing * kTileWords * 4;
+    return SmemAct(PrepLayout(K), M).bytes() + (size_t)kStreamWarps * (kStreamRing * kTileWords + 128) * 4;
 }
 
 bool stream_gemm_usable(int M, int N, int K) {

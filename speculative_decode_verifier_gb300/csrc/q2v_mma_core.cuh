@@ -378,4 +378,138 @@ __device__ __forceinline__ void prep_row_bf16(const uint16_t *__restrict__ src, 
                          reinterpret_cast<__half *>(P.slo + (size_t)r * L.sum_words_per_row()), b);
 }
 
+// ---------------------------------------------------------------- streamed units
+//
+// The streaming kernels give each CTA a contiguous range of units [u0, u1) (16 weight rows of
+// one matrix, ntk tiles each), and each warp streams its units' tiles through its own ring.
+// Two ways to share the range among the CTA's nw warps:
+//   strided (EVEN = false): warp w takes units u0 + w, u0 + w + nw, ...;
+//   even (EVEN = true): the range is flattened to tiles f = (u - u0) * ntk + tile and cut into
+//     nw contiguous warp ranges whose lengths differ by at most one tile, so no warp has a whole
+//     unit more to stream than another.  A unit cut between warps is finished by the warp that
+//     began it: each later warp holding a piece of it leaves that piece's 16 x 8 partial sum in
+//     shared memory (its first piece, one slot per warp), and after one barrier the first warp
+//     adds them in warp order, so the result does not depend on timing.
+struct WarpTiles {
+    int f0, f1;
+};
+__device__ __forceinline__ WarpTiles warp_tiles(int u0, int u1, int ntk, int nw, int w) {
+    const long long T = (long long)(u1 - u0) * ntk;
+    return {(int)(T * w / nw), (int)(T * (w + 1) / nw)};
+}
+
+// A warp's first unit, first tile and tile count under either split.
+template <bool EVEN>
+__device__ __forceinline__ void warp_start(int u0, int u1, int ntk, int nw, int w, int &u, int &tile, int &n) {
+    if (EVEN) {
+        const WarpTiles r = warp_tiles(u0, u1, ntk, nw, w);
+        u = u0 + r.f0 / ntk;
+        tile = r.f0 - (u - u0) * ntk;
+        n = r.f1 - r.f0;
+    } else {
+        u = u0 + w;
+        tile = 0;
+        n = u < u1 ? cdiv(u1 - u, nw) * ntk : 0;
+    }
+}
+
+// Producer cursor over a warp's tiles: one cp.async group per call, empty once the warp's tiles
+// are exhausted (the group count stays uniform).  unit_w(u) is the first weight row of unit u.
+template <bool EVEN, class UnitW>
+struct TileCursor {
+    const uint8_t *W;
+    int u, tile, left;
+    __device__ __forceinline__ void begin(int u0, int u1, int ntk, int nw, int warp, const UnitW &unit_w) {
+        warp_start<EVEN>(u0, u1, ntk, nw, warp, u, tile, left);
+        W = left > 0 ? unit_w(u) : nullptr;
+    }
+    __device__ __forceinline__ void produce(uint32_t *stage, size_t row_bytes, int ntk, int nw, int lane,
+                                            const UnitW &unit_w) {
+        if (left > 0) {
+            issue_tile_cpasync(stage, W, row_bytes, tile, lane);
+            --left;
+            if (++tile == ntk) {
+                tile = 0;
+                u += EVEN ? 1 : nw;
+                if (left > 0) W = unit_w(u);
+            }
+        }
+        cp_async_commit();
+    }
+};
+
+// Consume a warp's tiles through its RING-stage ring (the caller has issued RING - 1 groups
+// with `cur` and waited for the staged activations).  cols(u) gives unit u's MMA columns
+// {n, c0} (columns c0 .. c0 + n - 1 of the staged activations); store(u, nc, v) writes the
+// unit's result, nc = cols(u), v[q] the sum for rows g + 8 (q >> 1), column 2t + (q & 1).
+// EVEN: part is nw x 128 floats of shared memory, and every thread of the CTA calls this (it
+// holds one barrier); a unit cut at the range's start is recognised by its index, a cut at the
+// end after the loop, so the loop carries no more state than the strided one.
+template <int RING, bool EVEN, class UnitW, class Cols, class Store>
+__device__ __forceinline__ void stream_warp_tiles(TileCursor<EVEN, UnitW> &cur, uint32_t *ring, uint32_t *sm_act,
+                                                  const SmemAct &SA, float *part, int u0, int u1, int ntk,
+                                                  size_t row_bytes, int nw, int warp, int lane, const UnitW &unit_w,
+                                                  const Cols &cols, const Store &store, uint32_t &scale_max) {
+    int cu, ctile, n;
+    warp_start<EVEN>(u0, u1, ntk, nw, warp, cu, ctile, n);
+    const int head_u = EVEN && ctile != 0 ? cu : -1;  // begun by an earlier warp
+    int2 nc = n > 0 ? cols(cu) : make_int2(0, 0);
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    auto finish = [&](bool keep) {
+        float v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            v[q] = acc[0][q] + acc[1][q];
+            acc[0][q] = 0.0f;
+            acc[1][q] = 0.0f;
+        }
+        if (EVEN && cu == head_u)
+            *reinterpret_cast<float4 *>(part + warp * 128 + lane * 4) = make_float4(v[0], v[1], v[2], v[3]);
+        else if (!keep)
+            store(cu, nc, v);
+    };
+    int pst = RING - 1, cst = 0;  // producer and consumer ring stages
+    for (int it = 0; it < n; ++it) {
+        cur.produce(ring + pst * kTileWords, row_bytes, ntk, nw, lane, unit_w);
+        pst = pst == RING - 1 ? 0 : pst + 1;
+        cp_async_wait<RING - 1>();  // this tile's group has landed
+        __syncwarp();
+        TileRegs tr;
+        read_tile_smem(tr, ring + cst * kTileWords, lane);
+        cst = cst == RING - 1 ? 0 : cst + 1;
+        compute_tile_smem(tr, sm_act, SA, nc.x, ctile, lane, acc, scale_max, nc.y);
+        if (++ctile == ntk) {
+            finish(false);
+            ctile = 0;
+            cu += EVEN ? 1 : nw;
+            if (it + 1 < n) nc = cols(cu);
+        }
+        __syncwarp();  // every lane has read this stage before a later copy refills it
+    }
+    cp_async_wait<0>();
+    if (!EVEN) return;
+    // the range ends inside unit cu: its piece is a later warp's part, or this warp began it
+    const bool tail = ctile != 0 && cu != head_u;
+    if (ctile != 0 && cu == head_u) finish(true);
+    __syncthreads();  // every piece of a cut unit is in shared memory
+    if (tail) {
+        float v[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) v[q] = acc[0][q] + acc[1][q];
+        const int fend = (cu + 1 - u0) * ntk;  // first tile after the unit
+        for (int w2 = warp + 1; w2 < nw; ++w2) {
+            const WarpTiles r2 = warp_tiles(u0, u1, ntk, nw, w2);
+            if (r2.f0 >= fend) break;
+            if (r2.f1 > r2.f0) {
+                const float4 p = *reinterpret_cast<const float4 *>(part + w2 * 128 + lane * 4);
+                v[0] += p.x;
+                v[1] += p.y;
+                v[2] += p.z;
+                v[3] += p.w;
+            }
+        }
+        store(cu, nc, v);
+    }
+}
+
 }  // namespace q2v

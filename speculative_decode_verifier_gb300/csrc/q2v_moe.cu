@@ -430,14 +430,16 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
 // small-M GEMM (q2_gemm_stream_kernel) over the active experts' gate and up matrices.  One CTA of
 // kGuWarps warps per SM; all M prepared X rows are staged in shared memory once per CTA (each
 // expert's MMA columns are all of them, and only the rows routed to the expert are stored);
-// units (active expert, gate|up, 16-row group) are taken from the CTA's contiguous range by its
-// warps in turn, each streaming its units' 16 x 256 tiles through its own cp.async ring.
+// the CTA's contiguous range of units (active expert, gate|up, 16-row group) is split evenly
+// over its warps by tiles, each warp streaming its 16 x 256 tiles through its own cp.async ring.
 // Compared with moe_stream_kernel there is no per-expert staging or barrier, and the smaller
-// register footprint (71 registers) leaves room for 3.5 times the warps per scheduler.  Measured
-// at the verifier shape (gate+up µs): 28 warps with 3-tile rings 56.3; 24 x 3: 57.8; 28 x 4: 57.9;
-// 24 x 4: 57.4; 32 x 3: 59.9; 32 x 2: 59.7; 20 x 4: 63.4; 16 x 5: 62.5; moe_stream_kernel 60.0.
-constexpr int kGuWarps = 28;
+// register footprint leaves room for three times the warps per scheduler.  Measured at the
+// verifier shape (gate+up µs): even split, 24 warps, 3-tile rings: 56.4; even, 28 warps (at the
+// register limit, spilling): 64.3; even, 20 warps: 59.4; strided units, 28 x 3: 56.3 (24 x 3:
+// 57.8, 28 x 4: 57.9, 32 x 3: 59.9, 16 x 5: 62.5); moe_stream_kernel 60.0.
+constexpr int kGuWarps = 24;
 constexpr int kGuRing = 3;
+constexpr bool kGuEven = true;
 
 __global__ void __launch_bounds__(kGuWarps * 32, 1) moe_gateup_stream_kernel(MoeArgs a, MoeWs w) {
     extern __shared__ __align__(16) uint32_t sm_dyn[];
@@ -481,55 +483,32 @@ __global__ void __launch_bounds__(kGuWarps * 32, 1) moe_gateup_stream_kernel(Moe
         const int mat = r / groups, grp = r - mat * groups;
         return (mat ? a.Wu : a.Wg) + (size_t)s_active[ai] * mat_bytes + (size_t)grp * kRowsPerCta * row_bytes;
     };
-    int pu = u0 + warp, ptile = 0;
-    const uint8_t *pW = nullptr;
+    TileCursor<kGuEven, decltype(unit_w)> pc;
     __syncthreads();  // s_pos complete
-    if (pu < u1) pW = unit_w(pu);
-    auto produce = [&](int stage) {
-        if (pu < u1) {
-            issue_tile_cpasync(ring + stage * kTileWords, pW, row_bytes, ptile, lane);
-            if (++ptile == L.ntk) {
-                ptile = 0;
-                pu += kGuWarps;
-                if (pu < u1) pW = unit_w(pu);
-            }
-        }
-        cp_async_commit();  // one group per slot, empty or not, keeps the count uniform
-    };
+    pc.begin(u0, u1, L.ntk, kGuWarps, warp, unit_w);
 #pragma unroll
-    for (int sidx = 0; sidx < kGuRing - 1; ++sidx) produce(sidx);
+    for (int sidx = 0; sidx < kGuRing - 1; ++sidx)
+        pc.produce(ring + sidx * kTileWords, row_bytes, L.ntk, kGuWarps, lane, unit_w);
     stage_act_issue(sm_act, SA, w.prepX, L, s_rows, M);  // the newest group: wait for every group
     cp_async_wait<0>();
     __syncthreads();
     uint32_t scale_max = 0u;  // running max of |d|, |m| (f16x2)
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    int cu = u0 + warp, ctile = 0;
-    for (int it = 0; cu < u1; ++it) {
-        produce((it + kGuRing - 1) % kGuRing);
-        cp_async_wait<kGuRing - 1>();  // this tile's group has landed
-        __syncwarp();
-        TileRegs cur;
-        read_tile_smem(cur, ring + (it % kGuRing) * kTileWords, lane);
-        compute_tile_smem(cur, sm_act, SA, M, ctile, lane, acc, scale_max);
-        if (++ctile == L.ntk) {
-            // rows g, g+8 of the unit for X rows 2t, 2t+1, stored for the rows routed here
-            const int ai = cu / per_expert, r = cu - ai * per_expert;
-            const int mat = r / groups, grp = r - mat * groups;
-            float *dst = w.h + (size_t)mat * P * F + (size_t)grp * kRowsPerCta;
+    auto cols = [&](int) { return make_int2(M, 0); };
+    // rows g, g+8 of the unit for X rows 2t, 2t+1, stored for the rows routed to the expert
+    auto store = [&](int u, int2, const float *v) {
+        const int ai = u / per_expert, r = u - ai * per_expert;
+        const int mat = r / groups, grp = r - mat * groups;
+        float *dst = w.h + (size_t)mat * P * F + (size_t)grp * kRowsPerCta;
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                const int c = 2 * t + (qq & 1), rr = g + 8 * (qq >> 1);
-                const int pos = c < M ? s_pos[ai][c] : -1;
-                if (pos >= 0) dst[(size_t)pos * F + rr] = ldexpf(acc[0][qq] + acc[1][qq], s_exps[c]);
-                acc[0][qq] = 0.0f;
-                acc[1][qq] = 0.0f;
-            }
-            ctile = 0;
-            cu += kGuWarps;
+        for (int qq = 0; qq < 4; ++qq) {
+            const int c = 2 * t + (qq & 1), rr = g + 8 * (qq >> 1);
+            const int pos = c < M ? s_pos[ai][c] : -1;
+            if (pos >= 0) dst[(size_t)pos * F + rr] = ldexpf(v[qq], s_exps[c]);
         }
-        __syncwarp();  // every lane has read this stage before a later copy refills it
-    }
-    cp_async_wait<0>();
+    };
+    float *part = reinterpret_cast<float *>(sm_dyn + SA.words() + (size_t)kGuWarps * kGuRing * kTileWords);
+    stream_warp_tiles<kGuRing, kGuEven>(pc, ring, sm_act, SA, part, u0, u1, L.ntk, row_bytes, kGuWarps, warp, lane, unit_w,
+                               cols, store, scale_max);
     if (scale_mag_out_of_range(scale_max)) set_status(a.status, Q2_ERR_RANGE);
 }
 
@@ -540,17 +519,22 @@ __global__ void __launch_bounds__(kGuWarps * 32, 1) moe_gateup_stream_kernel(Moe
 // columns in that window.  The routing comes from two kernels back (complete before this grid
 // was launched), so the unit addresses are known and the first ring tiles are requested before
 // the programmatic wait, which only the h rows need.
-// warps per CTA: measured at the 5-row, 64-expert top-6 shape (whole verifier step, us):
-// 20 -> 121.5, 24 -> 119.0, 28 -> 120.8; the grouped kernel it replaces -> 123.5
+// Measured at the 5-row, 64-expert top-6 shape (whole verifier step, us): 20 warps -> 121.5,
+// 24 -> 119.0, 28 -> 120.8; the grouped kernel it replaces -> 123.5.  Down kernel alone: strided
+// units 34.5 us, the even split 38.8 (a 16-row unit here is only 8 tiles, so most units would be
+// cut between warps).
 constexpr int kDnWarps = 24;
+constexpr bool kDnEven = false;
 constexpr int kDnRing = 3;
 constexpr int kDnMaxExperts = 2;
 
 __global__ void __launch_bounds__(kDnWarps * 32, 1) moe_down_stream_kernel(MoeArgs a, MoeWs w, int win_max) {
     extern __shared__ __align__(16) uint32_t sm_dyn[];
     __shared__ int s_rows[64], s_exps[64], s_slot[64];
-    __shared__ int s_pos0, s_win;
-    const int H = a.H, P = a.M * a.topk;
+    // the CTA's experts (at most kDnMaxExperts): id, pair count, first column in the window
+    __shared__ int s_e[kDnMaxExperts], s_cnt[kDnMaxExperts], s_col[kDnMaxExperts];
+    __shared__ int s_ai0, s_pos0, s_win;
+    const int H = a.H;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int g = lane >> 2, t = lane & 3;
     const PrepLayout L(a.F);
@@ -562,51 +546,50 @@ __global__ void __launch_bounds__(kDnWarps * 32, 1) moe_down_stream_kernel(MoeAr
     const int total = na * groups;
     const int q = cdiv(total, gridDim.x);
     const int u0 = blockIdx.x * q, u1 = min(total, u0 + q);
-    auto unit_expert = [&](int u) { return __ldcg(w.active + u / groups); };
+    if (threadIdx.x == 0) {
+        int ai0 = 0, pos0 = 0, win = 0;
+        if (u0 < u1) {
+            ai0 = u0 / groups;
+            const int ai1 = (u1 - 1) / groups;
+            pos0 = __ldcg(w.offsets + __ldcg(w.active + ai0));
+            for (int j = 0; j < kDnMaxExperts; ++j) {
+                const int e = ai0 + j <= ai1 ? __ldcg(w.active + ai0 + j) : 0;
+                s_e[j] = e;
+                s_cnt[j] = ai0 + j <= ai1 ? __ldcg(w.counts + e) : 0;
+                s_col[j] = __ldcg(w.offsets + e) - pos0;
+                if (ai0 + j <= ai1) win = s_col[j] + s_cnt[j];
+            }
+            // a range over more experts than the window holds is refused below
+            if (ai1 - ai0 >= kDnMaxExperts) win = win_max + 1;
+        }
+        s_ai0 = ai0;
+        s_pos0 = pos0;
+        s_win = win;
+    }
+    __syncthreads();
+    const int ai0 = s_ai0;
     auto unit_w = [&](int u) {
-        return a.Wd + (size_t)unit_expert(u) * mat_bytes + (size_t)(u % groups) * kRowsPerCta * row_bytes;
+        const int j = min(u / groups - ai0, kDnMaxExperts - 1);
+        return a.Wd + (size_t)s_e[j] * mat_bytes + (size_t)(u % groups) * kRowsPerCta * row_bytes;
     };
     const SmemAct SA(L, win_max);
     uint32_t *sm_act = sm_dyn;
     uint32_t *ring = sm_dyn + SA.words() + (size_t)warp * kDnRing * kTileWords;
-    int pu = u0 + warp, ptile = 0;
-    const uint8_t *pW = pu < u1 ? unit_w(pu) : nullptr;
-    auto produce = [&](int stage) {
-        if (pu < u1) {
-            issue_tile_cpasync(ring + stage * kTileWords, pW, row_bytes, ptile, lane);
-            if (++ptile == L.ntk) {
-                ptile = 0;
-                pu += kDnWarps;
-                if (pu < u1) pW = unit_w(pu);
-            }
-        }
-        cp_async_commit();  // one group per slot, empty or not, keeps the count uniform
-    };
-#pragma unroll
-    for (int sidx = 0; sidx < kDnRing - 1; ++sidx) produce(sidx);
-    // the window of grouped positions this CTA's experts cover
-    if (threadIdx.x == 0) {
-        int pos0 = 0, win = 0;
-        if (u0 < u1) {
-            const int ai0 = u0 / groups;
-            const int ai1 = (u1 - 1) / groups;
-            const int e0 = __ldcg(w.active + ai0), e1 = __ldcg(w.active + ai1);
-            pos0 = __ldcg(w.offsets + e0);
-            win = __ldcg(w.offsets + e1) + __ldcg(w.counts + e1) - pos0;
-        }
-        s_pos0 = pos0;
-        s_win = win;
-    }
-    pdl_wait();
-    pdl_trigger();
-    __syncthreads();
     const int pos0 = s_pos0, win = s_win;
     if (win > win_max) {
         // a range over more experts than the host sized the window for: refuse, no partial output
         if (threadIdx.x == 0) set_status(a.status, Q2_ERR_UNSUPPORTED);
-        cp_async_wait<0>();
+        pdl_wait();
+        pdl_trigger();
         return;
     }
+    TileCursor<kDnEven, decltype(unit_w)> pc;
+    pc.begin(u0, u1, L.ntk, kDnWarps, warp, unit_w);
+#pragma unroll
+    for (int sidx = 0; sidx < kDnRing - 1; ++sidx)
+        pc.produce(ring + sidx * kTileWords, row_bytes, L.ntk, kDnWarps, lane, unit_w);
+    pdl_wait();
+    pdl_trigger();
     if (threadIdx.x < win) {
         s_rows[threadIdx.x] = pos0 + threadIdx.x;
         s_exps[threadIdx.x] = w.prepH.exps[pos0 + threadIdx.x];
@@ -617,38 +600,23 @@ __global__ void __launch_bounds__(kDnWarps * 32, 1) moe_down_stream_kernel(MoeAr
     cp_async_wait<0>();
     __syncthreads();
     uint32_t scale_max = 0u;  // running max of |d|, |m| (f16x2)
-    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    int cu = u0 + warp, ctile = 0;
-    int ce = cu < u1 ? unit_expert(cu) : 0;
-    int coff = cu < u1 ? __ldcg(w.offsets + ce) - pos0 : 0, ccnt = cu < u1 ? __ldcg(w.counts + ce) : 0;
-    for (int it = 0; cu < u1; ++it) {
-        produce((it + kDnRing - 1) % kDnRing);
-        cp_async_wait<kDnRing - 1>();  // this tile's group has landed
-        __syncwarp();
-        TileRegs cur;
-        read_tile_smem(cur, ring + (it % kDnRing) * kTileWords, lane);
-        compute_tile_smem(cur, sm_act, SA, ccnt, ctile, lane, acc, scale_max, coff);
-        if (++ctile == L.ntk) {
-            // rows g, g+8 of the unit for the expert's pairs 2t, 2t+1, stored by (row, slot)
-            float *dst = w.out + (size_t)(cu % groups) * kRowsPerCta;
+    // an expert's MMA columns: its pairs' columns in the staged window
+    auto cols = [&](int u) {
+        const int j = min(u / groups - ai0, kDnMaxExperts - 1);
+        return make_int2(s_cnt[j], s_col[j]);
+    };
+    // rows g, g+8 of the unit for the expert's pairs 2t, 2t+1, stored by (row, slot)
+    auto store = [&](int u, int2 nc, const float *v) {
+        float *dst = w.out + (size_t)(u % groups) * kRowsPerCta;
 #pragma unroll
-            for (int qq = 0; qq < 4; ++qq) {
-                const int c = 2 * t + (qq & 1), rr = g + 8 * (qq >> 1);
-                if (c < ccnt) dst[(size_t)s_slot[coff + c] * H + rr] = ldexpf(acc[0][qq] + acc[1][qq], s_exps[coff + c]);
-                acc[0][qq] = 0.0f;
-                acc[1][qq] = 0.0f;
-            }
-            ctile = 0;
-            cu += kDnWarps;
-            if (cu < u1) {
-                ce = unit_expert(cu);
-                coff = __ldcg(w.offsets + ce) - pos0;
-                ccnt = __ldcg(w.counts + ce);
-            }
+        for (int qq = 0; qq < 4; ++qq) {
+            const int c = 2 * t + (qq & 1), rr = g + 8 * (qq >> 1);
+            if (c < nc.x) dst[(size_t)s_slot[nc.y + c] * H + rr] = ldexpf(v[qq], s_exps[nc.y + c]);
         }
-        __syncwarp();  // every lane has read this stage before a later copy refills it
-    }
-    cp_async_wait<0>();
+    };
+    float *part = reinterpret_cast<float *>(sm_dyn + SA.words() + (size_t)kDnWarps * kDnRing * kTileWords);
+    stream_warp_tiles<kDnRing, kDnEven>(pc, ring, sm_act, SA, part, u0, u1, L.ntk, row_bytes, kDnWarps, warp, lane,
+                                        unit_w, cols, store, scale_max);
     if (scale_mag_out_of_range(scale_max)) set_status(a.status, Q2_ERR_RANGE);
 }
 
@@ -783,7 +751,7 @@ cudaError_t launch_moe(const MoeArgs &a, const MoeWs &w, int num_sms, cudaStream
     const int ks_d = choose_ks(expect_active * cdiv(a.H, kRowsPerCta), LH.ntk, resident_warps);
     // the streaming gate+up when it applies: at most 8 X rows, no K split, whole 16-row groups and
     // whole K tiles, and the staged rows plus the rings fit in shared memory
-    const size_t gu_smem = SmemAct(LX, min(8, a.M)).bytes() + (size_t)kGuWarps * kGuRing * kTileWords * 4;
+    const size_t gu_smem = SmemAct(LX, min(8, a.M)).bytes() + (size_t)kGuWarps * (kGuRing * kTileWords + 128) * 4;
     const bool gu_stream = a.M <= 8 && ks_gu == 1 && a.F % kRowsPerCta == 0 && LX.nb == LX.ntk * kTileBlocks &&
                            LX.nb % 4 == 0 && gu_smem <= (size_t)220 * 1024;
     err = probed(kProbeMoeGateUp, s, [&] {
@@ -799,7 +767,7 @@ cudaError_t launch_moe(const MoeArgs &a, const MoeWs &w, int num_sms, cudaStream
     const int dn_units_max = expect_active * cdiv(a.H, kRowsPerCta);
     const int dn_q = cdiv(dn_units_max, num_sms);
     const int dn_win = min(P, kDnMaxExperts * a.M);
-    const size_t dn_smem = SmemAct(LH, dn_win).bytes() + (size_t)kDnWarps * kDnRing * kTileWords * 4;
+    const size_t dn_smem = SmemAct(LH, dn_win).bytes() + (size_t)kDnWarps * (kDnRing * kTileWords + 128) * 4;
     const bool dn_stream = a.M <= 8 && ks_d == 1 && a.H % kRowsPerCta == 0 && LH.nb == LH.ntk * kTileBlocks &&
                            LH.nb % 4 == 0 && dn_q <= cdiv(a.H, kRowsPerCta) && dn_win <= 64 &&
                            dn_smem <= (size_t)220 * 1024;
