@@ -48,9 +48,10 @@ EXPERT_BYTES = 3 * 2048 * (4096 // 32) * 12   # gate + up + down of one expert
 
 
 def _kernel_source_digest() -> str:
-    """sha256 (first 16 hex digits) of the source the gate+up stream kernel is built from: the
-    shared device headers and the kernel's own definition.  The traffic figure recorded with the
-    ncu summaries is only reported while this digest still matches the one recorded with it."""
+    """sha256 (first 16 hex digits) of the source the streaming gate+up kernel is built from: the
+    shared device headers and the kernel's own definition (with its warp and ring constants).  The
+    traffic figure recorded with the ncu summaries is only reported while this digest still
+    matches the one recorded with it."""
     import hashlib
     import re
     csrc = os.path.join(ROOT, "speculative_decode_verifier_gb300", "csrc")
@@ -60,7 +61,7 @@ def _kernel_source_digest() -> str:
             h.update(f.read())
     with open(os.path.join(csrc, "q2v_moe.cu")) as f:
         text = f.read()
-    m = re.search(r"^struct UnitInfo.*?^__global__[^\n]*moe_stream_kernel.*?^}\n", text, re.S | re.M)
+    m = re.search(r"^constexpr int kGuWarps.*?^__global__[^\n]*moe_gateup_stream_kernel.*?^}\n", text, re.S | re.M)
     h.update((m.group(0) if m else text).encode())
     return h.hexdigest()[:16]
 
@@ -698,7 +699,7 @@ def run_device(args, rank: int, world: int):
         "pq_verify_rows_per_s": parts["pq_verify"]["rows_per_s"],
         "parts": parts,
         "kernels": kernels,
-        "roofline": {"bound": "hbm", "kernel": "moe_stream_kernel<gate+up> (MoE gate+up grouped dequant GEMM)",
+        "roofline": {"bound": "hbm", "kernel": "moe_gateup_stream_kernel (MoE gate+up grouped dequant GEMM)",
                      "achieved": dom["GB/s"], "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
                      "frac": dom["frac"], "traffic": traffic, "traffic_eager": traffic_eager,
                      "read_probe_GB/s": read_gbs, "frac_of_read_probe": dom["GB/s"] / read_gbs,

@@ -385,17 +385,21 @@ __device__ __forceinline__ void prep_row_bf16(const uint16_t *__restrict__ src, 
 // Two ways to share the range among the CTA's nw warps:
 //   strided (EVEN = false): warp w takes units u0 + w, u0 + w + nw, ...;
 //   even (EVEN = true): the range is flattened to tiles f = (u - u0) * ntk + tile and cut into
-//     nw contiguous warp ranges whose lengths differ by at most one tile, so no warp has a whole
-//     unit more to stream than another.  A unit cut between warps is finished by the warp that
+//     nw contiguous warp ranges whose lengths differ by at most four tiles, so no warp has a
+//     whole unit more to stream than another.  A unit cut between warps is finished by the warp that
 //     began it: each later warp holding a piece of it leaves that piece's 16 x 8 partial sum in
 //     shared memory (its first piece, one slot per warp), and after one barrier the first warp
 //     adds them in warp order, so the result does not depend on timing.
+// Cuts fall on multiples of 4 tiles when ntk allows it: a 4-tile step is 384 bytes of every
+// row, so a cut never splits a 128-byte line between two warps (whose reads of it, far apart in
+// time, would each bring it from DRAM).
 struct WarpTiles {
     int f0, f1;
 };
 __device__ __forceinline__ WarpTiles warp_tiles(int u0, int u1, int ntk, int nw, int w) {
-    const long long T = (long long)(u1 - u0) * ntk;
-    return {(int)(T * w / nw), (int)(T * (w + 1) / nw)};
+    const int G = (ntk & 3) == 0 ? 4 : 1;
+    const long long Tg = (long long)(u1 - u0) * (ntk / G);
+    return {(int)(Tg * w / nw) * G, (int)(Tg * (w + 1) / nw) * G};
 }
 
 // A warp's first unit, first tile and tile count under either split.

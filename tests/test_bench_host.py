@@ -19,7 +19,7 @@ def test_launches_per_step():
 def test_traffic_record_parses():
     rec = bench._traffic_record()
     assert rec is not None
-    assert rec["kernel"].startswith("moe_stream_kernel<1,1>")
+    assert rec["kernel"] == "moe_gateup_stream_kernel"
     assert int(rec["bytes"]) > 0 and int(rec["units"]) > 0 and rec["unit"] == "active_experts"
     assert re.fullmatch(r"[0-9a-f]{16}", rec["sources"])
     assert re.fullmatch(r"[0-9a-f]{16}", bench._kernel_source_digest())
