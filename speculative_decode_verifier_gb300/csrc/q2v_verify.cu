@@ -530,22 +530,23 @@ __global__ void __launch_bounds__(GW == 1 ? 256 : 32 * GW) pqv_small_kernel(PqAr
 
 // Level 1 of a large-V draw: the segment (one of the session's nseg segment masses) holding
 // the crossing of u_fin * total.  The whole block stages the masses in shared memory (`sm`,
-// nseg floats; the p_j masses in the zero-residual fallback), then warp 0 alone decides: lane l
-// sums the contiguous run of cdiv(nseg, 32) entries it owns, a compensated warp scan gives each
-// lane its prefix, the first lane whose run crosses walks it (if rounding puts the target past
-// the end, the last entry with mass is taken).  Returns, in every thread, the entry (-1: no
-// mass at all), the compensated prefix before it, the target and the mode (0 residual, 1 p_j).
+// nseg floats; the p_j masses in the zero-residual fallback); thread i sums the contiguous run
+// of cdiv(nseg, threads) entries it owns, a compensated block scan gives each thread its prefix
+// and every thread the total, and the first thread whose run crosses walks it (if rounding puts
+// the target past the end, the last entry with mass is taken).  Returns, in every thread, the
+// entry (-1: no mass at all), the compensated prefix before it, the target and the mode
+// (0 residual, 1 p_j).  `scan` is block_excl_scan's scratch; s_first and s_lastpos are shared ints.
 struct SegPick {
     int ent, mode;
     float pre_hi, pre_lo, target;
 };
 
 __device__ __forceinline__ SegPick pick_segment(const float *mass, const float *pmass, int nseg, int mode0, float u,
-                                                float *sm, SegPick *shared_out) {
-    const int tid = threadIdx.x, nt = blockDim.x, lane = tid & 31;
-    const bool w0 = tid < 32;
-    const int q = cdiv(nseg, 32);
-    const int e0 = min(nseg, lane * q), e1 = min(nseg, e0 + q);
+                                                float *sm, float *scan, int *s_first, int *s_lastpos,
+                                                SegPick *shared_out) {
+    const int tid = threadIdx.x, nt = blockDim.x;
+    const int q = cdiv(nseg, nt);
+    const int e0 = min(nseg, tid * q), e1 = min(nseg, e0 + q);
     CSum own, excl, tot;
     int mode = mode0;
     for (int pass = 0; pass < 2; ++pass) {  // pass 1 only when the residual has no mass
@@ -560,54 +561,55 @@ __device__ __forceinline__ SegPick pick_segment(const float *mass, const float *
                 if (e + k * nt < nseg) sm[e + k * nt] = v[k];
         }
         __syncthreads();
-        if (w0) {
-            own = CSum();
-            for (int e = e0; e < e1; ++e) own.add(sm[e]);
-            excl = warp_excl_scan_c(own, lane, tot);
-            if (lane == 0) shared_out->pre_hi = tot.hi;  // whether the pass found mass, for all
-        }
-        __syncthreads();
-        const float th = shared_out->pre_hi;
-        __syncthreads();
-        if (mode == 1 || th > 0.0f) break;
-        mode = 1;  // zero residual mass: draw from p_j
+        own = CSum();
+        for (int e = e0; e < e1; ++e) own.add(sm[e]);
+        excl = block_excl_scan(own, scan, tot);  // tot is the same in every thread
+        if (mode == 1 || tot.hi > 0.0f) break;
+        __syncthreads();  // sm and scan are refilled by the fallback pass
+        mode = 1;         // zero residual mass: draw from p_j
     }
-    if (w0) {
-        const float target = u * (tot.hi + tot.lo);
-        const float own_m = own.hi + own.lo;
-        const unsigned cm = __ballot_sync(0xffffffffu, own_m > 0.0f && excl.exceeds(own_m, target));
-        const unsigned pm = __ballot_sync(0xffffffffu, own_m > 0.0f);
-        const int first = cm ? __ffs(cm) - 1 : 32;
-        const int owner = first < 32 ? first : (pm ? 31 - __clz(pm) : -1);
-        if (owner < 0 && lane == 0) {
-            shared_out->ent = -1;
-            shared_out->mode = mode;
-            shared_out->target = target;
-        }
-        if (lane == owner) {
-            // the first entry of this run whose end passes the target (else its last entry with mass)
-            CSum pre = excl, last_pre, found_pre;
-            int found = -1, last_nz = -1;
-            for (int e = e0; e < e1; ++e) {
-                const float me = sm[e];
-                if (me > 0.0f) {
-                    last_nz = e;
-                    last_pre = pre;
-                    if (first < 32 && pre.exceeds(me, target)) {
-                        found = e;
-                        found_pre = pre;
-                        break;
-                    }
+    const float target = u * (tot.hi + tot.lo);
+    const float own_m = own.hi + own.lo;
+    if (tid == 0) {
+        *s_first = nt;
+        *s_lastpos = -1;
+    }
+    __syncthreads();
+    if (own_m > 0.0f) {
+        atomicMax(s_lastpos, tid);
+        if (excl.exceeds(own_m, target)) atomicMin(s_first, tid);
+    }
+    __syncthreads();
+    const int first = *s_first;
+    const int owner = first < nt ? first : *s_lastpos;
+    if (owner < 0 && tid == 0) {
+        shared_out->ent = -1;
+        shared_out->mode = mode;
+        shared_out->target = target;
+    }
+    if (tid == owner) {
+        // the first entry of this run whose end passes the target (else its last entry with mass)
+        CSum pre = excl, last_pre, found_pre;
+        int found = -1, last_nz = -1;
+        for (int e = e0; e < e1; ++e) {
+            const float me = sm[e];
+            if (me > 0.0f) {
+                last_nz = e;
+                last_pre = pre;
+                if (first < nt && pre.exceeds(me, target)) {
+                    found = e;
+                    found_pre = pre;
+                    break;
                 }
-                pre.add(me);
             }
-            const CSum pr = found >= 0 ? found_pre : last_pre;
-            shared_out->ent = found >= 0 ? found : last_nz;
-            shared_out->pre_hi = pr.hi;
-            shared_out->pre_lo = pr.lo;
-            shared_out->mode = mode;
-            shared_out->target = target;
+            pre.add(me);
         }
+        const CSum pr = found >= 0 ? found_pre : last_pre;
+        shared_out->ent = found >= 0 ? found : last_nz;
+        shared_out->pre_hi = pr.hi;
+        shared_out->pre_lo = pr.lo;
+        shared_out->mode = mode;
+        shared_out->target = target;
     }
     __syncthreads();
     return *shared_out;
@@ -919,11 +921,14 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
     }
     __syncthreads();
     if (tid == 0) {
-        __threadfence();  // release this CTA's masses (the barrier above ordered them before it)
-        const unsigned ticket = atomicAdd(sp.tickets + s, 1u);
-        const int last = ticket == (unsigned)(sp.C - 1);
-        if (last) __threadfence();  // acquire: the other CTAs' masses, read below with ld.cg
-        s_last = last;
+        // one acquire-release atomic: releases this CTA's masses (the barrier above ordered them
+        // before it) and, for the last CTA, acquires the others' (read below with ld.cg)
+        unsigned ticket;
+        asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;\n"
+                     : "=r"(ticket)
+                     : "l"(sp.tickets + s)
+                     : "memory");
+        s_last = ticket == (unsigned)(sp.C - 1);
     }
     __syncthreads();
     if (!s_last) return;
@@ -940,7 +945,7 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
     const int nseg = sp.C * kSegsPerChunk;
     const int nt = blockDim.x;
     const SegPick pk = pick_segment(sp.mass + (size_t)s * nseg, sp.pmass + (size_t)s * nseg, nseg, D.mode,
-                                    a.u_fin[s], pq_dyn, &s_pick);
+                                    a.u_fin[s], pq_dyn, s_scan, &s_first, &s_lastpos, &s_pick);
     D.mode = pk.mode;
     const float target = pk.target;
     const int owner1 = pk.ent;
