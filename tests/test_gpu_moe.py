@@ -59,6 +59,7 @@ def test_moe_config_full_size(env):
     dict(E=1, H=256, F=128, M=5, topk=1),      # one expert: every row routed to it with gate weight 1
     dict(E=2, H=512, F=256, M=8, topk=2),      # top-k = E: every row routed to every expert
     dict(E=64, H=4096, F=2048, M=8, topk=6),   # 8 rows at full size: up to 48 active experts
+    dict(E=64, H=768, F=1024, M=8, topk=8),    # streaming gate+up over 3-tile units (cuts on single tiles)
 ])
 def test_shapes(env, over):
     m = synth.config_moe(2, salt=sum(over.values()), **over)
