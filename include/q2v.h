@@ -106,10 +106,11 @@ size_t q2_moe_grouped_workspace(int M, int E, int topk, int H, int F);
 #define Q2_MOE_RENORMALIZE 1u /* divide the selected gate probabilities by their sum */
 
 /*
- * Routed-expert FFN over M rows (the "routed MoE" of the K+1-row verify; the fused
- * router, fused gate+up+SwiGLU decode and expert dedup named in "1x Spark tuned
- * DSpark for DeepSeek-V4-Flash ...", reply on the decode arc, and "ds4-on-spark",
- * section "What the fork adds": "MoE gate_up expert dedup"):
+ * Routed-expert FFN over M rows (the routed-expert part of the K+1-row verify; the fused
+ * router, fused gate+up+SwiGLU decode and expert deduplication listed in "1x Spark tuned
+ * DSpark for DeepSeek-V4-Flash ...", reply on the decode arc, and in "ds4-on-spark",
+ * section "What the fork adds", where each active expert's gate/up weights are read once
+ * for all rows routed to it):
  *
  *   prob[r] = softmax(router_logits[r][0..E));  top-`topk` experts by probability,
  *   ties to the lower expert index;  g = the selected probabilities (renormalised to

@@ -5,7 +5,7 @@
 // GB10/GX10 with DSpark speculative decoding", page 2, verifier-bottleneck reply); the
 // engines fused the router, fused gate+up+SwiGLU for decode ("1x Spark tuned DSpark for
 // DeepSeek-V4-Flash ...", reply on the decode arc) and deduplicated expert reads across
-// rows ("ds4-on-spark", section "What the fork adds": MoE gate_up expert dedup).
+// rows ("ds4-on-spark", section "What the fork adds").
 //
 // Steps (one stream, no host synchronisation):
 //   1. route:    softmax over experts, top-k by logit (ties to the lower index), gate
