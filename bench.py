@@ -8,7 +8,9 @@ One step = one pass of the whole hot path at the M=5 verifier shapes:
 Inputs are seeded synthetic tensors (see speculative_decode_verifier_gb300.synth); weights
 are random, not trained.  Device timing replays one CUDA graph per input set, rotating over
 4 sets, each with its own weights (the linear's and all 64 experts'), so every step touches
-> 250 MB that the previous step did not (more than the 126 MB L2).
+> 250 MB that the previous step did not (more than the 126 MB L2).  The per-part times (the
+linear's GB/s, pq_verify rows/s) and the extra configurations are timed one graph replay at a
+time with L2 flushed (a 256 MB write, then a 256 MB read) before each replay.
 
 Prints one JSON line.  `value` is the device-timed step time in microseconds (inputs resident
 in HBM); `e2e` is the same step through the Python binding with pinned host buffers copied
@@ -353,10 +355,34 @@ def run_device(args, rank: int, world: int):
                       ("gemm", q2v.PROBE_GEMM), ("pq_stats", q2v.PROBE_PQ_STATS), ("pq_verify", q2v.PROBE_PQ_VERIFY)):
         kern_us[name] = probe_pass(kid)
 
+    # The parts and the extras below are timed one graph replay at a time with L2 flushed before
+    # each, outside the events: the four input sets of the dense linear (26 MB) or of pq_verify
+    # (56 MB) would otherwise stay in L2 from one replay to the next.  The flush writes a 256 MB
+    # buffer (twice the L2) and then reads another, so the timed kernels find L2 holding clean
+    # lines of neither their data nor the write (whose write-backs would otherwise land inside
+    # the timed region).  It is enqueued ahead of the replay, so the GPU never waits for the
+    # host between the two events.
+    flush_buf = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    flush_rd = torch.ones(256 << 20, dtype=torch.uint8, device=dev)
+
+    def replays_us(gr, reps):
+        """Mean µs of one replay of gr, L2 flushed before each timed replay."""
+        evs = []
+        for i in range(reps):
+            flush_buf.fill_(i & 0xFF)
+            flush_rd.sum()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record()
+            gr.replay()
+            b.record()
+            evs.append((a, b))
+        torch.cuda.synchronize()
+        return sum(a.elapsed_time(b) for a, b in evs) / reps * 1000.0
+
     def part_us(fn):
         """Mean µs of one call of fn inside a graph that makes one call per input set (N_SETS
         calls back to back, PDL between them, as inside a step), so the time per graph launch
-        does not count as the part's own."""
+        is shared by N_SETS calls; L2 flushed before every timed replay."""
         def all_sets():
             for s in sets:
                 fn(s)
@@ -365,24 +391,18 @@ def run_device(args, rank: int, world: int):
         gr = torch.cuda.CUDAGraph()
         with torch.cuda.graph(gr):
             all_sets()
-        reps = max(3, args.steps // N_SETS)
         for _ in range(args.warmup):
             gr.replay()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(reps):
-            gr.replay()
-        b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / (reps * N_SETS) * 1000.0
+        return replays_us(gr, max(5, args.steps // N_SETS)) / N_SETS
 
     gemm_us = part_us(part_gemm)
     moe_us = part_us(part_moe)
     pq_us = part_us(part_pq)
 
     def graph_us(fn, reps):
-        """Mean µs of fn() replayed from one CUDA graph (3 warm-up replays first)."""
+        """Mean µs of fn() replayed from one CUDA graph (3 warm-up replays first; L2 flushed
+        before every timed replay)."""
         fn()
         torch.cuda.synchronize()
         gr = torch.cuda.CUDAGraph()
@@ -397,13 +417,7 @@ def run_device(args, rank: int, world: int):
         for _ in range(3):
             gr.replay()
         torch.cuda.synchronize()
-        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        a.record()
-        for _ in range(reps):
-            gr.replay()
-        b.record()
-        torch.cuda.synchronize()
-        return a.elapsed_time(b) / reps * 1000.0
+        return replays_us(gr, reps)
 
     peak_x, _ = _peaks()
     lin_bytes = sh["N"] * (sh["K"] // 32) * 12 + sh["M"] * sh["K"] * 2 + sh["M"] * sh["N"] * 4
@@ -692,7 +706,8 @@ def run_device(args, rank: int, world: int):
         "scaling": "weak", "vs_baseline": None, "dtype": "q2b32 weights, bf16->f16 operands, fp32 accumulate/logits",
         "data": "synthetic (seeded; random weights)",
         "config": {"workload": WORKLOAD, "sets": N_SETS,
-                   "l2": "inputs larger than L2: 4 rotating input sets, > 250 MB touched per step",
+                   "l2": "inputs larger than L2: 4 rotating input sets, > 250 MB touched per step; parts and "
+                         "extras: L2 flushed (256 MB write, then 256 MB read) before every timed graph replay",
                    "parallelism": "replicas" if world > 1 else "single GPU", "graph": "one CUDA graph per step"},
         "q2_gemm_m5_GB/s": gemm_gbs, "q2_gemm_m5_frac_of_measured_peak": gemm_gbs / peak,
         "q2_gemm_m5_frac_of_8TBs": gemm_gbs / 8000.0,
