@@ -614,7 +614,7 @@ __global__ void __launch_bounds__(kDnWarps * 32, 1) moe_down_stream_kernel(MoeAr
             if (c < nc.x) dst[(size_t)s_slot[nc.y + c] * H + rr] = ldexpf(v[qq], s_exps[nc.y + c]);
         }
     };
-    float *part = reinterpret_cast<float *>(sm_dyn + SA.words() + (size_t)kDnWarps * kDnRing * kTileWords);
+    float *part = reinterpret_cast<float *>(sm_dyn + SA.words() + (size_t)kDnWarps * kDnRing * kTileWords);  // even split only
     stream_warp_tiles<kDnRing, kDnEven>(pc, ring, sm_act, SA, part, u0, u1, L.ntk, row_bytes, kDnWarps, warp, lane,
                                         unit_w, cols, store, scale_max);
     if (scale_mag_out_of_range(scale_max)) set_status(a.status, Q2_ERR_RANGE);
@@ -767,7 +767,8 @@ cudaError_t launch_moe(const MoeArgs &a, const MoeWs &w, int num_sms, cudaStream
     const int dn_units_max = expect_active * cdiv(a.H, kRowsPerCta);
     const int dn_q = cdiv(dn_units_max, num_sms);
     const int dn_win = min(P, kDnMaxExperts * a.M);
-    const size_t dn_smem = SmemAct(LH, dn_win).bytes() + (size_t)kDnWarps * (kDnRing * kTileWords + 128) * 4;
+    const size_t dn_smem =
+        SmemAct(LH, dn_win).bytes() + (size_t)kDnWarps * (kDnRing * kTileWords + (kDnEven ? 128 : 0)) * 4;
     const bool dn_stream = a.M <= 8 && ks_d == 1 && a.H % kRowsPerCta == 0 && LH.nb == LH.ntk * kTileBlocks &&
                            LH.nb % 4 == 0 && dn_q <= cdiv(a.H, kRowsPerCta) && dn_win <= 64 &&
                            dn_smem <= (size_t)220 * 1024;
