@@ -477,6 +477,23 @@ def run_device(args, rank: int, world: int):
         layer = {"workload": "Q,K,V,O 4096x4096 Q2B32 linears + routed MoE FFN (64 experts, top-6), M=5",
                  "us": l_us, "GB/s": l_bytes / (l_us * 1e-6) / 1e9, "frac": l_bytes / (l_us * 1e-6) / 1e9 / peak_x}
         del layers
+        # the same layer with Q, K and V as one linear over their stacked weights (12,288 rows
+        # sharing the layer input, as a serving engine lays them out), then O
+        qkv = [D(synth.q2b32_weights(synth.Streams(9500 + j), 3 * sh["N"], sh["K"]).reshape(-1)) for j in range(N_SETS)]
+        wo = [D(synth.q2b32_weights(synth.Streams(9600 + j), sh["N"], sh["K"]).reshape(-1)) for j in range(N_SETS)]
+        Yqkv = torch.empty((sh["M"], 3 * sh["N"]), dtype=torch.float32, device=dev)
+        wsq = q2v.workspace(q2v.q2_tiny_gemm_workspace(sh["M"], 3 * sh["N"], sh["K"]), dev)
+
+        def layer_fused_all():
+            for j in range(N_SETS):
+                q2v.q2_tiny_gemm(qkv[j], 3 * sh["N"], sh["K"], sets[j]["A"], Y=Yqkv, ws=wsq)
+                q2v.q2_tiny_gemm(wo[j], sh["N"], sh["K"], sets[j]["A"], Y=Yq, ws=wsc)
+                part_moe(sets[j])
+
+        lf_us = graph_us(layer_fused_all, max(3, args.steps // 4)) / N_SETS
+        layer["us_qkv_as_one_linear"] = lf_us
+        layer["GB/s_qkv_as_one_linear"] = l_bytes / (lf_us * 1e-6) / 1e9
+        del qkv, wo
 
     # the tiny configuration: the K=256, N=512 Q2B32 linear at M = 1..4 and pq_verify of one
     # session (k=4, V=1024), each timed as 4 distinct calls back to back in one graph

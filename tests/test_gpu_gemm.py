@@ -54,6 +54,7 @@ def test_verifier_linear_config(env):
     (1, 1, 32),        # the smallest problem
     (6, 4100, 4064),   # a ragged last 16-row group at the verifier width; 127 blocks (odd), a partial 16th tile
     (8, 4864, 1024),   # 8 rows in one activation slice, 304 row groups
+    (5, 12288, 4096),  # Q, K and V of the verifier layer as one linear (768 CTAs: two waves)
     (5, 40960, 4096),  # the streaming kernel (many weight rows per SM): one session against a head
     (1, 65536, 256),   # streaming, one activation row, one K tile
     (8, 40000, 1024),  # streaming, all 8 columns of the MMA, units not a multiple of the warps
