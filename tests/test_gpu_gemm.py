@@ -70,11 +70,12 @@ def test_shapes(env, M, N, K):
     check_gemm(Y, Yo, absY, f"M={M} N={N} K={K}")
 
 
-def test_activation_range_extremes(env):
+@pytest.mark.parametrize("N,K", [(32, 512), (38912, 256)])  # per-CTA kernel; streaming kernel
+def test_activation_range_extremes(env, N, K):
     """Rows far outside the f16 range, tiny rows and an all-zero row: the per-row power-of-two
     scale keeps them exact."""
     st = synth.Streams(77)
-    M, N, K = 5, 32, 512
+    M = 5
     W = synth.q2b32_weights(st, N, K)
     a = st["A"].normal(0, 1, size=(M, K))
     a[0] *= 1e30
@@ -88,10 +89,11 @@ def test_activation_range_extremes(env):
     check_gemm(Y[[0, 1, 3, 4]], Yo[[0, 1, 3, 4]], absY[[0, 1, 3, 4]], "extremes")
 
 
-def test_scale_extremes_within_range(env):
+@pytest.mark.parametrize("N", [48, 38912])  # per-CTA kernel; streaming kernel
+def test_scale_extremes_within_range(env, N):
     """d = 0 (offset only), subnormal-small and the largest in-range scales."""
     st = synth.Streams(78)
-    M, N, K = 4, 48, 256
+    M, K = 4, 256
     codes = st["codes"].integers(0, 4, size=(N, K), dtype=np.uint8)
     d = st["d"].uniform(0.01, 0.05, size=(N, K // 32))
     d[0:16] = 0.0
@@ -105,13 +107,14 @@ def test_scale_extremes_within_range(env):
     check_gemm(Y, Yo, absY, "scales")
 
 
-def test_scale_out_of_range_sets_status(env):
+@pytest.mark.parametrize("N,K,row", [(16, 64, 3), (38912, 256, 38900)])  # per-CTA kernel; streaming kernel
+def test_scale_out_of_range_sets_status(env, N, K, row):
     dev, q2v, _ = env
     st = synth.Streams(79)
-    N, K, M = 16, 64, 2
+    M = 2 if N < 1000 else 5
     codes = st["codes"].integers(0, 4, size=(N, K), dtype=np.uint8)
     d = np.full((N, K // 32), 0.02)
-    d[3, 1] = 64.0
+    d[row, 1] = 64.0
     W = synth.pack_q2b32(codes, synth.fp16_bits(d), synth.fp16_bits(np.zeros((N, K // 32))))
     A = synth.activations_bf16(st, M, K)
     ws = q2v.workspace(q2v.q2_tiny_gemm_workspace(M, N, K), dev)

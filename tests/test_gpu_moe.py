@@ -93,3 +93,21 @@ def test_verifier_shape_is_deterministic(env):
     a, _ = _run(env, m)
     b, _ = _run(env, m)
     assert np.array_equal(a, b)
+
+
+@pytest.mark.parametrize("mat", ["Wg", "Wd"])
+def test_scale_out_of_range_sets_status(env, mat):
+    """A gate (or down) scale of 64 in every expert: the streaming gate+up (or down) kernel, which
+    this shape takes, flags Q2_ERR_RANGE in the status word."""
+    import torch
+    dev, q2v, _ = env
+    m = synth.config_moe(2, salt=5, E=8, H=256, F=256, M=5, topk=3)
+    W = {k: np.array(m[k], copy=True) for k in ("Wg", "Wu", "Wd")}
+    d = W[mat].reshape(-1, W[mat].shape[-2], 12)[:, 0, 8:10]   # block 0 of every row: the d half
+    d[:] = synth.fp16_bits(np.full(1, 64.0)).view(np.uint8)
+    ws = q2v.workspace(q2v.q2_moe_grouped_workspace(m["M"], m["E"], m["topk"], m["H"], m["F"]), dev)
+    q2v.q2_moe_grouped(to_dev(W["Wg"].reshape(-1), dev), to_dev(W["Wu"].reshape(-1), dev),
+                       to_dev(W["Wd"].reshape(-1), dev), m["E"], m["H"], m["F"], m["topk"],
+                       to_dev(m["X"], dev), to_dev(m["router"], dev), ws=ws)
+    torch.cuda.synchronize()
+    assert q2v.q2_get_device_status(ws) == 8  # Q2_ERR_RANGE
