@@ -193,12 +193,14 @@ def run_device(args, rank: int, world: int):
             a = a.view(np.int16)
         return torch.from_numpy(a).to(dev)
 
-    if args.profile_cohort:
-        # eager calls of the M=60 vocabulary-head GEMM (tcgen05 path), for an ncu capture
+    if args.profile_cohort or args.profile_session:
+        # eager calls of the vocabulary-head GEMM, for an ncu capture: M=60 (the cohort, tcgen05
+        # path) or M=5 (one session: the first 5 rows, streaming path)
         gc = synth.config_gemm(4)
-        Wc, Ac = D(gc["W"].reshape(-1)), D(gc["A"])
-        Yc = torch.empty((gc["M"], gc["N"]), dtype=torch.float32, device=dev)
-        wsc = q2v.workspace(q2v.q2_tiny_gemm_workspace(gc["M"], gc["N"], gc["K"]), dev)
+        Mh = gc["M"] if args.profile_cohort else 5
+        Wc, Ac = D(gc["W"].reshape(-1)), D(gc["A"][:Mh])
+        Yc = torch.empty((Mh, gc["N"]), dtype=torch.float32, device=dev)
+        wsc = q2v.workspace(q2v.q2_tiny_gemm_workspace(Mh, gc["N"], gc["K"]), dev)
         for _ in range(args.warmup + args.steps):
             q2v.q2_tiny_gemm(Wc, gc["N"], gc["K"], Ac, Y=Yc, ws=wsc)
         torch.cuda.synchronize()
@@ -858,6 +860,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--profile-cohort", action="store_true",
                     help="eager calls of the M=60 x 129280 x 4096 GEMM only (for ncu); prints nothing")
+    ap.add_argument("--profile-session", action="store_true",
+                    help="eager calls of the M=5 x 129280 x 4096 GEMM only (for ncu); prints nothing")
     ap.add_argument("--no-extras", action="store_true",
                     help="skip the chained-linear and cohort (M=60) measurements")
     ap.add_argument("--profile", action="store_true",
