@@ -12,8 +12,9 @@
 //   * TMA warp: one 2-D tensor copy per stage brings the tile's raw Q2B32 bytes
 //     (128 rows x 48 B) into a deep shared-memory ring (the weights do not depend on the
 //     previous kernel, so this warp starts before the programmatic wait);
-//   * B warp: one bulk copy per stage brings the prepared activation stage (the B operand,
-//     laid out by prep_umma_kernel) into a shared-memory ring;
+//   * B warp: brings each prepared activation stage (the B operand, laid out by
+//     prep_umma_kernel) into a shared-memory ring with 16-byte cp.async copies (small and
+//     L2-resident, so they stay off the TMA engine that streams the weights);
 //   * 8 dequant warps, in two groups that take the stages in turn: each thread decodes one
 //     weight row of the stage with the exact lop3 + f16x2 fma decode and writes it straight
 //     from registers into tensor memory (tcgen05.st) as the MMA's A operand; the blocks'
@@ -172,12 +173,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *map, i
             "r"(smem_u32(dst)),
         "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
-}
-__device__ __forceinline__ void bulk_load(void *dst, const void *src, uint32_t bytes, uint64_t *bar) {
-    asm volatile("cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];\n" ::"r"(
-                     smem_u32(dst)),
-                 "l"(src), "r"(bytes), "r"(smem_u32(bar))
-                 : "memory");
 }
 
 __device__ __forceinline__ void tc_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;\n" ::: "memory"); }
