@@ -13,12 +13,17 @@
 //                (pairs of one expert ordered by row), the list of active experts;
 //   2. prep X:   the activation rows in the small-M GEMM's B-operand layout;
 //   3. gate/up:  one grouped GEMM over units (active expert, gate|up, 16-row group, K split);
-//                a CTA stages the prepared rows of each expert run in shared memory once, and
-//                each warp streams its units' weight tiles through its own cp.async ring;
-//                every active expert's weights are read once for all rows routed to it;
+//                every active expert's weights are read once for all rows routed to it.  At
+//                most 8 rows without a K split (the verifier shape): moe_gateup_stream_kernel,
+//                one 24-warp CTA per SM with all X rows staged once and its tiles cut evenly
+//                over the warps; otherwise moe_stream_kernel, whose CTAs stage the prepared rows
+//                of each expert run and whose warps take units in turn; every warp streams its
+//                weight tiles through its own cp.async ring;
 //   4. prep h:   h = silu(sum of gate splits) * (sum of up splits), fused into the B-operand
 //                prep of the down GEMM;
-//   5. down:     the same grouped GEMM over (active expert, 16-row group, K split) units;
+//   5. down:     the same over (active expert, 16-row group, K split) units:
+//                moe_down_stream_kernel at the verifier shape (the h rows of the CTA's one or two
+//                experts staged once), moe_stream_kernel otherwise;
 //   6. combine:  Y[r] = sum over slots, in slot order, of g * (sum of the down splits).
 // Every sum runs in a fixed order, so the result is deterministic.
 #include <math.h>
