@@ -263,6 +263,7 @@ __device__ __forceinline__ DrawRows draw_rows(const PqArgs &a, int s, int j, con
 
 constexpr int kSmallWarpMaxV = 512;   // one warp per session up to this V
 constexpr int kSmallMaxRun = 16;      // tokens per lane in the draw, one warp per session
+constexpr int kSegWarpRun = 8;       // a large-V draw segment of <= 32 x this many tokens is walked by one warp
 
 // (max, log2 sum 2^((x - max) beta)) of one row of V logits, by one warp; loads in batches.
 template <bool VEC>
@@ -957,10 +958,64 @@ __global__ void __launch_bounds__(256) pqv_verify_kernel(PqArgs a, PqSplit sp) {
     __syncthreads();
     int y_sel = -1;
     if (owner1 >= 0) {
-        // level 2: the tokens of the selected segment, r per thread
+        // level 2: the tokens of the selected segment
         const int ent = s_ent;
         const int sc = ent / kSegsPerChunk, sw = ent - sc * kSegsPerChunk;
         const int ty0 = sc * sp.L + sw * Lw, ty1 = min(min(a.V, sc * sp.L + sp.L), ty0 + Lw);
+        if (Lw <= 32 * kSegWarpRun) {
+            // a segment of at most 32 x kSegWarpRun tokens: warp 0 alone, each lane a contiguous
+            // run of the segment's weights in registers (loaded at once), one compensated warp
+            // scan, a ballot for the first run that crosses (else the last run with mass) and
+            // that lane's walk -- no block barrier
+            if (warp == 0) {
+                const int rl = cdiv(max(ty1 - ty0, 0), 32);
+                const int y0 = min(ty1, ty0 + lane * rl), y1 = min(ty1, y0 + rl);
+                CSum seg_pre;
+                seg_pre.hi = s_pre[0];
+                seg_pre.lo = s_pre[1];
+                float wv[kSegWarpRun];
+                CSum own, tot;
+#pragma unroll
+                for (int u = 0; u < kSegWarpRun; ++u) {
+                    const int y = y0 + u;
+                    wv[u] = y < y1 ? draw_weight(D, beta, D.t[y], D.d[y]) : 0.0f;
+                    if (y < y1) own.add(wv[u]);
+                }
+                const CSum excl = csum_plus(seg_pre, warp_excl_scan_c(own, lane, tot));
+                const float own_m = own.hi + own.lo;
+                const unsigned cm = __ballot_sync(0xffffffffu, own_m > 0.0f && excl.exceeds(own_m, target));
+                const unsigned pm = __ballot_sync(0xffffffffu, own_m > 0.0f);
+                const int first = cm ? __ffs(cm) - 1 : 32;
+                const int owner = first < 32 ? first : (pm ? 31 - __clz(pm) : -1);
+                int pick = -1;
+                if (lane == owner) {
+                    // the first token of the run whose end passes the target, else its last token with mass
+                    CSum pre = excl;
+                    int found = -1, last_nz = -1;
+                    bool done = false;
+#pragma unroll
+                    for (int u = 0; u < kSegWarpRun; ++u) {
+                        const int y = y0 + u;
+                        if (!done && y < y1) {
+                            const float w = wv[u];
+                            if (w > 0.0f) {
+                                last_nz = y;
+                                if (first < 32 && pre.exceeds(w, target)) {
+                                    found = y;
+                                    done = true;
+                                }
+                            }
+                            if (!done) pre.add(w);
+                        }
+                    }
+                    pick = found >= 0 ? found : last_nz;
+                }
+                const int y = owner >= 0 ? __shfl_sync(0xffffffffu, pick, owner) : -1;
+                if (lane == 0) write_tokens(a, s, j, y);
+            }
+            return;
+        }
+        // larger segments: r tokens per thread, block-wide scan
         const int r = cdiv(max(ty1 - ty0, 0), nt);
         const int y0 = min(ty1, ty0 + tid * r), y1 = min(ty1, y0 + r);
         CSum seg_pre;
