@@ -49,6 +49,14 @@ LAUNCHES_PER_STEP = 2 + 5 + 2   # prep + gemm; route with X prep, gate/up, prep 
 EXPERT_BYTES = 3 * 2048 * (4096 // 32) * 12   # gate + up + down of one expert
 
 
+def run_config(world: int) -> dict:
+    """The `config` of the JSON line, the same for both arms."""
+    return {"workload": WORKLOAD, "sets": N_SETS,
+            "l2": "inputs larger than L2: 4 rotating input sets, > 250 MB touched per step; parts and "
+                  "extras: L2 flushed (256 MB write, then 256 MB read) before every timed graph replay",
+            "parallelism": "replicas" if world > 1 else "single GPU", "graph": "one CUDA graph per step"}
+
+
 def _kernel_source_digest() -> str:
     """sha256 (first 16 hex digits) of the source the streaming gate+up kernel is built from: the
     shared device headers and the kernel's own definition (with its warp and ring constants).  The
@@ -724,10 +732,7 @@ def run_device(args, rank: int, world: int):
         "warmup": args.warmup, "ms_per_step": step_us / 1000.0, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "q2b32 weights, bf16->f16 operands, fp32 accumulate/logits",
         "data": "synthetic (seeded; random weights)",
-        "config": {"workload": WORKLOAD, "sets": N_SETS,
-                   "l2": "inputs larger than L2: 4 rotating input sets, > 250 MB touched per step; parts and "
-                         "extras: L2 flushed (256 MB write, then 256 MB read) before every timed graph replay",
-                   "parallelism": "replicas" if world > 1 else "single GPU", "graph": "one CUDA graph per step"},
+        "config": run_config(world),
         "q2_gemm_m5_GB/s": gemm_gbs, "q2_gemm_m5_frac_of_measured_peak": gemm_gbs / peak,
         "q2_gemm_m5_frac_of_8TBs": gemm_gbs / 8000.0,
         "pq_verify_rows_per_s": parts["pq_verify"]["rows_per_s"],
@@ -888,7 +893,7 @@ def main():
             "impl": "reference", "metric": METRIC, "value": us, "unit": "µs", "n_gpus": 0,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1000.0, "higher_is_better": False,
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic (seeded; random weights)",
-            "config": {"workload": WORKLOAD},
+            "config": run_config(world),
             "cpu_baseline": {"value": us, "unit": "µs", "cores": cores, "kind": "oracle", "sample": sample},
             "e2e": {"value": us, "unit": "µs", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         }))

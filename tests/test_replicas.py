@@ -65,5 +65,9 @@ def test_reference_arm_prints_on_rank_zero_only(rank, expect_output):
         assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
         cb = d["cpu_baseline"]
         assert cb["kind"] == "oracle" and cb["value"] == d["value"] and cb["cores"] >= 1 and cb["sample"]
+        # the same config, metric and unit as the device arm's line
+        sys.path.insert(0, ROOT)
+        import bench
+        assert d["config"] == bench.run_config(2) and d["metric"] == bench.METRIC and d["unit"] == "µs"
     else:
         assert lines == []
