@@ -49,6 +49,25 @@ def test_noalloc_matches_workspace_entry_point_on_consecutive_calls(env):
         assert torch.equal(toks.cpu(), tok_ref.cpu())
 
 
+def test_noalloc_at_its_largest_size(env):
+    """S = 15 sessions at k = 4, V = 129,280: the largest verify the 2 MiB scratch holds, run and
+    compared with the workspace entry point."""
+    import torch
+    dev, q2v, lib = env
+    assert q2v.pq_verify_workspace(15, 4, 129280) <= 2 << 20 < q2v.pq_verify_workspace(16, 4, 129280)
+    stream = torch.cuda.current_stream().cuda_stream
+    v = synth.verify_inputs(synth.Streams(4242), 15, 4, 129280, t_std=3.0, noise_std=1.0, T=1.0)
+    S, k1, V = v["target"].shape
+    t = {n: to_dev(v[n], dev) for n in ("target", "draft", "drafts", "u_acc", "u_fin")}
+    n_ref, tok_ref = q2v.pq_verify(t["target"], t["draft"], t["drafts"], t["u_acc"], t["u_fin"], v["T"])
+    n_acc = torch.full((S,), -7, dtype=torch.int32, device=dev)
+    toks = torch.full((S, k1), -7, dtype=torch.int32, device=dev)
+    assert _call_noalloc_c(lib, t, S, k1 - 1, V, v["T"], n_acc, toks, stream) == 0
+    torch.cuda.synchronize()
+    assert torch.equal(n_acc.cpu(), n_ref.cpu())
+    assert torch.equal(toks.cpu(), tok_ref.cpu())
+
+
 def test_noalloc_binding_and_bad_token(env):
     import torch
     dev, q2v, lib = env
