@@ -385,19 +385,22 @@ __device__ __forceinline__ void prep_row_bf16(const uint16_t *__restrict__ src, 
 // Two ways to share the range among the CTA's nw warps:
 //   strided (EVEN = false): warp w takes units u0 + w, u0 + w + nw, ...;
 //   even (EVEN = true): the range is flattened to tiles f = (u - u0) * ntk + tile and cut into
-//     nw contiguous warp ranges whose lengths differ by at most four tiles, so no warp has a
+//     nw contiguous warp ranges whose lengths differ by at most two tiles, so no warp has a
 //     whole unit more to stream than another.  A unit cut between warps is finished by the warp that
 //     began it: each later warp holding a piece of it leaves that piece's 16 x 8 partial sum in
 //     shared memory (its first piece, one slot per warp), and after one barrier the first warp
 //     adds them in warp order, so the result does not depend on timing.
-// Cuts fall on multiples of 4 tiles when ntk allows it: a 4-tile step is 384 bytes of every
-// row, so a cut never splits a 128-byte line between two warps (whose reads of it, far apart in
-// time, would each bring it from DRAM).
+// Cuts fall on multiples of 2 tiles when ntk allows it (192 bytes of every row).  A cut can
+// split a 128-byte line between two warps, whose reads of it, far apart in time, would each
+// bring it from DRAM; on single tiles that re-read 3% of the weights and was slower, on 4-tile
+// steps none, but at the verifier's MoE shape (~688 tiles over 24 warps) 4-tile steps leave the
+// busiest warp 32 tiles against 30: measured, gate+up took 54.9-55.4 us with 2-tile cuts,
+// 55.7-56.2 with 4-tile and 56.2-56.3 with 1-tile cuts.
 struct WarpTiles {
     int f0, f1;
 };
 __device__ __forceinline__ WarpTiles warp_tiles(int u0, int u1, int ntk, int nw, int w) {
-    const int G = (ntk & 3) == 0 ? 4 : 1;
+    const int G = (ntk & 1) == 0 ? 2 : 1;
     const long long Tg = (long long)(u1 - u0) * (ntk / G);
     return {(int)(Tg * w / nw) * G, (int)(Tg * (w + 1) / nw) * G};
 }
