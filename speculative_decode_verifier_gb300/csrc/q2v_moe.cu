@@ -439,9 +439,10 @@ __global__ void __launch_bounds__(256, 2) moe_stream_kernel(MoeArgs a, MoeWs w, 
 // over its warps by tiles, each warp streaming its 16 x 256 tiles through its own cp.async ring.
 // Compared with moe_stream_kernel there is no per-expert staging or barrier, and the smaller
 // register footprint leaves room for three times the warps per scheduler.  Measured at the
-// verifier shape (gate+up µs): even split, 24 warps, 3-tile rings: 56.4; even, 28 warps (at the
-// register limit, spilling): 64.3; even, 20 warps: 59.4; strided units, 28 x 3: 56.3 (24 x 3:
-// 57.8, 28 x 4: 57.9, 32 x 3: 59.9, 16 x 5: 62.5); moe_stream_kernel 60.0.
+// verifier shape (gate+up µs): even split, 24 warps, 3-tile rings: 55.4-55.6 (cuts on 2-tile
+// steps; 56.1-56.4 on 4-tile steps); even, 28 warps (at the register limit, spilling): 64.3;
+// even, 20 warps: 59.4; strided units, 28 x 3: 56.3 (24 x 3: 57.8, 28 x 4: 57.9, 32 x 3: 59.9,
+// 16 x 5: 62.5); moe_stream_kernel 60.0.
 constexpr int kGuWarps = 24;
 constexpr int kGuRing = 3;
 constexpr bool kGuEven = true;
