@@ -123,10 +123,13 @@ def test_scale_out_of_range_sets_status(env, N, K, row):
     assert q2v.q2_get_device_status(ws) == 0  # read clears it
 
 
-def test_deterministic_and_ldy(env):
+@pytest.mark.parametrize("N,K", [(4096, 4096), (40960, 4096)])  # per-CTA kernel; streaming kernel
+def test_deterministic_and_ldy(env, N, K):
+    """Repeated calls give the same bits (the streaming kernel sums the pieces of units cut between
+    warps in warp order), and a padded output (ldy > N) keeps its padding."""
     import torch
     dev, q2v, orc = env
-    g = synth.config_gemm(1, M=5)
+    g = synth.config_gemm(1, M=5, N=N, K=K)
     Wd = to_dev(g["W"].reshape(-1), dev)
     Ad = to_dev(g["A"], dev)
     Y1 = q2v.q2_tiny_gemm(Wd, g["N"], g["K"], Ad).cpu()
