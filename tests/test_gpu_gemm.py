@@ -55,6 +55,11 @@ def test_verifier_linear_config(env):
     (6, 4100, 4064),   # a ragged last 16-row group at the verifier width; 127 blocks (odd), a partial 16th tile
     (8, 4864, 1024),   # 8 rows in one activation slice, 304 row groups
     (5, 12288, 4096),  # Q, K and V of the verifier layer as one linear (768 CTAs: two waves)
+    (2, 38912, 512),   # the streaming kernel at every other row count: masked MMA columns
+    (3, 38912, 512),
+    (4, 38912, 512),
+    (6, 38912, 512),
+    (7, 38928, 512),   # and a unit count that is not a multiple of the SMs
     (5, 40960, 4096),  # the streaming kernel (many weight rows per SM): one session against a head
     (1, 65536, 256),   # streaming, one activation row, one K tile
     (8, 40000, 1024),  # streaming, all 8 columns of the MMA, units not a multiple of the warps

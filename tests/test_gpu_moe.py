@@ -60,6 +60,8 @@ def test_moe_config_full_size(env):
     dict(E=2, H=512, F=256, M=8, topk=2),      # top-k = E: every row routed to every expert
     dict(E=64, H=4096, F=2048, M=8, topk=6),   # 8 rows at full size: up to 48 active experts
     dict(E=64, H=768, F=1024, M=8, topk=8),    # streaming gate+up over 3-tile units (cuts on single tiles)
+    dict(E=64, H=256, F=2048, M=7, topk=8),    # streaming gate+up at 7 rows (masked MMA columns)
+    dict(E=64, H=256, F=4096, M=3, topk=6),    # streaming gate+up at 3 rows
 ])
 def test_shapes(env, over):
     m = synth.config_moe(2, salt=sum(over.values()), **over)
