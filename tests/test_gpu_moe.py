@@ -62,6 +62,8 @@ def test_moe_config_full_size(env):
     dict(E=64, H=768, F=1024, M=8, topk=8),    # streaming gate+up over 3-tile units (cuts on single tiles)
     dict(E=64, H=256, F=2048, M=7, topk=8),    # streaming gate+up at 7 rows (masked MMA columns)
     dict(E=64, H=256, F=4096, M=3, topk=6),    # streaming gate+up at 3 rows
+    dict(E=64, H=8192, F=256, M=3, topk=6),    # streaming down at 3 rows (windows of up to 6 pairs)
+    dict(E=64, H=1024, F=256, M=7, topk=8),    # streaming down at 7 rows (windows of up to 14 pairs)
 ])
 def test_shapes(env, over):
     m = synth.config_moe(2, salt=sum(over.values()), **over)
